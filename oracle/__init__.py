@@ -1,0 +1,249 @@
+"""fp64 CPU oracle for row-wise safe softmax -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The product
+path (``online_softmax_dispatcher_gb300``) never imports it and fails loudly
+when its CUDA library is missing.
+
+The arithmetic lives in ``softmax_oracle.c`` (plain C, binary64, compiled with
+``-ffp-contract=off`` so that x86 and Arm hosts round identically).  This
+module only builds that file and marshals numpy arrays into it:
+
+* ``softmax(x)``            -- the definition y = exp(x - max) / sum exp(x - max)
+                               in binary64 for fp32/fp16/bf16 input arrays
+                               ("[CUDA] safe online softmax", section 1,
+                               safe_softmax; HIP softmax tutorial, section 1).
+* ``softmax_f64(x)``        -- the same definition on a float64 array.
+* ``online_softmax_f64``    -- the chunked (m, d) form of "[CUDA] safe online
+                               softmax", section 1, safe_online_softmax.
+* ``decode`` / ``encode``   -- exact dtype -> binary64, and binary64 -> dtype
+                               with round-to-nearest-even from binary64.
+* ``check``                 -- streaming comparison of a candidate output with
+                               the definition, row by row, over OpenMP threads.
+
+bf16 arrays travel as ``numpy.uint16`` bit patterns (numpy has no bfloat16);
+fp16 arrays may be ``numpy.float16`` or ``numpy.uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+F32, F16, BF16 = 0, 1, 2
+DTYPE_NAMES = {F32: "fp32", F16: "fp16", BF16: "bf16"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "softmax_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+
+def build(force: bool = False, src: str = SOURCE, out: str = _LIB_PATH) -> str:
+    """Compile an oracle C source (by default softmax_oracle.c) into a shared library."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if (not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-fPIC", "-shared", "-Wall", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+class CheckResult(ctypes.Structure):
+    _fields_ = [
+        ("checked", ctypes.c_int64),
+        ("violations", ctypes.c_int64),
+        ("nonfinite", ctypes.c_int64),
+        ("first_bad", ctypes.c_int64),
+        ("max_rel", ctypes.c_double),
+        ("max_ulp", ctypes.c_int64),
+        ("max_rowsum_dev", ctypes.c_double),
+        ("rowsum_violations", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _as_bits(x: np.ndarray, dtype: int) -> np.ndarray:
+    """Contiguous storage of x in the oracle's layout for `dtype`."""
+    if dtype == F32:
+        if x.dtype != np.float32:
+            raise TypeError(f"fp32 input must be numpy.float32, got {x.dtype}")
+        return np.ascontiguousarray(x)
+    if x.dtype not in (np.uint16, np.float16):
+        raise TypeError(f"{DTYPE_NAMES[dtype]} input must be 16-bit, got {x.dtype}")
+    return np.ascontiguousarray(x).view(np.uint16)
+
+
+def dtype_of(x: np.ndarray) -> int:
+    if x.dtype == np.float32:
+        return F32
+    if x.dtype == np.float16:
+        return F16
+    raise TypeError("pass dtype= explicitly for uint16 (bf16 or fp16 bit patterns)")
+
+
+def _rows_cols(x: np.ndarray) -> tuple[int, int]:
+    if x.ndim == 1:
+        return 1, x.shape[0]
+    if x.ndim != 2:
+        raise ValueError("oracle works on [rows, cols] arrays")
+    return x.shape[0], x.shape[1]
+
+
+class Oracle:
+    """Marshalling around one build of the oracle C source."""
+
+    def __init__(self, path: str):
+        L = ctypes.CDLL(path)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+        L.oracle_f16_to_f64.restype = ctypes.c_double
+        L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        L.oracle_bf16_to_f64.restype = ctypes.c_double
+        L.oracle_f64_to_f16.argtypes = [ctypes.c_double]
+        L.oracle_f64_to_f16.restype = ctypes.c_uint16
+        L.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+        L.oracle_f64_to_bf16.restype = ctypes.c_uint16
+        L.oracle_decode.argtypes = [vp, i32, i64, vp]
+        L.oracle_encode.argtypes = [vp, i32, i64, vp]
+        L.oracle_softmax_f64.argtypes = [vp, i64, i64, vp]
+        L.oracle_softmax.argtypes = [vp, i32, i64, i64, vp]
+        L.oracle_online_softmax_f64.argtypes = [vp, i64, i64, i64, vp]
+        L.oracle_check.argtypes = [vp, vp, i32, i64, i64, vp, i64, ctypes.c_double,
+                                   ctypes.c_double, i64, ctypes.c_double, ctypes.c_double,
+                                   ctypes.POINTER(CheckResult)]
+        L.oracle_num_threads.argtypes = []
+        for name in ("oracle_decode", "oracle_encode", "oracle_softmax_f64", "oracle_softmax",
+                     "oracle_online_softmax_f64", "oracle_check", "oracle_num_threads"):
+            getattr(L, name).restype = ctypes.c_int
+        self.lib = L
+        self.path = path
+
+    def decode(self, x: np.ndarray, dtype: int | None = None) -> np.ndarray:
+        """Exact dtype -> binary64."""
+        dtype = dtype_of(x) if dtype is None else dtype
+        bits = _as_bits(x, dtype)
+        out = np.empty(bits.shape, dtype=np.float64)
+        rc = self.lib.oracle_decode(_ptr(bits), dtype, bits.size, _ptr(out))
+        assert rc == 0
+        return out
+
+    def encode(self, y: np.ndarray, dtype: int) -> np.ndarray:
+        """binary64 -> dtype (RNE from binary64).  fp16/bf16 come back as uint16 bits."""
+        y = np.ascontiguousarray(y, dtype=np.float64)
+        out = np.empty(y.shape, dtype=np.float32 if dtype == F32 else np.uint16)
+        rc = self.lib.oracle_encode(_ptr(y), dtype, y.size, _ptr(out))
+        assert rc == 0
+        return out
+
+    def softmax_f64(self, x: np.ndarray) -> np.ndarray:
+        """The definition on a float64 [rows, cols] array."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        rows, cols = _rows_cols(x)
+        y = np.empty_like(x)
+        rc = self.lib.oracle_softmax_f64(_ptr(x), rows, cols, _ptr(y))
+        assert rc == 0
+        return y
+
+    def softmax(self, x: np.ndarray, dtype: int | None = None) -> np.ndarray:
+        """The definition in binary64 on a dtype-typed [rows, cols] array."""
+        dtype = dtype_of(x) if dtype is None else dtype
+        bits = _as_bits(x, dtype)
+        rows, cols = _rows_cols(bits)
+        y = np.empty(bits.shape, dtype=np.float64)
+        rc = self.lib.oracle_softmax(_ptr(bits), dtype, rows, cols, _ptr(y))
+        assert rc == 0
+        return y
+
+    def softmax_rounded(self, x: np.ndarray, dtype: int | None = None) -> np.ndarray:
+        """The definition rounded once (RNE from binary64) to the input dtype."""
+        dtype = dtype_of(x) if dtype is None else dtype
+        return self.encode(self.softmax(x, dtype), dtype)
+
+    def online_softmax_f64(self, x: np.ndarray, chunk: int) -> np.ndarray:
+        """The chunked (m, d) form on a float64 [rows, cols] array."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        rows, cols = _rows_cols(x)
+        y = np.empty_like(x)
+        rc = self.lib.oracle_online_softmax_f64(_ptr(x), rows, cols, int(chunk), _ptr(y))
+        assert rc == 0
+        return y
+
+    def check(self, x: np.ndarray, y: np.ndarray, dtype: int, *, rel_tol: float = 0.0,
+              abs_floor: float = 0.0, max_ulp: int = 0, rowsum_a: float = 0.0,
+              rowsum_b: float = 0.0, rows_sel: np.ndarray | None = None) -> dict:
+        """Compare a candidate output y with the definition applied to x, row by row."""
+        xb = _as_bits(x, dtype)
+        yb = _as_bits(y, dtype)
+        if xb.shape != yb.shape:
+            raise ValueError(f"shape mismatch {xb.shape} vs {yb.shape}")
+        rows, cols = _rows_cols(xb)
+        res = CheckResult()
+        sel_ptr, n_sel = None, 0
+        if rows_sel is not None:
+            rows_sel = np.ascontiguousarray(rows_sel, dtype=np.int64)
+            sel_ptr, n_sel = _ptr(rows_sel), rows_sel.size
+        rc = self.lib.oracle_check(_ptr(xb), _ptr(yb), dtype, rows, cols, sel_ptr, n_sel,
+                                   float(rel_tol), float(abs_floor), int(max_ulp),
+                                   float(rowsum_a), float(rowsum_b), ctypes.byref(res))
+        if rc != 0:
+            raise ValueError("oracle_check rejected its arguments")
+        return res.as_dict()
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+
+def default() -> Oracle:
+    """The oracle built from softmax_oracle.c (built on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def decode(x, dtype=None):
+    return default().decode(x, dtype)
+
+
+def encode(y, dtype):
+    return default().encode(y, dtype)
+
+
+def softmax_f64(x):
+    return default().softmax_f64(x)
+
+
+def softmax(x, dtype=None):
+    return default().softmax(x, dtype)
+
+
+def softmax_rounded(x, dtype=None):
+    return default().softmax_rounded(x, dtype)
+
+
+def online_softmax_f64(x, chunk):
+    return default().online_softmax_f64(x, chunk)
+
+
+def check(x, y, dtype, **kw):
+    return default().check(x, y, dtype, **kw)
+
+
+def num_threads():
+    return default().num_threads()

@@ -1,0 +1,473 @@
+/*
+ * softmax_oracle.c -- the fp64 CPU oracle for row-wise safe softmax.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker, not the product: only
+ * tests/, __graft_entry__.smoke() and the cpu_baseline / reference legs of
+ * bench.py may load it.  It shares no code, header, table or constant with the
+ * CUDA library under online_softmax_dispatcher_gb300/csrc, and neither side
+ * includes or links the other.  The only agreement between the two is the
+ * numeric dtype code (0 = fp32, 1 = fp16, 2 = bf16), which is an interface.
+ *
+ * What it computes (plain definitions, written out; no blocking, fusion or
+ * reordering beyond what the definitions state):
+ *
+ *   safe softmax along the last dimension of a row-major [rows, cols] array,
+ *       m   = max_j x_j
+ *       s   = sum_j exp(x_j - m)
+ *       y_j = exp(x_j - m) / s
+ *   as stated in
+ *     - "[CUDA] safe online softmax" (wingedge777.com), section 1 "safe online
+ *       softmax", the safe_softmax listing (max, then exp(x - max), then divide
+ *       by the sum);
+ *     - the HIP softmax tutorial (forum.sourcefind.cn), section 1 "Softmax
+ *       operator definition", the numerically stable formula
+ *       y_i = e^(x_i - max(x)) / sum_j e^(x_j - max(x));
+ *     - "Softmax on DCU: from 2.34 ms to 0.62 ms" (czchanglian.com), section 1,
+ *       which motivates the max subtraction (exp overflows without it).
+ *   All arithmetic is IEEE binary64 in the C default rounding mode
+ *   (round-to-nearest-even).  The sum is Neumaier-compensated (Neumaier 1974),
+ *   so s carries far less than one fp32 ulp of error even for rows of 2^22
+ *   terms; x_j - m is exact in binary64 for fp16/bf16/fp32 inputs whose
+ *   exponents are within 2^52 of each other, which holds for every finite
+ *   input that does not underflow exp.
+ *
+ *   the chunked online softmax: the running pair (m, d) updated chunk by chunk,
+ *       m_new = max(m, max(chunk))
+ *       d     = d * exp(m - m_new) + sum_{j in chunk} exp(x_j - m_new)
+ *       m     = m_new
+ *   followed by y_j = exp(x_j - m) / d, as stated in "[CUDA] safe online
+ *   softmax", section 1, the safe_online_softmax listing (the per-element
+ *   form of the same update is section 4.3 of "Softmax on DCU").  It equals
+ *   the definition algebraically; the oracle keeps it as a self-check of the
+ *   (m, d) rescaling rule that the split-k and streaming kernels rely on.
+ *
+ *   dtype decode (fp16, bf16, fp32 -> binary64, exact) and encode (binary64
+ *   -> fp16 / bf16 / fp32, round to nearest, ties to even, straight from the
+ *   binary64 value with no intermediate fp32 rounding), written from the
+ *   IEEE 754-2008 binary16 layout and the bfloat16 layout (the top 16 bits of
+ *   a binary32).  Round-to-nearest-even output is what "Softmax on DCU"
+ *   section 4.5 and the "[CUDA] safe online softmax" kernels use when they
+ *   write half results.
+ *
+ * Non-finite inputs follow IEEE propagation through the definition above:
+ * a NaN anywhere in a row, a +inf in a row, or a row that is all -inf gives a
+ * NaN row; -inf entries in an otherwise finite row give exact zeros.
+ *
+ * Parity pins (tests/test_oracle_pins.py): the worked example of the HIP
+ * softmax tutorial, its printed 4-element output, closed forms (cols = 1,
+ * constant rows, the two-element logistic, a single planted peak), row sums,
+ * bitwise shift invariance on dyadic grids, online == direct, scipy's
+ * softmax on random rows, exhaustive fp16/bf16 decode against numpy / bit
+ * reinterpretation, and encode against ties constructed at every midpoint.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_F32 0
+#define ORACLE_F16 1
+#define ORACLE_BF16 2
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL (-1)
+
+/* ------------------------------------------------------------------------ */
+/* decode                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24); /* subnormal: f * 2^-24 */
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of a binary32 pattern. */
+double oracle_bf16_to_f64(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+double oracle_f32_to_f64(float f) { return (double)f; }
+
+/* ------------------------------------------------------------------------ */
+/* encode: round to nearest, ties to even, directly from binary64             */
+/* ------------------------------------------------------------------------ */
+
+/* Round a >= 0 to the nearest multiple of q (a power of two), ties to even
+ * multiple.  a / q is exact in binary64 because q is a power of two and the
+ * quotient stays in range for every case used below. */
+static double round_to_quantum(double a, double q)
+{
+    double n = a / q;
+    double r = floor(n);
+    double frac = n - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0))
+        r += 1.0;
+    return r * q;
+}
+
+/* Generic encoder for a binary format with `fbits` fraction bits, exponent
+ * bias `bias` and all-ones exponent `emax_field` reserved for inf/NaN.
+ * Returns the bit pattern in the low (1 + ebits + fbits) bits. */
+static uint32_t encode_binary(double v, int ebits, int fbits)
+{
+    int bias = (1 << (ebits - 1)) - 1;
+    int emax_field = (1 << ebits) - 1;
+    uint32_t sign = signbit(v) ? 1u : 0u;
+    uint32_t signbit_pos = (uint32_t)(ebits + fbits);
+    if (isnan(v))
+        return (sign << signbit_pos) | ((uint32_t)emax_field << fbits) | (1u << (fbits - 1));
+    double a = fabs(v);
+    /* largest finite value and the rounding threshold above which RNE gives inf */
+    double maxf = ldexp(2.0 - ldexp(1.0, -fbits), bias);
+    double ovf = ldexp(2.0 - ldexp(1.0, -fbits - 1), bias);
+    if (isinf(a) || a >= ovf)
+        return (sign << signbit_pos) | ((uint32_t)emax_field << fbits);
+    int min_exp = 1 - bias; /* exponent of the smallest normal */
+    double q;
+    if (a < ldexp(1.0, min_exp)) {
+        q = ldexp(1.0, min_exp - fbits); /* subnormal quantum */
+    } else {
+        int k;
+        frexp(a, &k); /* a = f * 2^k, f in [0.5, 1) */
+        q = ldexp(1.0, (k - 1) - fbits);
+    }
+    double R = round_to_quantum(a, q);
+    if (R > maxf) /* cannot happen below ovf, kept as a guard */
+        return (sign << signbit_pos) | ((uint32_t)emax_field << fbits);
+    uint32_t bits;
+    if (R < ldexp(1.0, min_exp)) {
+        /* subnormal (or zero): the fraction field counts quanta; a value that
+         * rounded up to exactly the smallest normal gives 1 << fbits, which is
+         * that normal's pattern. */
+        bits = (uint32_t)(R / ldexp(1.0, min_exp - fbits));
+    } else {
+        int k;
+        double f = frexp(R, &k);            /* R = f * 2^k, f in [0.5, 1) */
+        int E = k - 1;                      /* R = (2f) * 2^E, 2f in [1, 2) */
+        uint32_t frac = (uint32_t)((2.0 * f - 1.0) * ldexp(1.0, fbits));
+        bits = ((uint32_t)(E + bias) << fbits) | frac;
+    }
+    return (sign << signbit_pos) | bits;
+}
+
+uint16_t oracle_f64_to_f16(double v) { return (uint16_t)encode_binary(v, 5, 10); }
+uint16_t oracle_f64_to_bf16(double v) { return (uint16_t)encode_binary(v, 8, 7); }
+float oracle_f64_to_f32(double v) { return (float)v; /* C conversion: RNE */ }
+
+/* ------------------------------------------------------------------------ */
+/* bulk decode / encode                                                       */
+/* ------------------------------------------------------------------------ */
+
+static double decode_at(const void *x, int dtype, int64_t i)
+{
+    if (dtype == ORACLE_F32)
+        return (double)((const float *)x)[i];
+    if (dtype == ORACLE_F16)
+        return oracle_f16_to_f64(((const uint16_t *)x)[i]);
+    return oracle_bf16_to_f64(((const uint16_t *)x)[i]);
+}
+
+int oracle_decode(const void *x, int dtype, int64_t n, double *out)
+{
+    if (n < 0 || dtype < 0 || dtype > 2 || (n > 0 && (!x || !out)))
+        return ORACLE_EINVAL;
+    for (int64_t i = 0; i < n; i++)
+        out[i] = decode_at(x, dtype, i);
+    return ORACLE_OK;
+}
+
+int oracle_encode(const double *y, int dtype, int64_t n, void *out)
+{
+    if (n < 0 || dtype < 0 || dtype > 2 || (n > 0 && (!y || !out)))
+        return ORACLE_EINVAL;
+    for (int64_t i = 0; i < n; i++) {
+        if (dtype == ORACLE_F32)
+            ((float *)out)[i] = oracle_f64_to_f32(y[i]);
+        else if (dtype == ORACLE_F16)
+            ((uint16_t *)out)[i] = oracle_f64_to_f16(y[i]);
+        else
+            ((uint16_t *)out)[i] = oracle_f64_to_bf16(y[i]);
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* the definition                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* max over a row with NaN made sticky (a NaN input makes the row NaN). */
+static double row_max(const double *xr, int64_t cols)
+{
+    double m = -INFINITY;
+    for (int64_t j = 0; j < cols; j++) {
+        if (isnan(xr[j]))
+            return NAN;
+        if (xr[j] > m)
+            m = xr[j];
+    }
+    return m;
+}
+
+/* Neumaier's compensated sum of exp(x_j - m). */
+static double row_expsum(const double *xr, int64_t cols, double m)
+{
+    double s = 0.0, c = 0.0;
+    for (int64_t j = 0; j < cols; j++) {
+        double t = exp(xr[j] - m);
+        double u = s + t;
+        if (fabs(s) >= fabs(t))
+            c += (s - u) + t;
+        else
+            c += (t - u) + s;
+        s = u;
+    }
+    return s + c;
+}
+
+/* One row of the definition: m = max, s = sum exp(x - m), y = exp(x - m)/s. */
+static void softmax_row(const double *xr, int64_t cols, double *yr)
+{
+    double m = row_max(xr, cols);
+    double s = row_expsum(xr, cols, m);
+    for (int64_t j = 0; j < cols; j++)
+        yr[j] = exp(xr[j] - m) / s;
+}
+
+int oracle_softmax_f64(const double *x, int64_t rows, int64_t cols, double *y)
+{
+    if (rows < 0 || cols < 0 || (rows > 0 && cols > 0 && (!x || !y)))
+        return ORACLE_EINVAL;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++)
+        softmax_row(x + r * cols, cols, y + r * cols);
+    return ORACLE_OK;
+}
+
+/* decode a [rows, cols] array of `dtype` and apply the definition. */
+int oracle_softmax(const void *x, int dtype, int64_t rows, int64_t cols, double *y)
+{
+    if (rows < 0 || cols < 0 || dtype < 0 || dtype > 2 || (rows > 0 && cols > 0 && (!x || !y)))
+        return ORACLE_EINVAL;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *xs = (rows > 0 && cols > 0) ? (double *)malloc((size_t)cols * sizeof(double)) : NULL;
+        if (rows > 0 && cols > 0 && !xs) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < rows; r++) {
+            if (!xs)
+                continue;
+            for (int64_t j = 0; j < cols; j++)
+                xs[j] = decode_at(x, dtype, r * cols + j);
+            softmax_row(xs, cols, y + r * cols);
+        }
+        free(xs);
+    }
+    return failed ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* the chunked online form (self-check of the (m, d) rescaling rule)          */
+/* ------------------------------------------------------------------------ */
+
+int oracle_online_softmax_f64(const double *x, int64_t rows, int64_t cols, int64_t chunk, double *y)
+{
+    if (rows < 0 || cols < 0 || chunk <= 0 || (rows > 0 && cols > 0 && (!x || !y)))
+        return ORACLE_EINVAL;
+    for (int64_t r = 0; r < rows; r++) {
+        const double *xr = x + r * cols;
+        double m = -INFINITY, d = 0.0;
+        for (int64_t i = 0; i < cols; i += chunk) {
+            int64_t end = i + chunk < cols ? i + chunk : cols;
+            double m_local = row_max(xr + i, end - i);
+            double m_new = (isnan(m_local) || isnan(m)) ? NAN : (m_local > m ? m_local : m);
+            double d_local = row_expsum(xr + i, end - i, m_new);
+            /* scale of the history: exp(m - m_new); with no history (d == 0,
+             * m == -inf) the term is zero. */
+            double scale = (d == 0.0 && m == -INFINITY) ? 0.0 : exp(m - m_new);
+            d = d * scale + d_local;
+            m = m_new;
+        }
+        for (int64_t j = 0; j < cols; j++)
+            y[r * cols + j] = exp(xr[j] - m) / d;
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* streaming comparison of a candidate output against the definition         */
+/* ------------------------------------------------------------------------ */
+
+/* Per-call summary of oracle_check.  Counts are over the rows checked. */
+typedef struct {
+    int64_t checked;           /* elements compared */
+    int64_t violations;        /* elements outside the tolerance */
+    int64_t nonfinite;         /* inf / NaN outputs on rows whose input is finite */
+    int64_t first_bad;         /* flat index of the first violation, or -1 */
+    double max_rel;            /* fp32: max |y - y*| / y* over y* >= abs_floor */
+    int64_t max_ulp;           /* fp16 / bf16: max |bits(y) - bits(RNE(y*))| */
+    double max_rowsum_dev;     /* max |sum_j y_j - 1| over finite-input rows */
+    int64_t rowsum_violations; /* rows whose sum misses rowsum_a + cols * rowsum_b */
+} oracle_check_result;
+
+static int row_is_finite(const double *xr, int64_t cols)
+{
+    for (int64_t j = 0; j < cols; j++)
+        if (!isfinite(xr[j]))
+            return 0;
+    return 1;
+}
+
+/* Compare y (same dtype and layout as x) with the definition applied to x.
+ *   fp32:        |y - y*| <= rel_tol * y* + abs_floor
+ *   fp16, bf16:  |bits(y) - bits(RNE_dtype(y*))| <= max_ulp  (outputs are >= 0,
+ *                so the bit distance is the distance in ulps, subnormals and
+ *                zero included); a NaN matches only a NaN.
+ *   row sums:    |sum_j y_j - 1| <= rowsum_a + cols * rowsum_b on rows with
+ *                finite inputs, y_j decoded exactly and summed in binary64.
+ * rows_sel (length n_sel) picks rows to check; NULL checks all rows. */
+int oracle_check(const void *x, const void *y, int dtype, int64_t rows, int64_t cols,
+                 const int64_t *rows_sel, int64_t n_sel, double rel_tol, double abs_floor,
+                 int64_t max_ulp, double rowsum_a, double rowsum_b, oracle_check_result *res)
+{
+    if (!res || rows < 0 || cols < 0 || dtype < 0 || dtype > 2)
+        return ORACLE_EINVAL;
+    memset(res, 0, sizeof *res);
+    res->first_bad = -1;
+    if (rows == 0 || cols == 0)
+        return ORACLE_OK;
+    if (!x || !y)
+        return ORACLE_EINVAL;
+    int64_t n = rows_sel ? n_sel : rows;
+    for (int64_t i = 0; rows_sel && i < n; i++)
+        if (rows_sel[i] < 0 || rows_sel[i] >= rows)
+            return ORACLE_EINVAL;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *xs = (double *)malloc((size_t)cols * sizeof(double));
+        double *ys = (double *)malloc((size_t)cols * sizeof(double));
+        oracle_check_result loc;
+        memset(&loc, 0, sizeof loc);
+        loc.first_bad = -1;
+        if (!xs || !ys) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t i = 0; i < n; i++) {
+            if (!xs || !ys)
+                continue;
+            int64_t r = rows_sel ? rows_sel[i] : i;
+            for (int64_t j = 0; j < cols; j++)
+                xs[j] = decode_at(x, dtype, r * cols + j);
+            softmax_row(xs, cols, ys);
+            int finite_row = row_is_finite(xs, cols);
+            double s = 0.0, c = 0.0;
+            for (int64_t j = 0; j < cols; j++) {
+                int64_t flat = r * cols + j;
+                double want = ys[j];
+                double got = decode_at(y, dtype, flat);
+                int bad = 0;
+                if (finite_row && !isfinite(got))
+                    loc.nonfinite++;
+                if (dtype == ORACLE_F32) {
+                    if (isnan(want) || isnan(got)) {
+                        bad = !(isnan(want) && isnan(got));
+                    } else {
+                        double err = fabs(got - want);
+                        bad = !(err <= rel_tol * fabs(want) + abs_floor);
+                        if (fabs(want) >= abs_floor && want != 0.0 && err / fabs(want) > loc.max_rel)
+                            loc.max_rel = err / fabs(want);
+                    }
+                } else {
+                    uint16_t gb = ((const uint16_t *)y)[flat];
+                    uint16_t wb = dtype == ORACLE_F16 ? oracle_f64_to_f16(want) : oracle_f64_to_bf16(want);
+                    if (isnan(want) || isnan(got)) {
+                        bad = !(isnan(want) && isnan(got));
+                    } else if ((gb | wb) & 0x8000u) {
+                        bad = gb != wb; /* a negative output matches only exactly */
+                    } else {
+                        int64_t dist = gb > wb ? (int64_t)gb - wb : (int64_t)wb - gb;
+                        if (dist > loc.max_ulp)
+                            loc.max_ulp = dist;
+                        bad = dist > max_ulp;
+                    }
+                }
+                if (bad) {
+                    if (loc.first_bad < 0 || flat < loc.first_bad)
+                        loc.first_bad = flat;
+                    loc.violations++;
+                }
+                loc.checked++;
+                if (finite_row) {
+                    double u = s + got;
+                    if (fabs(s) >= fabs(got))
+                        c += (s - u) + got;
+                    else
+                        c += (got - u) + s;
+                    s = u;
+                }
+            }
+            if (finite_row) {
+                double dev = fabs((s + c) - 1.0);
+                if (!(dev <= rowsum_a + (double)cols * rowsum_b))
+                    loc.rowsum_violations++;
+                if (dev > loc.max_rowsum_dev || isnan(dev))
+                    loc.max_rowsum_dev = isnan(dev) ? INFINITY : dev;
+            }
+        }
+#pragma omp critical
+        {
+            res->checked += loc.checked;
+            res->violations += loc.violations;
+            res->nonfinite += loc.nonfinite;
+            res->rowsum_violations += loc.rowsum_violations;
+            if (loc.first_bad >= 0 && (res->first_bad < 0 || loc.first_bad < res->first_bad))
+                res->first_bad = loc.first_bad;
+            if (loc.max_rel > res->max_rel)
+                res->max_rel = loc.max_rel;
+            if (loc.max_ulp > res->max_ulp)
+                res->max_ulp = loc.max_ulp;
+            if (loc.max_rowsum_dev > res->max_rowsum_dev)
+                res->max_rowsum_dev = loc.max_rowsum_dev;
+        }
+        free(xs);
+        free(ys);
+    }
+    return failed ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/* Number of OpenMP threads a parallel region of the oracle uses (1 without
+ * OpenMP). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

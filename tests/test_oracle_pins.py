@@ -1,0 +1,343 @@
+"""Pins that tie the fp64 oracle to something other than itself.
+
+Each pin is a function of an ``oracle.Oracle`` so that the same pins also run
+against deliberately broken builds of the oracle source (``test_mutants_fail``):
+every plausible slip there (a flipped sign, a dropped term, a wrong bias, a
+tie rounded the wrong way, a swapped row) must trip at least one pin.
+
+What pins what:
+* the worked example of the HIP softmax tutorial, section 1, and its printed
+  run output, section 8 (tests/golden, values as printed on the page);
+* closed forms: cols = 1, constant rows (1/n), the two-element case
+  (scipy.special.expit), a single planted peak, and a sum whose small terms
+  vanish without compensation;
+* invariants: unit row sums, bitwise shift invariance on dyadic grids;
+* the chunked online form equals the direct definition;
+* scipy.special.softmax on random and brute-force enumerated rows;
+* dtype decode against numpy (fp16) and torch (bf16) on all 65536 patterns;
+* dtype encode against numpy (fp16, fp32) and against ties built at every
+  midpoint between consecutive fp16 / bf16 values;
+* the comparison helper against planted errors.
+"""
+import math
+import os
+import re
+import shutil
+import tempfile
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from oracle import BF16, F16, F32
+from tests.conftest import load_golden
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def _bf16_bits_from_f32(vals):
+    t = torch.tensor(np.asarray(vals, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _all_positive_finite(dtype):
+    """All positive finite bit patterns of a 16-bit dtype, ascending by value."""
+    if dtype == F16:
+        return np.arange(0x0000, 0x7C00, dtype=np.uint16)
+    return np.arange(0x0000, 0x7F80, dtype=np.uint16)
+
+
+# ----------------------------------------------------------------------------- pins
+
+
+def pin_worked_example(o):
+    g = load_golden("worked_example.txt")
+    d = int(g["decimals"])
+    x = np.array(g["x"], dtype=np.float64)
+    want = np.array(g["y"])
+    for y in (o.softmax_f64(x), o.softmax(x.astype(np.float32)), o.softmax(x.astype(np.float16))):
+        assert np.array_equal(np.round(y, d), want), y
+
+
+def pin_printed_output(o):
+    g = load_golden("printed_run_output.txt")
+    sig = int(g["significant"])
+    y = o.softmax_f64(np.array(g["x"]))
+    for got_row, want_row in zip(y, g["y"]):
+        for got, want in zip(got_row, want_row):
+            assert float(f"{got:.{sig}g}") == want, (got, want)
+
+
+def pin_cols_one(o):
+    x = np.array([[-200.0], [0.0], [3.5], [1e30]])
+    assert np.array_equal(o.softmax_f64(x), np.ones_like(x))
+    for dt, arr in ((F16, np.array([[7.0]], np.float16)), (F32, np.array([[-3.0]], np.float32))):
+        assert o.softmax(arr, dt)[0, 0] == 1.0
+
+
+def pin_constant_rows(o):
+    for n in (1, 2, 3, 7, 1000, 4096):
+        for c in (-200.0, 0.0, 1.0, 200.0):
+            y = o.softmax_f64(np.full((1, n), c))
+            assert np.allclose(y, 1.0 / n, rtol=1e-15, atol=0)
+
+
+def pin_two_element_logistic(o):
+    rng = np.random.default_rng(11)
+    a = rng.normal(0, 10, 200)
+    b = rng.normal(0, 10, 200)
+    y = o.softmax_f64(np.stack([a, b], axis=1))
+    assert np.allclose(y[:, 0], scipy.special.expit(a - b), rtol=1e-14, atol=1e-300)
+    assert np.allclose(y[:, 1], scipy.special.expit(b - a), rtol=1e-14, atol=1e-300)
+
+
+def pin_planted_peak(o):
+    # zeros everywhere except one entry of +30: y_peak = 1 / (1 + (n - 1) e^-30)
+    for n, pos in ((5, 0), (1000, 517), (32000, 31999)):
+        x = np.zeros((1, n))
+        x[0, pos] = 30.0
+        y = o.softmax_f64(x)
+        peak = 1.0 / (1.0 + (n - 1) * math.exp(-30.0))
+        rest = math.exp(-30.0) * peak
+        assert abs(y[0, pos] - peak) <= 1e-15 * peak
+        others = np.delete(y[0], pos)
+        assert np.allclose(others, rest, rtol=1e-14, atol=0)
+
+
+def pin_compensated_sum(o):
+    # one 0 and N entries of -40: y_0 = 1 / (1 + N e^-40).  N e^-40 ~ 4e-13 is made
+    # of terms far below half an ulp of 1, so only a compensated sum keeps it.
+    n = 100_000
+    x = np.full((1, n + 1), -40.0)
+    x[0, 0] = 0.0
+    y = o.softmax_f64(x)
+    want = 1.0 / (1.0 + n * math.exp(-40.0))
+    assert abs(y[0, 0] - want) <= 2e-16, (y[0, 0], want)
+
+
+def pin_row_sums(o):
+    rng = np.random.default_rng(12)
+    for dt, arr in ((F32, rng.normal(0, 5, (16, 999)).astype(np.float32)),
+                    (F16, rng.normal(0, 20, (16, 512)).astype(np.float16)),
+                    (BF16, _bf16_bits_from_f32(rng.normal(0, 4, (16, 3000))))):
+        y = o.softmax(arr, dt)
+        for row in y:
+            assert abs(math.fsum(row) - 1.0) <= 1e-14
+
+
+def pin_shift_invariance(o):
+    # fp16 multiples of 2^-4 with |x| < 32; x + 16 stays exact, so x - max is
+    # the same number and y must be bitwise identical.
+    rng = np.random.default_rng(13)
+    grid = rng.integers(-511, 512, size=(8, 300)) / 16.0
+    x = grid.astype(np.float16)
+    xs = (grid + 16.0).astype(np.float16)
+    assert np.array_equal(xs.astype(np.float64) - 16.0, grid)
+    assert np.array_equal(o.softmax(x, F16), o.softmax(xs, F16))
+    g32 = rng.integers(-2**20, 2**20, size=(4, 777)) / 1024.0
+    assert np.array_equal(o.softmax(g32.astype(np.float32), F32),
+                          o.softmax((g32 + 64.0).astype(np.float32), F32))
+
+
+def pin_online_equals_direct(o):
+    rng = np.random.default_rng(14)
+    x = rng.normal(0, 30, (5, 1000))
+    x[:, 13] = 250.0
+    direct = o.softmax_f64(x)
+    for chunk in (1, 7, 256, 1000):
+        online = o.online_softmax_f64(x, chunk)
+        assert np.allclose(online, direct, rtol=1e-14, atol=1e-300), chunk
+
+
+def pin_scipy_random(o):
+    rng = np.random.default_rng(15)
+    for scale, cols in ((1.0, 17), (20.0, 512), (200.0, 64), (1000.0, 9)):
+        x = rng.normal(0, scale, (32, cols))
+        want = scipy.special.softmax(x, axis=1)
+        got = o.softmax_f64(x)
+        assert np.allclose(got, want, rtol=1e-13, atol=1e-300)
+
+
+def pin_brute_force_tiny(o):
+    # every row of length 1..4 over a fixed value set, in each dtype
+    vals = [-200.0, -3.0, -1.0, 0.0, 0.5, 2.0, 3.0, 200.0]
+    for n in range(1, 5):
+        rows = np.array(np.meshgrid(*([vals] * n), indexing="ij")).reshape(n, -1).T
+        want = scipy.special.softmax(rows, axis=1)
+        for dt, arr in ((F32, rows.astype(np.float32)), (F16, rows.astype(np.float16)),
+                        (BF16, _bf16_bits_from_f32(rows))):
+            got = o.softmax(arr, dt)
+            assert np.allclose(got, want, rtol=1e-13, atol=1e-300)
+        assert np.array_equal(o.encode(want, F16), want.astype(np.float16).view(np.uint16))
+
+
+def pin_decode_f16_exhaustive(o):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = o.decode(bits, F16)
+    want = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def pin_decode_bf16_exhaustive(o):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = o.decode(bits, BF16)
+    want = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def pin_encode_f16_numpy(o):
+    rng = np.random.default_rng(16)
+    y = np.concatenate([rng.uniform(0, 1, 20000), rng.uniform(0, 7e4, 2000),
+                        np.exp(rng.uniform(-40, 0, 20000)), -rng.uniform(0, 1, 100),
+                        [0.0, -0.0, 65504.0, 65519.99, 65520.0, 1e9, np.inf, -np.inf]])
+    got = o.encode(y, F16)
+    with np.errstate(over="ignore"):
+        want = y.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def pin_encode_f32_numpy(o):
+    rng = np.random.default_rng(17)
+    y = np.concatenate([rng.uniform(0, 1, 5000), np.exp(rng.uniform(-110, 0, 5000)),
+                        [1e-45, 7e-46, 1.5e-45, 3.4028235677973366e38, 1e39]])
+    with np.errstate(over="ignore"):
+        want = y.astype(np.float32)
+    assert np.array_equal(o.encode(y, F32), want)
+
+
+def _encode_midpoints(o, dtype):
+    pos = _all_positive_finite(dtype)
+    v = o.decode(pos, dtype)
+    a, b = v[:-1], v[1:]
+    abits, bbits = pos[:-1], pos[1:]
+    mid = (a + b) / 2.0  # exact in binary64
+    even = np.where(abits % 2 == 0, abits, bbits)
+    lo = np.nextafter(mid, -np.inf)
+    hi = np.nextafter(mid, np.inf)
+    assert np.array_equal(o.encode(mid, dtype), even)
+    assert np.array_equal(o.encode(lo, dtype), abits)
+    assert np.array_equal(o.encode(hi, dtype), bbits)
+    assert np.array_equal(o.encode(a, dtype), abits)
+    # negatives mirror the positives with the sign bit set
+    assert np.array_equal(o.encode(-mid[1:], dtype), even[1:] | 0x8000)
+    # top of the range: the midpoint above the largest finite value rounds to inf
+    top = v[-1]
+    step = top - v[-2]
+    inf_bits = 0x7C00 if dtype == F16 else 0x7F80
+    assert o.encode(np.array([top + step / 2]), dtype)[0] == inf_bits
+    assert o.encode(np.array([np.nextafter(top + step / 2, 0)]), dtype)[0] == pos[-1]
+
+
+def pin_encode_f16_midpoints(o):
+    _encode_midpoints(o, F16)
+
+
+def pin_encode_bf16_midpoints(o):
+    _encode_midpoints(o, BF16)
+
+
+def pin_nonfinite(o):
+    x = np.array([[0.0, np.nan, 1.0], [0.0, np.inf, 1.0], [-np.inf, -np.inf, -np.inf],
+                  [-np.inf, 0.0, 0.0]])
+    y = o.softmax_f64(x)
+    assert np.isnan(y[0]).all() and np.isnan(y[1]).all() and np.isnan(y[2]).all()
+    assert np.array_equal(y[3], [0.0, 0.5, 0.5])
+
+
+def pin_check_helper(o):
+    rng = np.random.default_rng(18)
+    x = rng.normal(0, 3, (6, 40)).astype(np.float16)
+    ref = o.softmax_rounded(x, F16)
+    res = o.check(x, ref, F16, max_ulp=0, rowsum_a=2**-10, rowsum_b=2**-24)
+    assert res["violations"] == 0 and res["checked"] == x.size and res["rowsum_violations"] == 0
+    bad = ref.copy()
+    bad[3, 7] += 1
+    assert o.check(x, bad, F16, max_ulp=1)["violations"] == 0
+    r0 = o.check(x, bad, F16, max_ulp=0)
+    assert r0["violations"] == 1 and r0["first_bad"] == 3 * 40 + 7 and r0["max_ulp"] == 1
+    bad[1, 2] += 2
+    assert o.check(x, bad, F16, max_ulp=1)["first_bad"] == 1 * 40 + 2
+    x32 = rng.normal(0, 3, (3, 50)).astype(np.float32)
+    y32 = o.softmax(x32, F32).astype(np.float32)
+    assert o.check(x32, y32, F32, rel_tol=2e-6, abs_floor=2**-126)["violations"] == 0
+    y32[2, 5] *= 1 + 1e-5
+    r = o.check(x32, y32, F32, rel_tol=2e-6, abs_floor=2**-126)
+    assert r["violations"] == 1 and r["first_bad"] == 2 * 50 + 5
+    sel = o.check(x32, y32, F32, rel_tol=2e-6, abs_floor=2**-126, rows_sel=np.array([0, 1]))
+    assert sel["violations"] == 0 and sel["checked"] == 100
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(orc, pin):
+    pin(orc)
+
+
+# ----------------------------------------------------------------------------- mutants
+
+# (name, text in softmax_oracle.c, replacement).  Each is a plausible slip.
+MUTANTS = [
+    ("exp_sign_flipped", "yr[j] = exp(xr[j] - m) / s;", "yr[j] = exp(m - xr[j]) / s;"),
+    ("sum_drops_last_term", "static double row_expsum(const double *xr, int64_t cols, double m)\n{\n"
+     "    double s = 0.0, c = 0.0;\n    for (int64_t j = 0; j < cols; j++)",
+     "static double row_expsum(const double *xr, int64_t cols, double m)\n{\n"
+     "    double s = 0.0, c = 0.0;\n    for (int64_t j = 0; j < cols - 1; j++)"),
+    ("max_skips_first", "    double m = -INFINITY;\n    for (int64_t j = 0; j < cols; j++) {\n"
+     "        if (isnan(xr[j]))", "    double m = -INFINITY;\n    for (int64_t j = 1; j < cols; j++) {\n"
+     "        if (isnan(xr[j]))"),
+    ("compensation_sign", "            c += (s - u) + t;", "            c -= (s - u) + t;"),
+    ("no_compensation", "    return s + c;\n}\n\n/* One row", "    return s;\n}\n\n/* One row"),
+    ("ties_away", "(frac == 0.5 && fmod(r, 2.0) != 0.0)", "(frac == 0.5)"),
+    ("f16_bias", "e - 25); /* (1 + f/1024)", "e - 24); /* (1 + f/1024)"),
+    ("bf16_shift", "((uint32_t)b) << 16;", "((uint32_t)b) << 15;"),
+    ("online_no_rescale", "d = d * scale + d_local;", "d = d + d_local;"),
+    ("overflow_threshold", "if (isinf(a) || a >= ovf)", "if (isinf(a) || a > maxf)"),
+    ("row_swapped", "softmax_row(x + r * cols, cols, y + r * cols);",
+     "softmax_row(x + r * cols, cols, y + (rows - 1 - r) * cols);"),
+    ("check_off_by_one", "bad = dist > max_ulp;", "bad = dist > max_ulp + 1;"),
+    ("subnormal_quantum", "q = ldexp(1.0, min_exp - fbits); /* subnormal quantum */",
+     "q = ldexp(1.0, min_exp - fbits + 1); /* subnormal quantum */"),
+]
+
+
+@pytest.fixture(scope="module")
+def mutant_dir():
+    d = tempfile.mkdtemp(prefix="oracle_mutants_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutants_fail(mutant_dir, name, old, new):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique / missing"
+    path = os.path.join(mutant_dir, f"{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = oracle.build(force=True, src=path, out=os.path.join(mutant_dir, f"lib{name}.so"))
+    o = oracle.Oracle(lib)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
+
+
+def test_mutation_anchors_are_code():
+    # keep the anchors honest: none of them may sit inside a comment
+    src = open(oracle.SOURCE).read()
+    no_comments = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for name, old, _ in MUTANTS:
+        first = old.splitlines()[0].split("/*")[0].strip()
+        assert first in no_comments, name
