@@ -1,0 +1,423 @@
+"""Benchmark: row-wise softmax GB/s on one GB300 (and N replicas under torchrun).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one softmax pass over the whole workload batch (the default is the
+attention-score softmax [4, 32, 512, 512] fp16 = [65536, 512]).  The timed
+region is K steps bracketed by a barrier and torch.cuda.synchronize(),
+measured with CUDA events on the launching stream; consecutive steps rotate
+over input/output buffer sets that total more than twice the L2 size, so every
+step reads x from and writes y to HBM.  value = algorithmic bytes
+(rows * cols * (in + out dtype bytes)) / time, summed over ranks.
+
+Extra keys: `e2e` (the same metric through the public API with pinned host
+buffers, host->device copy of x and device->host copy of y inside the timed
+region), `roofline` (the dominant kernel's achieved bandwidth against the
+measured HBM copy peak), `latency_us` (median single-launch time, cold L2),
+`clocks` (nvidia-smi samples during the timed region), `cpu_baseline` (the
+fp64 oracle on the host's cores over a bounded sample, rank 0 only).
+
+--impl reference times the oracle itself on the host cores (the pages'
+method has no runnable reference implementation here) on the same config.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "softmax GB/s (read+write) and % of GB300 HBM peak; latency at [4,32,512,512] fp16"
+DEFAULT_WORKLOAD = "attn_fp16_65536x512"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+
+def dist_setup(n_gpus: int):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, ws, local
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    """Largest v over all ranks (every rank gets it)."""
+    if ws <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v: float, ws: int) -> float:
+    if ws <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, with host timestamps."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.t_start = time.time()
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu=timestamp,{self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_id:
+            cmd[1:1] = ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self) -> list[dict]:
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for rec in csv.reader(io.StringIO(out)):
+            if len(rec) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(rec[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + rec[0].strip().split(".")[1]) if "." in rec[0] else 0.0
+                rows.append({"t": ts + frac, "sm": float(rec[1]), "sm_max": float(rec[2]),
+                             "power": float(rec[3]) if rec[3].strip() not in ("[N/A]", "") else None,
+                             "hw_slowdown": "Active" in rec[5], "hw_thermal": "Active" in rec[6],
+                             "sw_thermal": "Active" in rec[7], "sw_power_cap": "Active" in rec[8]})
+            except (ValueError, IndexError):
+                continue
+        return rows
+
+
+def summarize_clocks(samples: list[dict], t0: float, t1: float) -> dict:
+    inside = [s for s in samples if t0 - 0.15 <= s["t"] <= t1 + 0.15]
+    if not inside and samples:
+        inside = [min(samples, key=lambda s: abs(s["t"] - (t0 + t1) / 2))]
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+    reasons = sorted({k for s in inside for k in ("hw_slowdown", "hw_thermal", "sw_thermal", "sw_power_cap") if s[k]})
+    return {"sm_mhz": statistics.median(s["sm"] for s in inside), "sm_max_mhz": max(s["sm_max"] for s in inside),
+            "reasons": reasons, "samples": len(inside)}
+
+
+def gpu_id_for_nvsmi() -> str | None:
+    import torch
+
+    try:
+        props = torch.cuda.get_device_properties(torch.cuda.current_device())
+        bus = getattr(props, "pci_bus_id", None)
+        dom = getattr(props, "pci_domain_id", None)
+        dev = getattr(props, "pci_device_id", None)
+        if bus is not None and dom is not None and dev is not None:
+            return f"{dom:08X}:{bus:02X}:{dev:02X}.0"
+    except Exception:  # noqa: BLE001 - best effort; fall back to the visible index
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    return vis.split(",")[torch.cuda.current_device()] if vis else None
+
+
+# ----------------------------------------------------------------------------- traffic record
+
+
+def kernel_fingerprint(variant: str) -> str:
+    """Hash of the sources the dominant kernel is built from (invalidates stale ncu traffic)."""
+    csrc = os.path.join(ROOT, "online_softmax_dispatcher_gb300", "csrc")
+    files = {"rowgroup": "k_rowgroup.cu", "block": "k_block.cu", "block_tma": "k_tma.cu",
+             "stream": "k_stream.cu", "splitk": "k_stream.cu"}
+    h = hashlib.sha256()
+    for name in (files.get(variant, ""), "common.cuh", "tma.cuh", "launch.h", "plan.cpp"):
+        p = os.path.join(csrc, name)
+        if name and os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, variant: str) -> tuple[float | None, str]:
+    """dram bytes per launch from a committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None, "no ncu record"
+    if not rec or rec.get("variant") != variant:
+        return None, "no ncu record for this kernel"
+    if rec.get("fingerprint") != kernel_fingerprint(variant):
+        return None, "kernel changed since the ncu capture"
+    return float(rec["dram_bytes_per_launch"]), rec.get("source", "")
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+
+def time_oracle(w, sample_rows: int, reps: int, budget_s: float) -> dict:
+    """The oracle (fp64, OpenMP over rows) on the first sample_rows rows."""
+    import oracle
+    from online_softmax_dispatcher_gb300 import workloads as W
+
+    x = W.generate(w, rows=sample_rows)
+    o = oracle.default()
+    o.softmax(x[: min(2, sample_rows)], w.dtype_code)  # warm
+    times = []
+    t_all = time.perf_counter()
+    for _ in range(reps):
+        t = time.perf_counter()
+        o.softmax(x, w.dtype_code)
+        times.append(time.perf_counter() - t)
+        if time.perf_counter() - t_all > budget_s:
+            break
+    per = statistics.median(times)
+    return {"value": w.bytes_moved(sample_rows) / per / 1e9, "unit": "GB/s", "cores": o.num_threads(),
+            "kind": "oracle", "sample": f"first {sample_rows} of {w.rows} rows, median of {len(times)} passes",
+            "seconds_per_pass": per, "passes": len(times)}
+
+
+def oracle_sample_rows(w, target_elems: int = 1 << 25) -> int:
+    return max(1, min(w.rows, target_elems // w.cols))
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+
+def run_ours(args, rank: int, ws: int) -> dict | None:
+    import torch
+
+    import online_softmax_dispatcher_gb300 as osd
+    from online_softmax_dispatcher_gb300 import workloads as W
+
+    w = W.WORKLOADS[args.workload]
+    dev = torch.device("cuda")
+    x_np = W.generate(w)
+    x_host = W.as_torch(x_np, w.dtype).pin_memory()
+    set_bytes = w.bytes_moved()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nbuf = max(2, -(-int(2.5 * l2) // set_bytes) + 1)
+    xs = [x_host.to(dev) for _ in range(nbuf)]
+    ys = [torch.empty_like(xs[0]) for _ in range(nbuf)]
+    plan = osd.plan_for(xs[0], ys[0])
+    variant = osd.softmax_variant_name(plan.variant)
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    rows, cols, dt = w.rows, w.cols, w.dtype_code
+    ptrs = [(a.data_ptr(), b.data_ptr()) for a, b in zip(xs, ys)]
+    fwd = osd.lib().softmax_fwd
+
+    def step(i):
+        xp, yp = ptrs[i % nbuf]
+        rc = fwd(xp, yp, rows, cols, dt, s)
+        if rc != 0:
+            raise osd.SoftmaxError(rc)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_id_for_nvsmi()).start() if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.3)
+    # ---- timed region: K steps
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, ws)
+    samples = sampler.stop() if sampler is not None else []
+    clocks = summarize_clocks(samples, t_host0, t_host1)
+
+    # ---- single-launch latency (cold: each launch on the next buffer set)
+    lat = []
+    for i in range(min(200, max(20, args.steps))):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step(i)
+        b.record(stream)
+        b.synchronize()
+        lat.append(a.elapsed_time(b) * 1e3)
+    latency_us = statistics.median(lat)
+
+    # ---- e2e through the public API: pinned host x -> device, softmax, device -> pinned host y
+    y_host = torch.empty_like(x_host).pin_memory()
+    ke = max(3, min(args.steps, 30))
+    for _ in range(2):
+        xs[0].copy_(x_host, non_blocking=True)
+        osd.softmax(xs[0], out=ys[0])
+        y_host.copy_(ys[0], non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(ke):
+        xs[0].copy_(x_host, non_blocking=True)
+        osd.softmax(xs[0], out=ys[0])
+        y_host.copy_(ys[0], non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / ke, ws)
+
+    total_bytes = sum_over_ranks(float(set_bytes) * args.steps, ws)
+    value = total_bytes / (ms_max / 1e3) / 1e9
+    peaks = load_peaks()
+    per_launch_ms = ms / args.steps
+    achieved = set_bytes / (per_launch_ms / 1e3) / 1e9
+    traffic, tsrc = recorded_traffic(w.name, variant)
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "about": w.about,
+                   "variant": variant, "plan": plan.as_dict(),
+                   "l2": f"rotating {nbuf} buffer sets, {nbuf * set_bytes / 2**20:.0f} MiB > 2x L2 "
+                         f"({l2 / 2**20:.0f} MiB)",
+                   "pct_of_peak": round(100 * value / ws / peaks["hbm_gbs"], 2),
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "latency_us": round(latency_us, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": f"{peaks['source']} hbm_gbs (copy of 1 Gi bf16)",
+                     "algorithmic_bytes_per_launch": set_bytes,
+                     "traffic": traffic, "traffic_source": tsrc},
+        "e2e": {"value": round(set_bytes / (e2e_ms / 1e3) / 1e9 * ws, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size(), "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = time_oracle(w, oracle_sample_rows(w), reps=5, budget_s=20.0)
+    return res if rank == 0 else None
+
+
+def run_reference(args, rank: int, ws: int) -> dict | None:
+    if rank != 0:
+        return None
+    from online_softmax_dispatcher_gb300 import workloads as W
+
+    w = W.WORKLOADS[args.workload]
+    rows = oracle_sample_rows(w, target_elems=1 << 23)
+    import oracle
+
+    x = W.generate(w, rows=rows)
+    o = oracle.default()
+    for _ in range(max(0, min(args.warmup, 3))):
+        o.softmax(x, w.dtype_code)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        o.softmax(x, w.dtype_code)
+    dt_s = (time.perf_counter() - t) / max(1, args.steps)
+    value = w.bytes_moved(rows) / dt_s / 1e9
+    sample = f"each step: first {rows} of {w.rows} rows of {w.name}"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt_s * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "about": w.about,
+                   "reference": "fp64 CPU oracle (OpenMP over rows) standing in for the pages' method"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, ws, _ = dist_setup(args.gpus)
+    if args.impl == "reference":
+        res = run_reference(args, rank, ws)
+    else:
+        import __graft_entry__
+
+        if rank == 0 or ws == 1:
+            __graft_entry__.build()
+        barrier(ws)
+        res = run_ours(args, rank, ws)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

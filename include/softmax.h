@@ -1,0 +1,209 @@
+/*
+ * softmax.h -- C ABI of libosd_softmax.so: row-wise safe softmax on one GB300
+ * (sm_103a) GPU.
+ *
+ * The operation (every entry point below computes it, or reports on it):
+ *
+ *     for each row r of a contiguous row-major [rows, cols] array x:
+ *         m    = max_j x[r, j]
+ *         d    = sum_j exp(x[r, j] - m)
+ *         y[r, j] = exp(x[r, j] - m) / d
+ *
+ * defined in "[CUDA] safe online softmax" (wingedge777.com), section 1 "safe
+ * online softmax" (the safe_softmax form: max, exp of the shifted values,
+ * divide by their sum), and in the HIP softmax tutorial (forum.sourcefind.cn),
+ * section 1 "Softmax operator definition", whose worked example maps
+ * [[1,2,3],[1,1,1]] to [[0.0900,0.2447,0.6652],[0.3333,0.3333,0.3333]].
+ * The max and the sum are accumulated in fp32 whatever the storage dtype
+ * ("Softmax on DCU: from 2.34 ms to 0.62 ms" (czchanglian.com), section 4.5:
+ * fp16 storage, fp32 accumulation), and y is rounded to nearest-even into the
+ * dtype of x.  Accuracy against the exact (binary64) result y*:
+ *     fp32        |y - y*| <= 2e-6 * y* + 2^-126
+ *     fp16, bf16  at most 1 ulp from y* rounded to the dtype
+ * with no inf or NaN for finite inputs.  Non-finite inputs propagate as IEEE
+ * arithmetic does: a NaN or +inf in a row, or a row of all -inf, gives a NaN
+ * row; -inf entries in an otherwise finite row give 0.
+ *
+ * Conventions shared by every entry point:
+ *   - x and y are DEVICE pointers to contiguous row-major [rows, cols] arrays
+ *     of the same dtype (row stride = cols elements).  The caller owns both;
+ *     the library never allocates, frees or copies between host and device.
+ *     Pointers must be aligned to the element size (4 bytes for fp32, 2 for
+ *     fp16 / bf16); 16-byte aligned rows take the vectorised fast path, any
+ *     other alignment is handled by peeling partial 16-byte chunks.
+ *   - x and y must not overlap (in-place is not supported).
+ *   - work is enqueued on `stream` (NULL = the legacy default stream) and the
+ *     call returns without synchronising.  Faults during execution surface at
+ *     the caller's next synchronisation, as for any CUDA launch.
+ *   - the current CUDA device is used; per-device attributes (SM count, shared
+ *     memory limit, cluster support) are read once per device and cached
+ *     (thread-safe).
+ *   - return value: SOFTMAX_OK (0) or a negative softmax_status.  Nothing
+ *     prints, throws or exits.
+ */
+#ifndef OSD_SOFTMAX_H
+#define OSD_SOFTMAX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *softmax_stream_t;
+
+/* Storage dtype of x and y. */
+typedef enum {
+    SOFTMAX_F32 = 0,
+    SOFTMAX_F16 = 1,
+    SOFTMAX_BF16 = 2
+} softmax_dtype;
+
+typedef enum {
+    SOFTMAX_OK = 0,
+    SOFTMAX_ERR_INVALID_ARG = -1,       /* null pointer with non-zero size, rows or cols < 0,
+                                           rows*cols*size overflows int64, misaligned pointer,
+                                           bad variant id, null out-pointer */
+    SOFTMAX_ERR_UNSUPPORTED_DTYPE = -2, /* dtype not in softmax_dtype */
+    SOFTMAX_ERR_ALIAS = -3,             /* x and y byte ranges overlap */
+    SOFTMAX_ERR_CUDA = -4,              /* a CUDA runtime call failed; see softmax_last_cuda_error */
+    SOFTMAX_ERR_UNSUPPORTED_SHAPE = -5, /* a forced variant cannot serve this shape / device */
+    SOFTMAX_ERR_DEVICE_TIMEOUT = -6     /* a bounded device-side wait gave up (see
+                                           softmax_get_device_error) */
+} softmax_status;
+
+/* Kernel variants the dispatcher chooses among. */
+typedef enum {
+    SOFTMAX_VARIANT_AUTO = 0,      /* let the dispatcher choose */
+    SOFTMAX_VARIANT_ROWGROUP = 1,  /* G = 1..32 lanes per row, row cached in registers */
+    SOFTMAX_VARIANT_BLOCK = 2,     /* one CTA per row, row cached in registers */
+    SOFTMAX_VARIANT_BLOCK_TMA = 3, /* persistent CTAs, rows staged in shared memory by bulk
+                                      async copies (TMA engine), one HBM read per element */
+    SOFTMAX_VARIANT_STREAM = 4,    /* one CTA per row, online (m, d) pass then a re-read pass;
+                                      any cols */
+    SOFTMAX_VARIANT_SPLITK = 5,    /* a thread-block cluster per row; partial (m, d) merged
+                                      through distributed shared memory */
+    SOFTMAX_VARIANT_COUNT = 6
+} softmax_variant;
+
+/*
+ * softmax_fwd -- y = softmax(x) along the last dimension.
+ *   x      device pointer, [rows, cols] of `dtype`, read only.
+ *   y      device pointer, [rows, cols] of `dtype`, written in full.
+ *   rows   number of rows (>= 0).  rows == 0 or cols == 0: SOFTMAX_OK, no launch.
+ *   cols   row length (>= 0).  cols == 1 gives y = 1.
+ *   dtype  softmax_dtype.
+ *   stream CUDA stream the work is enqueued on.
+ * Chooses a kernel from cols * sizeof(dtype), rows, the SM count and the
+ * 16-byte alignment of x, y and the row stride (the cols-based dispatch of the
+ * HIP softmax tutorial, section 7, rebuilt for this GPU), then issues exactly
+ * one kernel launch.
+ */
+int softmax_fwd(const void *x, void *y, int64_t rows, int64_t cols, int dtype,
+                softmax_stream_t stream);
+
+/*
+ * softmax_fwd_variant -- as softmax_fwd, with the kernel forced (for tests and
+ * benchmarks).  variant = SOFTMAX_VARIANT_AUTO behaves exactly like
+ * softmax_fwd.  Returns SOFTMAX_ERR_UNSUPPORTED_SHAPE when the forced variant
+ * cannot serve the shape on this device (e.g. a row too long to cache on
+ * chip for ROWGROUP / BLOCK / BLOCK_TMA, or no cluster launch for SPLITK).
+ */
+int softmax_fwd_variant(const void *x, void *y, int64_t rows, int64_t cols, int dtype,
+                        int variant, softmax_stream_t stream);
+
+/*
+ * softmax_query_variant -- the variant softmax_fwd would launch for these
+ * arguments on the current device, written to *variant.  Validates the
+ * arguments exactly as softmax_fwd does; launches nothing.
+ */
+int softmax_query_variant(const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
+                          int *variant);
+
+/* Device properties the dispatcher reads (one GPU). */
+typedef struct {
+    int sm_count;           /* multiprocessors */
+    int max_smem_optin;     /* max dynamic shared memory per block after opt-in, bytes */
+    int cluster_launch;     /* 1 if thread-block cluster launch is supported */
+    int l2_bytes;           /* L2 cache size, bytes */
+    int cc_major, cc_minor; /* compute capability */
+} softmax_device_info;
+
+/* A launch decision: which kernel, and its launch shape. */
+typedef struct {
+    int variant;            /* softmax_variant chosen (never AUTO) */
+    int lanes_per_row;      /* threads that share one row: ROWGROUP G (1..32); BLOCK_TMA
+                               32 x warps per row group (32..512); else 0 */
+    int chunks_per_thread;  /* 16-byte chunks each thread caches (ROWGROUP, BLOCK), or loads in
+                               flight per thread per streaming step (STREAM, SPLITK); else 0 */
+    int rows_per_tile;      /* BLOCK_TMA: consecutive rows moved by one bulk copy; else 0 */
+    int stages;             /* BLOCK_TMA: shared-memory tiles in flight per CTA; else 0 */
+    int block_threads;      /* threads per CTA */
+    int64_t grid_x;         /* CTAs along x */
+    int64_t grid_y;         /* CTAs along y (SPLITK: rows) */
+    int cluster_x;          /* SPLITK: CTAs per cluster (= per row); else 1 */
+    int smem_bytes;         /* dynamic shared memory per CTA (BLOCK_TMA: stages x stage bytes) */
+    int aligned;            /* 1 if every row of x and y starts 16-byte aligned and is a whole
+                               number of 16-byte chunks */
+    int y_vector;           /* 1 if y rows share x rows' 16-byte phase (vector stores) */
+} softmax_launch_plan;
+
+/*
+ * softmax_fwd_plan -- launch a caller-supplied plan (for tuning sweeps and
+ * benchmarks).  The plan is first checked against the shape, the pointers'
+ * alignment and the device: every field must describe a launch that covers
+ * each row exactly (e.g. lanes_per_row * chunks_per_thread >= the 16-byte
+ * chunks a row spans for ROWGROUP), `aligned` and `y_vector` must match the
+ * pointers, and a cluster must fit the device; otherwise
+ * SOFTMAX_ERR_INVALID_ARG and nothing is launched.  grid_x may be smaller than
+ * the number of rows (or row groups): the kernels loop over rows.
+ */
+int softmax_fwd_plan(const void *x, void *y, int64_t rows, int64_t cols, int dtype,
+                     const softmax_launch_plan *plan, softmax_stream_t stream);
+
+/*
+ * softmax_plan -- the dispatcher as a pure host function: the plan that
+ * softmax_fwd_variant would launch for these arguments on a device described
+ * by *dev.  x and y are only inspected for their addresses (alignment,
+ * overlap), never dereferenced, so host addresses may stand in for device
+ * ones.  Makes no CUDA call.
+ */
+int softmax_plan(const softmax_device_info *dev, const void *x, const void *y, int64_t rows,
+                 int64_t cols, int dtype, int variant, softmax_launch_plan *plan);
+
+/* softmax_device_query -- fill *dev for the current CUDA device (cached). */
+int softmax_device_query(softmax_device_info *dev);
+
+/*
+ * softmax_get_device_error -- read and clear the library's device-side error
+ * word on `stream` (the copy is ordered after work already enqueued there and
+ * the call synchronises that stream).  *code receives 0 when no kernel
+ * reported a problem since the last call, else a nonzero code whose low byte
+ * names the wait that gave up (1 = bulk-copy arrival, 2 = buffer release).
+ * Kernels that wait on an mbarrier bound the wait with %globaltimer; when it
+ * runs out they record the code here, drain their own copies in flight and
+ * return, so the context stays usable.  Returns SOFTMAX_ERR_DEVICE_TIMEOUT if
+ * *code is nonzero, SOFTMAX_OK otherwise, SOFTMAX_ERR_CUDA if the copy failed.
+ */
+int softmax_get_device_error(softmax_stream_t stream, unsigned int *code);
+
+/* softmax_last_cuda_error -- the cudaError_t of the last failing CUDA call made
+ * by this library on the calling thread (0 if none). */
+int softmax_last_cuda_error(void);
+
+/* softmax_strerror -- static description of a softmax_status. */
+const char *softmax_strerror(int status);
+
+/* softmax_variant_name -- static name of a softmax_variant ("auto", "rowgroup", ...). */
+const char *softmax_variant_name(int variant);
+
+/* softmax_abi_version -- bumped on any incompatible change of this header. */
+int softmax_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSD_SOFTMAX_H */

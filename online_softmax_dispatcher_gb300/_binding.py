@@ -1,0 +1,247 @@
+"""ctypes binding of libosd_softmax.so (C ABI: include/softmax.h).
+
+Argument marshalling only: every step of the softmax runs in the library's
+CUDA kernels.  The raw functions keep the C names and return the C status
+code; out-parameters come back as extra tuple members.  ``softmax`` is the
+torch convenience wrapper (torch supplies device memory and the stream).
+
+The library is loaded from the package's in-tree build directory.  If it is
+missing the import of any function raises ``SoftmaxLibraryMissing``: there is
+no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+F32, F16, BF16 = 0, 1, 2
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED_DTYPE = -2
+ERR_ALIAS = -3
+ERR_CUDA = -4
+ERR_UNSUPPORTED_SHAPE = -5
+ERR_DEVICE_TIMEOUT = -6
+
+VARIANT_AUTO = 0
+VARIANT_ROWGROUP = 1
+VARIANT_BLOCK = 2
+VARIANT_BLOCK_TMA = 3
+VARIANT_STREAM = 4
+VARIANT_SPLITK = 5
+VARIANT_COUNT = 6
+VARIANTS = {"auto": 0, "rowgroup": 1, "block": 2, "block_tma": 3, "stream": 4, "splitk": 5}
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libosd_softmax.so")
+
+# Exported symbols (kept equal to the declarations in include/softmax.h; a
+# host test checks both directions).
+EXPORTS = (
+    "softmax_fwd", "softmax_fwd_variant", "softmax_fwd_plan", "softmax_query_variant",
+    "softmax_plan", "softmax_device_query", "softmax_get_device_error",
+    "softmax_last_cuda_error", "softmax_strerror", "softmax_variant_name", "softmax_abi_version",
+)
+
+
+class SoftmaxLibraryMissing(RuntimeError):
+    pass
+
+
+class SoftmaxError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = f"softmax: {strerror(status)} (status {status})"
+        if status == ERR_CUDA:
+            msg += f", cudaError {softmax_last_cuda_error()}"
+        super().__init__(msg + (f": {what}" if what else ""))
+
+
+class DeviceInfo(ctypes.Structure):
+    _fields_ = [("sm_count", ctypes.c_int), ("max_smem_optin", ctypes.c_int),
+                ("cluster_launch", ctypes.c_int), ("l2_bytes", ctypes.c_int),
+                ("cc_major", ctypes.c_int), ("cc_minor", ctypes.c_int)]
+
+
+class LaunchPlan(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("lanes_per_row", ctypes.c_int),
+                ("chunks_per_thread", ctypes.c_int), ("rows_per_tile", ctypes.c_int),
+                ("stages", ctypes.c_int), ("block_threads", ctypes.c_int),
+                ("grid_x", ctypes.c_int64), ("grid_y", ctypes.c_int64), ("cluster_x", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("aligned", ctypes.c_int), ("y_vector", ctypes.c_int)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises SoftmaxLibraryMissing when it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise SoftmaxLibraryMissing(
+                    f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+                    "or `python online_softmax_dispatcher_gb300/build.py` (needs nvcc)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            sig = {
+                "softmax_fwd": [vp, vp, i64, i64, i32, vp],
+                "softmax_fwd_variant": [vp, vp, i64, i64, i32, i32, vp],
+                "softmax_fwd_plan": [vp, vp, i64, i64, i32, ctypes.POINTER(LaunchPlan), vp],
+                "softmax_query_variant": [vp, vp, i64, i64, i32, ctypes.POINTER(ctypes.c_int)],
+                "softmax_plan": [ctypes.POINTER(DeviceInfo), vp, vp, i64, i64, i32, i32,
+                                 ctypes.POINTER(LaunchPlan)],
+                "softmax_device_query": [ctypes.POINTER(DeviceInfo)],
+                "softmax_get_device_error": [vp, ctypes.POINTER(ctypes.c_uint)],
+                "softmax_last_cuda_error": [],
+                "softmax_strerror": [i32],
+                "softmax_variant_name": [i32],
+                "softmax_abi_version": [],
+            }
+            for name, args in sig.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = ctypes.c_int
+            L.softmax_strerror.restype = ctypes.c_char_p
+            L.softmax_variant_name.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+# ----------------------------------------------------------------------------- raw C entry points
+
+
+def softmax_fwd(x: int, y: int, rows: int, cols: int, dtype: int, stream: int = 0) -> int:
+    return lib().softmax_fwd(x, y, rows, cols, dtype, stream or None)
+
+
+def softmax_fwd_variant(x: int, y: int, rows: int, cols: int, dtype: int, variant: int,
+                        stream: int = 0) -> int:
+    return lib().softmax_fwd_variant(x, y, rows, cols, dtype, variant, stream or None)
+
+
+def softmax_fwd_plan(x: int, y: int, rows: int, cols: int, dtype: int, plan: LaunchPlan,
+                     stream: int = 0) -> int:
+    return lib().softmax_fwd_plan(x, y, rows, cols, dtype, ctypes.byref(plan), stream or None)
+
+
+def softmax_query_variant(x: int, y: int, rows: int, cols: int, dtype: int) -> tuple[int, int]:
+    v = ctypes.c_int(-1)
+    rc = lib().softmax_query_variant(x, y, rows, cols, dtype, ctypes.byref(v))
+    return rc, v.value
+
+
+def softmax_plan(dev: DeviceInfo, x: int, y: int, rows: int, cols: int, dtype: int,
+                 variant: int = VARIANT_AUTO) -> tuple[int, LaunchPlan]:
+    p = LaunchPlan()
+    rc = lib().softmax_plan(ctypes.byref(dev), x, y, rows, cols, dtype, variant, ctypes.byref(p))
+    return rc, p
+
+
+def softmax_device_query() -> tuple[int, DeviceInfo]:
+    d = DeviceInfo()
+    rc = lib().softmax_device_query(ctypes.byref(d))
+    return rc, d
+
+
+def softmax_get_device_error(stream: int = 0) -> tuple[int, int]:
+    code = ctypes.c_uint(0)
+    rc = lib().softmax_get_device_error(stream or None, ctypes.byref(code))
+    return rc, code.value
+
+
+def softmax_last_cuda_error() -> int:
+    return lib().softmax_last_cuda_error()
+
+
+def softmax_strerror(status: int) -> str:
+    return lib().softmax_strerror(status).decode()
+
+
+def softmax_variant_name(variant: int) -> str:
+    return lib().softmax_variant_name(variant).decode()
+
+
+def softmax_abi_version() -> int:
+    return lib().softmax_abi_version()
+
+
+def strerror(status: int) -> str:
+    try:
+        return softmax_strerror(status)
+    except SoftmaxLibraryMissing:
+        return f"status {status}"
+
+
+# ----------------------------------------------------------------------------- torch convenience
+
+_TORCH_DTYPES = None
+
+
+def dtype_code(t_dtype) -> int:
+    global _TORCH_DTYPES
+    if _TORCH_DTYPES is None:
+        import torch
+
+        _TORCH_DTYPES = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+    try:
+        return _TORCH_DTYPES[t_dtype]
+    except KeyError:
+        raise SoftmaxError(ERR_UNSUPPORTED_DTYPE, str(t_dtype)) from None
+
+
+def softmax(x, *, out=None, variant: int | str = VARIANT_AUTO, plan: LaunchPlan | None = None,
+            stream=None):
+    """y = softmax(x) over the last dimension of a contiguous CUDA tensor.
+
+    `out` (same shape and dtype, contiguous, not overlapping x) receives the
+    result when given; `variant` forces a kernel; `plan` launches a
+    caller-built plan; `stream` is a torch.cuda.Stream (default: current).
+    """
+    import torch
+
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise SoftmaxError(ERR_INVALID_ARG, "x must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise SoftmaxError(ERR_INVALID_ARG, "x must be contiguous")
+    if x.dim() == 0:
+        raise SoftmaxError(ERR_INVALID_ARG, "x must have at least one dimension")
+    dt = dtype_code(x.dtype)
+    y = torch.empty_like(x) if out is None else out
+    if y.shape != x.shape or y.dtype != x.dtype or not y.is_contiguous() or y.device != x.device:
+        raise SoftmaxError(ERR_INVALID_ARG, "out must match x in shape, dtype and device and be contiguous")
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
+    if isinstance(variant, str):
+        variant = VARIANTS[variant]
+    with torch.cuda.device(x.device):
+        if plan is not None:
+            rc = softmax_fwd_plan(x.data_ptr(), y.data_ptr(), rows, cols, dt, plan, s)
+        else:
+            rc = softmax_fwd_variant(x.data_ptr(), y.data_ptr(), rows, cols, dt, variant, s)
+    if rc != OK:
+        raise SoftmaxError(rc)
+    return y
+
+
+def plan_for(x, y, variant: int | str = VARIANT_AUTO) -> LaunchPlan:
+    """The plan the dispatcher picks for tensors x -> y on the current device."""
+    if isinstance(variant, str):
+        variant = VARIANTS[variant]
+    rc, dev = softmax_device_query()
+    if rc != OK:
+        raise SoftmaxError(rc)
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    rc, p = softmax_plan(dev, x.data_ptr(), y.data_ptr(), rows, cols, dtype_code(x.dtype), variant)
+    if rc != OK:
+        raise SoftmaxError(rc)
+    return p

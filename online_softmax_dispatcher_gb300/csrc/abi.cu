@@ -1,0 +1,263 @@
+// abi.cu -- the extern "C" entry points of libosd_softmax.so (declared and
+// documented in include/softmax.h): argument checks, the per-device attribute
+// cache, the dispatcher call and the single kernel launch.  No allocation, no
+// host<->device copy and no synchronisation on the launch path.
+#include <cuda_runtime.h>
+
+#include <functional>
+#include <mutex>
+
+#include "launch.h"
+#include "softmax.h"
+
+#define OSD_API extern "C" __attribute__((visibility("default")))
+
+namespace osd {
+
+// Device-side error word: kernels with bounded waits OR a code in here when a
+// wait gives up.  Its device address is looked up once per device and passed
+// to the kernels (separate translation units cannot name it directly).
+__device__ unsigned int g_device_error;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceCache {
+    std::once_flag once;
+    int status = SOFTMAX_OK;
+    softmax_device_info info = {};
+    unsigned int *error_word = nullptr;
+};
+
+DeviceCache g_devices[kMaxDevices];
+
+int cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = (int)e;
+    return SOFTMAX_ERR_CUDA;
+}
+
+void init_device(DeviceCache &c, int dev)
+{
+    int v = 0;
+    cudaError_t e;
+#define OSD_ATTR(field, attr)                                 \
+    e = cudaDeviceGetAttribute(&v, attr, dev);                \
+    if (e != cudaSuccess) {                                   \
+        c.status = cuda_fail(e);                              \
+        return;                                               \
+    }                                                         \
+    c.info.field = v;
+    OSD_ATTR(sm_count, cudaDevAttrMultiProcessorCount)
+    OSD_ATTR(max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin)
+    OSD_ATTR(cluster_launch, cudaDevAttrClusterLaunch)
+    OSD_ATTR(l2_bytes, cudaDevAttrL2CacheSize)
+    OSD_ATTR(cc_major, cudaDevAttrComputeCapabilityMajor)
+    OSD_ATTR(cc_minor, cudaDevAttrComputeCapabilityMinor)
+#undef OSD_ATTR
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) {
+        c.status = cuda_fail(e);
+        return;
+    }
+    c.error_word = static_cast<unsigned int *>(p);
+}
+
+int current_device(DeviceCache **out)
+{
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices)
+        return SOFTMAX_ERR_INVALID_ARG;
+    DeviceCache &c = g_devices[dev];
+    std::call_once(c.once, init_device, std::ref(c), dev);
+    if (c.status != SOFTMAX_OK)
+        return c.status;
+    *out = &c;
+    return SOFTMAX_OK;
+}
+
+int launch(const DeviceCache &dc, const void *x, void *y, int64_t rows, int64_t cols, int dtype,
+           const softmax_launch_plan &plan, softmax_stream_t stream)
+{
+    // every plan, the dispatcher's own included, is checked before it runs
+    const int rc = validate_plan(dc.info, x, y, rows, cols, dtype, plan);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    Launch l{x, y, rows, cols, dtype, plan, stream, dc.error_word};
+    int e;
+    switch (plan.variant) {
+    case SOFTMAX_VARIANT_ROWGROUP:
+        e = launch_rowgroup(l);
+        break;
+    case SOFTMAX_VARIANT_BLOCK:
+        e = launch_block(l);
+        break;
+    case SOFTMAX_VARIANT_BLOCK_TMA:
+        e = launch_block_tma(l);
+        break;
+    case SOFTMAX_VARIANT_STREAM:
+        e = launch_stream(l);
+        break;
+    case SOFTMAX_VARIANT_SPLITK:
+        e = launch_splitk(l);
+        break;
+    default:
+        return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (e != 0)
+        return cuda_fail((cudaError_t)e);
+    return SOFTMAX_OK;
+}
+
+}  // namespace
+}  // namespace osd
+
+using namespace osd;
+
+OSD_API int softmax_fwd_variant(const void *x, void *y, int64_t rows, int64_t cols, int dtype, int variant,
+                                softmax_stream_t stream)
+{
+    int rc = validate_args(x, y, rows, cols, dtype);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (variant < SOFTMAX_VARIANT_AUTO || variant >= SOFTMAX_VARIANT_COUNT)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    DeviceCache *dc = nullptr;
+    rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    softmax_launch_plan plan;
+    rc = softmax_plan(&dc->info, x, y, rows, cols, dtype, variant, &plan);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    return launch(*dc, x, y, rows, cols, dtype, plan, stream);
+}
+
+OSD_API int softmax_fwd(const void *x, void *y, int64_t rows, int64_t cols, int dtype, softmax_stream_t stream)
+{
+    return softmax_fwd_variant(x, y, rows, cols, dtype, SOFTMAX_VARIANT_AUTO, stream);
+}
+
+OSD_API int softmax_fwd_plan(const void *x, void *y, int64_t rows, int64_t cols, int dtype,
+                             const softmax_launch_plan *plan, softmax_stream_t stream)
+{
+    int rc = validate_args(x, y, rows, cols, dtype);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (!plan)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    DeviceCache *dc = nullptr;
+    rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    return launch(*dc, x, y, rows, cols, dtype, *plan, stream);
+}
+
+OSD_API int softmax_query_variant(const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
+                                  int *variant)
+{
+    if (!variant)
+        return SOFTMAX_ERR_INVALID_ARG;
+    int rc = validate_args(x, y, rows, cols, dtype);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    DeviceCache *dc = nullptr;
+    rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    softmax_launch_plan plan;
+    rc = softmax_plan(&dc->info, x, y, rows, cols, dtype, SOFTMAX_VARIANT_AUTO, &plan);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    *variant = plan.variant;
+    return SOFTMAX_OK;
+}
+
+OSD_API int softmax_device_query(softmax_device_info *dev)
+{
+    if (!dev)
+        return SOFTMAX_ERR_INVALID_ARG;
+    DeviceCache *dc = nullptr;
+    const int rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    *dev = dc->info;
+    return SOFTMAX_OK;
+}
+
+OSD_API int softmax_get_device_error(softmax_stream_t stream, unsigned int *code)
+{
+    if (!code)
+        return SOFTMAX_ERR_INVALID_ARG;
+    DeviceCache *dc = nullptr;
+    const int rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, dc->error_word, sizeof v, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(dc->error_word, 0, sizeof v, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    *code = v;
+    return v ? SOFTMAX_ERR_DEVICE_TIMEOUT : SOFTMAX_OK;
+}
+
+OSD_API int softmax_last_cuda_error(void) { return t_last_cuda_error; }
+
+OSD_API const char *softmax_strerror(int status)
+{
+    switch (status) {
+    case SOFTMAX_OK:
+        return "ok";
+    case SOFTMAX_ERR_INVALID_ARG:
+        return "invalid argument";
+    case SOFTMAX_ERR_UNSUPPORTED_DTYPE:
+        return "unsupported dtype";
+    case SOFTMAX_ERR_ALIAS:
+        return "x and y overlap";
+    case SOFTMAX_ERR_CUDA:
+        return "CUDA runtime error (see softmax_last_cuda_error)";
+    case SOFTMAX_ERR_UNSUPPORTED_SHAPE:
+        return "variant cannot serve this shape on this device";
+    case SOFTMAX_ERR_DEVICE_TIMEOUT:
+        return "a bounded device-side wait gave up";
+    default:
+        return "unknown status";
+    }
+}
+
+OSD_API const char *softmax_variant_name(int variant)
+{
+    switch (variant) {
+    case SOFTMAX_VARIANT_AUTO:
+        return "auto";
+    case SOFTMAX_VARIANT_ROWGROUP:
+        return "rowgroup";
+    case SOFTMAX_VARIANT_BLOCK:
+        return "block";
+    case SOFTMAX_VARIANT_BLOCK_TMA:
+        return "block_tma";
+    case SOFTMAX_VARIANT_STREAM:
+        return "stream";
+    case SOFTMAX_VARIANT_SPLITK:
+        return "splitk";
+    default:
+        return "unknown";
+    }
+}
+
+OSD_API int softmax_abi_version(void) { return 1; }

@@ -1,0 +1,454 @@
+// common.cuh -- device primitives shared by the softmax kernels (sm_103a).
+//
+// * 16-byte chunk I/O: every kernel moves a row as 16-byte chunks laid on the
+//   16-byte address grid.  A row whose start or end is not on that grid has a
+//   partial first / last chunk; those slots are read with scalar loads and the
+//   out-of-row slots are filled with -inf, which contributes exp(-inf) = 0
+//   (the vector-plus-scalar-edge technique of the InfiniTrain BF16 kernel PR,
+//   "AlignedVector" with an alignment check and a scalar tail, rebuilt as a
+//   per-row head/tail peel so that unaligned rows keep the vector body).
+// * dtype decode / RNE encode: fp32, fp16 (IEEE binary16), bf16.  Output
+//   rounding is round-to-nearest-even, as the half kernels of "[CUDA] safe
+//   online softmax" (section 2.1) and "Softmax on DCU" (section 4.5) do.
+// * exp: for fp16 / bf16 outputs exp(x - m) = 2^((x - m) * log2 e) on the SFU
+//   (ex2.approx, subnormal results kept: no .ftz); its ~2^-22 relative error is
+//   far below half an ulp of either 16-bit format.  For fp32 outputs the shift
+//   t = x - m is split exactly into t + r (Knuth's TwoSum) and
+//   exp(x - m) = expf(t) * (1 + r), which keeps the result within a few fp32
+//   ulps even when |x - m| is in the hundreds.
+// * sums: fp32 accumulation everywhere ("Softmax on DCU", section 4.5); for
+//   fp32 outputs the sum is a compensated (s, c) pair merged with TwoSum so a
+//   row of 2^22 terms stays within ~2 ulps.
+// * reductions: xor-butterfly warp shuffles ("[CUDA] safe online softmax",
+//   section 2.1.1) -- every lane ends with the identical value because each
+//   merge is commutative -- then one shared-memory slot per warp.
+// * (m, d) merge for the online form: m = max(m1, m2),
+//   d = d1 e^(m1 - m) + d2 e^(m2 - m) ("[CUDA] safe online softmax", section 1,
+//   safe_online_softmax, and its warp reduce in section 2.1).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+namespace osd {
+
+enum : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+template <int DT>
+struct Fmt;
+template <>
+struct Fmt<kF32> {
+    static constexpr int kBytes = 4;  // element size
+    static constexpr int kPerChunk = 4;  // elements per 16-byte chunk
+};
+template <>
+struct Fmt<kF16> {
+    static constexpr int kBytes = 2;
+    static constexpr int kPerChunk = 8;
+    static constexpr uint32_t kNegInf = 0xFC00u;
+};
+template <>
+struct Fmt<kBF16> {
+    static constexpr int kBytes = 2;
+    static constexpr int kPerChunk = 8;
+    static constexpr uint32_t kNegInf = 0xFF80u;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kNegInfF32 = 0xFF800000u;
+
+// ---------------------------------------------------------------- global memory
+
+// 16-byte read-only load, no L1 allocation (x is read once per pass).
+__device__ __forceinline__ uint4 ld_chunk(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_chunk(void *p, const uint4 &v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_u16(const void *p)
+{
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const void *p)
+{
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_u16(void *p, uint32_t v)
+{
+    asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"((unsigned short)v) : "memory");
+}
+
+__device__ __forceinline__ void st_u32(void *p, uint32_t v)
+{
+    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- decode / encode
+
+template <int DT>
+__device__ __forceinline__ void unpack(const uint4 &c, float (&f)[Fmt<DT>::kPerChunk])
+{
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    if constexpr (DT == kF32) {
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            f[i] = __uint_as_float(w[i]);
+    } else if constexpr (DT == kF16) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            __half2 h;
+            *reinterpret_cast<uint32_t *>(&h) = w[i];
+            const float2 p = __half22float2(h);
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+        }
+    } else {
+        // bf16 is the top half of an fp32 pattern: exact by shifting.
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack(const float (&f)[Fmt<DT>::kPerChunk])
+{
+    uint32_t w[4];
+    if constexpr (DT == kF32) {
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            w[i] = __float_as_uint(f[i]);
+    } else if constexpr (DT == kF16) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// A chunk whose every slot is -inf in the dtype.
+template <int DT>
+__device__ __forceinline__ uint4 neg_inf_chunk()
+{
+    if constexpr (DT == kF32) {
+        return make_uint4(kNegInfF32, kNegInfF32, kNegInfF32, kNegInfF32);
+    } else {
+        const uint32_t w = Fmt<DT>::kNegInf | (Fmt<DT>::kNegInf << 16);
+        return make_uint4(w, w, w, w);
+    }
+}
+
+// ---------------------------------------------------------------- row geometry
+
+// Where a row sits on the 16-byte grid.  Chunk k of the row covers element
+// indices [k * E - head, k * E - head + E); chunk 0 starts at `x0`.
+struct RowGeom {
+    const char *x0;   // 16-byte aligned address of chunk 0 of the x row
+    char *y0;         // same for y (meaningful when y rows share x rows' phase)
+    const char *xr;   // x row start
+    char *yr;         // y row start
+    int head;         // elements of chunk 0 that precede the row (0 when aligned)
+    int64_t nch;      // chunks covering the row
+};
+
+template <int DT, bool ALIGNED>
+__device__ __forceinline__ RowGeom row_geom(const char *x, char *y, int64_t r, int64_t cols)
+{
+    constexpr int S = Fmt<DT>::kBytes;
+    const int64_t row_bytes = cols * S;
+    RowGeom g;
+    g.xr = x + r * row_bytes;
+    g.yr = y + r * row_bytes;
+    if constexpr (ALIGNED) {
+        g.x0 = g.xr;
+        g.y0 = g.yr;
+        g.head = 0;
+        g.nch = row_bytes >> 4;
+    } else {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(g.xr);
+        const int lead = (int)(a & 15);
+        g.x0 = g.xr - lead;
+        g.y0 = g.yr - lead;
+        g.head = lead / S;
+        g.nch = (lead + row_bytes + 15) >> 4;
+    }
+    return g;
+}
+
+// Scalar read of the in-row slots of a partial chunk; other slots are -inf.
+template <int DT>
+__device__ __forceinline__ uint4 ld_partial(const char *xr, int64_t j0, int64_t cols)
+{
+    uint32_t w[4];
+    if constexpr (DT == kF32) {
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const int64_t j = j0 + e;
+            w[e] = (j >= 0 && j < cols) ? ld_u32(xr + 4 * j) : kNegInfF32;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int64_t j = j0 + 2 * i;
+            const uint32_t lo = (j >= 0 && j < cols) ? ld_u16(xr + 2 * j) : Fmt<DT>::kNegInf;
+            const uint32_t hi = (j + 1 >= 0 && j + 1 < cols) ? ld_u16(xr + 2 * (j + 1)) : Fmt<DT>::kNegInf;
+            w[i] = lo | (hi << 16);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Load chunk k of a row (k may be >= nch: then an all -inf chunk).
+template <int DT, bool ALIGNED>
+__device__ __forceinline__ uint4 load_chunk(const RowGeom &g, int64_t k, int64_t cols)
+{
+    constexpr int E = Fmt<DT>::kPerChunk;
+    if (k >= g.nch)
+        return neg_inf_chunk<DT>();
+    if constexpr (ALIGNED) {
+        return ld_chunk(g.x0 + 16 * k);
+    } else {
+        const int64_t j0 = k * E - g.head;
+        if (j0 >= 0 && j0 + E <= cols)
+            return ld_chunk(g.x0 + 16 * k);
+        return ld_partial<DT>(g.xr, j0, cols);
+    }
+}
+
+// Store chunk k (k < nch) of a row.  `y_vec` says that y rows sit on the same
+// 16-byte phase as x rows, so whole chunks go out as one 16-byte store; when
+// they do not, every element is stored on its own.
+template <int DT, bool ALIGNED>
+__device__ __forceinline__ void store_chunk(const RowGeom &g, int64_t k, int64_t cols, const uint4 &p,
+                                            bool y_vec)
+{
+    constexpr int E = Fmt<DT>::kPerChunk;
+    constexpr int S = Fmt<DT>::kBytes;
+    if constexpr (ALIGNED) {
+        st_chunk(g.y0 + 16 * k, p);
+    } else {
+        const int64_t j0 = k * E - g.head;
+        if (y_vec && j0 >= 0 && j0 + E <= cols) {
+            st_chunk(g.y0 + 16 * k, p);
+            return;
+        }
+        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            const int64_t j = j0 + e;
+            if (j >= 0 && j < cols) {
+                if constexpr (S == 4)
+                    st_u32(g.yr + 4 * j, w[e]);
+                else
+                    st_u16(g.yr + 2 * j, (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+            }
+        }
+    }
+}
+
+// Make the compiler treat a cached chunk as freshly defined, so that values
+// unpacked from it before this point are not kept alive in registers to be
+// reused after it (the chunk is cheaper to hold than its unpacked floats).
+__device__ __forceinline__ void opaque(uint4 &c)
+{
+    asm volatile("" : "+r"(c.x), "+r"(c.y), "+r"(c.z), "+r"(c.w));
+}
+
+// ---------------------------------------------------------------- exp and sums
+
+__device__ __forceinline__ float ex2_approx(float v)
+{
+    float r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Knuth's TwoSum: s + e == a + b exactly (no ordering requirement, symmetric in
+// a and b).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// Compensated sum: the value is s + c.
+struct CSum {
+    float s, c;
+};
+
+// Per-dtype arithmetic policy.  Acc is the running sum type.
+template <int DT>
+struct Math {
+    using Acc = float;
+    static __device__ __forceinline__ float exp_shift(float v, float m)
+    {
+        return ex2_approx((v - m) * kLog2e);
+    }
+    // exp(a) for a <= 0, used to rescale partial sums.
+    static __device__ __forceinline__ float exp_of(float a) { return ex2_approx(a * kLog2e); }
+    static __device__ __forceinline__ Acc zero() { return 0.f; }
+    static __device__ __forceinline__ void add(Acc &a, float v) { a += v; }
+    static __device__ __forceinline__ Acc merge(const Acc &a, const Acc &b) { return a + b; }
+    static __device__ __forceinline__ Acc scale(const Acc &a, float f) { return a * f; }
+    static __device__ __forceinline__ float value(const Acc &a) { return a; }
+    static __device__ __forceinline__ Acc shfl_xor(const Acc &a, int o)
+    {
+        return __shfl_xor_sync(0xFFFFFFFFu, a, o);
+    }
+};
+
+template <>
+struct Math<kF32> {
+    using Acc = CSum;
+    static __device__ __forceinline__ float exp_shift(float v, float m)
+    {
+        // t + r == v - m exactly; exp(v - m) = exp(t) * exp(r), exp(r) ~ 1 + r.
+        float t, r;
+        two_sum(v, -m, t, r);
+        const float e = expf(t);
+        return (fabsf(r) < INFINITY) ? fmaf(e, r, e) : e;
+    }
+    static __device__ __forceinline__ float exp_of(float a) { return expf(a); }
+    static __device__ __forceinline__ Acc zero() { return CSum{0.f, 0.f}; }
+    static __device__ __forceinline__ void add(Acc &a, float v)
+    {
+        float s, e;
+        two_sum(a.s, v, s, e);
+        a.s = s;
+        a.c += e;
+    }
+    static __device__ __forceinline__ Acc merge(const Acc &a, const Acc &b)
+    {
+        float s, e;
+        two_sum(a.s, b.s, s, e);
+        return CSum{s, (a.c + b.c) + e};
+    }
+    static __device__ __forceinline__ Acc scale(const Acc &a, float f) { return CSum{a.s * f, a.c * f}; }
+    static __device__ __forceinline__ float value(const Acc &a) { return a.s + a.c; }
+    static __device__ __forceinline__ Acc shfl_xor(const Acc &a, int o)
+    {
+        return CSum{__shfl_xor_sync(0xFFFFFFFFu, a.s, o), __shfl_xor_sync(0xFFFFFFFFu, a.c, o)};
+    }
+};
+
+// ---------------------------------------------------------------- warp / block reductions
+
+// Max over aligned groups of G lanes (xor butterfly; all 32 lanes must call).
+template <int G>
+__device__ __forceinline__ float group_max(float v)
+{
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+template <int DT, int G>
+__device__ __forceinline__ typename Math<DT>::Acc group_sum(typename Math<DT>::Acc a)
+{
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1)
+        a = Math<DT>::merge(a, Math<DT>::shfl_xor(a, o));
+    return a;
+}
+
+// Online (m, d) pair and its merge.  An empty side (m = -inf) contributes 0.
+struct MD {
+    float m, d;
+};
+
+template <int DT>
+__device__ __forceinline__ MD md_merge(const MD &a, const MD &b)
+{
+    const float m = fmaxf(a.m, b.m);
+    if (m == -INFINITY)
+        return MD{m, 0.f};
+    const float fa = (a.m == -INFINITY) ? 0.f : Math<DT>::exp_of(a.m - m);
+    const float fb = (b.m == -INFINITY) ? 0.f : Math<DT>::exp_of(b.m - m);
+    return MD{m, a.d * fa + b.d * fb};
+}
+
+template <int DT>
+__device__ __forceinline__ MD warp_md(MD v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        MD w{__shfl_xor_sync(0xFFFFFFFFu, v.m, o), __shfl_xor_sync(0xFFFFFFFFu, v.d, o)};
+        v = md_merge<DT>(v, w);
+    }
+    return v;
+}
+
+// Block-wide max; every thread gets the result.  `slots` holds >= 32 floats and
+// may be reused by the next reduction call (the leading barrier protects it).
+__device__ __forceinline__ float block_max(float v, float *slots)
+{
+    v = group_max<32>(v);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0)
+        slots[warp] = v;
+    __syncthreads();
+    v = lane < nw ? slots[lane] : -INFINITY;
+    return group_max<32>(v);
+}
+
+template <int DT>
+__device__ __forceinline__ typename Math<DT>::Acc block_sum(typename Math<DT>::Acc a,
+                                                            typename Math<DT>::Acc *slots)
+{
+    a = group_sum<DT, 32>(a);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0)
+        slots[warp] = a;
+    __syncthreads();
+    a = lane < nw ? slots[lane] : Math<DT>::zero();
+    return group_sum<DT, 32>(a);
+}
+
+template <int DT>
+__device__ __forceinline__ MD block_md(MD v, MD *slots)
+{
+    v = warp_md<DT>(v);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0)
+        slots[warp] = v;
+    __syncthreads();
+    v = lane < nw ? slots[lane] : MD{-INFINITY, 0.f};
+    return warp_md<DT>(v);
+}
+
+}  // namespace osd

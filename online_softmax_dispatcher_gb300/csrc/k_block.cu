@@ -1,0 +1,169 @@
+// k_block.cu -- one CTA per row, the row cached in registers: one HBM read and
+// one HBM write per element for rows of up to 512 threads x 16 chunks x 16 B
+// = 128 KiB.
+//
+// Prior art: the one-pass kernels of "[CUDA] safe online softmax", section 2
+// (fp16x8 register cache, 2.1; register + shared-memory cache, 2.2), written
+// for a 48 KB-per-block, 64K-register sm_120 part, and the block-per-row kernel
+// of the HIP softmax tutorial, section 3.  Differences here: any dtype and any
+// alignment (16-byte chunks with peeled partial edges), the CTA size is a
+// launch parameter (a multiple of 32 chosen by the dispatcher so that
+// threads x V just covers the row), the max is reduced before any exp so that
+// exp runs once per element (twice only when V * 8 > 32 floats would not fit
+// next to the cached chunks), and the reductions are shuffle butterflies with
+// one shared slot per warp ("Softmax on DCU", section 5.2: shuffles instead of
+// a shared-memory tree).
+#include "common.cuh"
+#include "launch.h"
+
+namespace osd {
+
+template <int DT, int V, bool ALIGNED>
+__global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
+    k_block(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int y_vec)
+{
+    using M = Math<DT>;
+    using Acc = typename M::Acc;
+    constexpr int E = Fmt<DT>::kPerChunk;
+    // keep e = exp(x - m) in registers when it fits, else recompute it
+    constexpr bool kKeepE = V * E <= 32;
+    __shared__ float smax[32];
+    __shared__ Acc ssum[32];
+    const int T = blockDim.x;
+    const int t = threadIdx.x;
+
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const RowGeom g = row_geom<DT, ALIGNED>(x, y, r, cols);
+        uint4 raw[V];
+#pragma unroll
+        for (int i = 0; i < V; i++)
+            raw[i] = load_chunk<DT, ALIGNED>(g, t + (int64_t)i * T, cols);
+
+        if constexpr (kKeepE) {
+            float v[V][E];
+            float m = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < V; i++) {
+                unpack<DT>(raw[i], v[i]);
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    m = fmaxf(m, v[i][e]);
+            }
+            m = block_max(m, smax);
+            Acc acc = M::zero();
+#pragma unroll
+            for (int i = 0; i < V; i++)
+#pragma unroll
+                for (int e = 0; e < E; e++) {
+                    v[i][e] = M::exp_shift(v[i][e], m);
+                    M::add(acc, v[i][e]);
+                }
+            acc = block_sum<DT>(acc, ssum);
+            const float inv = 1.0f / M::value(acc);
+#pragma unroll
+            for (int i = 0; i < V; i++) {
+                const int64_t k = t + (int64_t)i * T;
+                if (k < g.nch) {
+                    float o[E];
+#pragma unroll
+                    for (int e = 0; e < E; e++)
+                        o[e] = v[i][e] * inv;
+                    store_chunk<DT, ALIGNED>(g, k, cols, pack<DT>(o), y_vec != 0);
+                }
+            }
+        } else {
+            float m = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < V; i++) {
+                float f[E];
+                unpack<DT>(raw[i], f);
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    m = fmaxf(m, f[e]);
+            }
+            m = block_max(m, smax);
+#pragma unroll
+            for (int i = 0; i < V; i++)
+                opaque(raw[i]);
+            Acc acc = M::zero();
+#pragma unroll
+            for (int i = 0; i < V; i++) {
+                float f[E];
+                unpack<DT>(raw[i], f);
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    M::add(acc, M::exp_shift(f[e], m));
+            }
+            acc = block_sum<DT>(acc, ssum);
+            const float inv = 1.0f / M::value(acc);
+#pragma unroll
+            for (int i = 0; i < V; i++)
+                opaque(raw[i]);
+#pragma unroll
+            for (int i = 0; i < V; i++) {
+                const int64_t k = t + (int64_t)i * T;
+                if (k < g.nch) {
+                    float f[E];
+                    unpack<DT>(raw[i], f);
+#pragma unroll
+                    for (int e = 0; e < E; e++)
+                        f[e] = M::exp_shift(f[e], m) * inv;
+                    store_chunk<DT, ALIGNED>(g, k, cols, pack<DT>(f), y_vec != 0);
+                }
+            }
+        }
+    }
+}
+
+namespace {
+
+template <int DT, int V, bool A>
+int launch_one(const Launch &l)
+{
+    k_block<DT, V, A><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
+        (const char *)l.x, (char *)l.y, l.rows, l.cols, l.plan.y_vector);
+    return (int)cudaGetLastError();
+}
+
+template <int DT, int V>
+int launch_a(const Launch &l)
+{
+    return l.plan.aligned ? launch_one<DT, V, true>(l) : launch_one<DT, V, false>(l);
+}
+
+template <int DT>
+int launch_v(const Launch &l)
+{
+    switch (l.plan.chunks_per_thread) {
+    case 1:
+        return launch_a<DT, 1>(l);
+    case 2:
+        return launch_a<DT, 2>(l);
+    case 4:
+        return launch_a<DT, 4>(l);
+    case 8:
+        return launch_a<DT, 8>(l);
+    case 16:
+        return launch_a<DT, 16>(l);
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+int launch_block(const Launch &l)
+{
+    switch (l.dtype) {
+    case kF32:
+        return launch_v<kF32>(l);
+    case kF16:
+        return launch_v<kF16>(l);
+    case kBF16:
+        return launch_v<kBF16>(l);
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace osd

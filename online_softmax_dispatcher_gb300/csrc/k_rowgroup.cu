@@ -1,0 +1,181 @@
+// k_rowgroup.cu -- G lanes per row (G = 1, 2, ..., 32), the row cached in
+// registers, one HBM read and one HBM write per element.
+//
+// Prior art: the wavefront-per-row kernel of "Softmax on DCU", section 4.1
+// (one 64-lane wavefront per row, shuffle-reduced max), and the block-per-row
+// register-cached fp16x8 kernel of "[CUDA] safe online softmax", section 2.1.
+// On this GPU a row of up to 32 lanes x 32 floats is served by a group of
+// lanes of one 32-lane warp instead: short rows get G < 32 lanes (the HIP
+// softmax tutorial, section 5, likewise sizes its block to the next power of
+// two >= cols) so that a warp holds 32 / G rows and no lane idles; long rows
+// get a whole warp.
+//
+// Per row: the group's lanes load their 16-byte chunks (chunk k of the row goes
+// to lane k mod G), take the max with a G-lane xor butterfly, compute
+// e = exp(x - m) once per element and keep it in registers, butterfly-sum e,
+// then write e * (1 / d) as 16-byte stores.  Each group walks rows with a grid
+// stride and issues the loads of its next row before working on the current
+// one, so a row's HBM latency overlaps the previous row's arithmetic.
+#include "common.cuh"
+#include "launch.h"
+
+namespace osd {
+
+template <int DT, int G, int V, bool ALIGNED>
+__global__ void __launch_bounds__(kRowgroupThreads)
+    k_rowgroup(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int y_vec)
+{
+    using M = Math<DT>;
+    constexpr int E = Fmt<DT>::kPerChunk;
+    constexpr int kGroups = kRowgroupThreads / G;
+    const int gl = threadIdx.x & (G - 1);
+    const int64_t stride = (int64_t)gridDim.x * kGroups;
+    int64_t r = (int64_t)blockIdx.x * kGroups + threadIdx.x / G;
+    // every thread of a CTA runs the same number of iterations (the loop bound
+    // is the CTA's first row), so the butterflies see converged warps.
+    int64_t base = (int64_t)blockIdx.x * kGroups;
+
+    uint4 nxt[V];
+#pragma unroll
+    for (int i = 0; i < V; i++)
+        nxt[i] = neg_inf_chunk<DT>();
+    if (r < rows) {
+        const RowGeom g = row_geom<DT, ALIGNED>(x, y, r, cols);
+#pragma unroll
+        for (int i = 0; i < V; i++)
+            nxt[i] = load_chunk<DT, ALIGNED>(g, gl + i * G, cols);
+    }
+    for (; base < rows; base += stride, r += stride) {
+        uint4 cur[V];
+#pragma unroll
+        for (int i = 0; i < V; i++)
+            cur[i] = nxt[i];
+        const int64_t rn = r + stride;
+        if (rn < rows) {
+            const RowGeom gn = row_geom<DT, ALIGNED>(x, y, rn, cols);
+#pragma unroll
+            for (int i = 0; i < V; i++)
+                nxt[i] = load_chunk<DT, ALIGNED>(gn, gl + i * G, cols);
+        }
+        const bool valid = r < rows;
+
+        float v[V][E];
+#pragma unroll
+        for (int i = 0; i < V; i++)
+            unpack<DT>(cur[i], v[i]);
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < V; i++)
+#pragma unroll
+            for (int e = 0; e < E; e++)
+                m = fmaxf(m, v[i][e]);
+        m = group_max<G>(m);
+
+        typename M::Acc acc = M::zero();
+#pragma unroll
+        for (int i = 0; i < V; i++)
+#pragma unroll
+            for (int e = 0; e < E; e++) {
+                v[i][e] = M::exp_shift(v[i][e], m);
+                M::add(acc, v[i][e]);
+            }
+        acc = group_sum<DT, G>(acc);
+        const float inv = 1.0f / M::value(acc);
+
+        if (valid) {
+            const RowGeom g = row_geom<DT, ALIGNED>(x, y, r, cols);
+#pragma unroll
+            for (int i = 0; i < V; i++) {
+                const int64_t k = gl + i * G;
+                if (k < g.nch) {
+                    float o[E];
+#pragma unroll
+                    for (int e = 0; e < E; e++)
+                        o[e] = v[i][e] * inv;
+                    store_chunk<DT, ALIGNED>(g, k, cols, pack<DT>(o), y_vec != 0);
+                }
+            }
+        }
+    }
+}
+
+namespace {
+
+template <int DT, int G, int V, bool A>
+int launch_one(const Launch &l)
+{
+    k_rowgroup<DT, G, V, A><<<(unsigned)l.plan.grid_x, kRowgroupThreads, 0, (cudaStream_t)l.stream>>>(
+        (const char *)l.x, (char *)l.y, l.rows, l.cols, l.plan.y_vector);
+    return (int)cudaGetLastError();
+}
+
+template <int DT, int G, int V>
+int launch_a(const Launch &l)
+{
+    return l.plan.aligned ? launch_one<DT, G, V, true>(l) : launch_one<DT, G, V, false>(l);
+}
+
+// V chunks per lane; V * E <= 32 floats.
+template <int DT, int G>
+int launch_v(const Launch &l)
+{
+    constexpr int E = Fmt<DT>::kPerChunk;
+    switch (l.plan.chunks_per_thread) {
+    case 1:
+        return launch_a<DT, G, 1>(l);
+    case 2:
+        return launch_a<DT, G, 2>(l);
+    case 4:
+        return launch_a<DT, G, 4>(l);
+    case 8:
+        if constexpr (8 * E <= kRowgroupMaxFloats)
+            return launch_a<DT, G, 8>(l);
+        return (int)cudaErrorInvalidValue;
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+// Groups narrower than a warp only ever need one chunk per lane (the planner
+// widens G first), so only G = 32 is compiled with V > 1.
+template <int DT>
+int launch_g(const Launch &l)
+{
+    const int G = l.plan.lanes_per_row, V = l.plan.chunks_per_thread;
+    if (G < 32 && V != 1)
+        return (int)cudaErrorInvalidValue;
+    switch (G) {
+    case 1:
+        return launch_a<DT, 1, 1>(l);
+    case 2:
+        return launch_a<DT, 2, 1>(l);
+    case 4:
+        return launch_a<DT, 4, 1>(l);
+    case 8:
+        return launch_a<DT, 8, 1>(l);
+    case 16:
+        return launch_a<DT, 16, 1>(l);
+    case 32:
+        return launch_v<DT, 32>(l);
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+int launch_rowgroup(const Launch &l)
+{
+    switch (l.dtype) {
+    case kF32:
+        return launch_g<kF32>(l);
+    case kF16:
+        return launch_g<kF16>(l);
+    case kBF16:
+        return launch_g<kBF16>(l);
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace osd

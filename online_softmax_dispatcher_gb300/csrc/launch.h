@@ -1,0 +1,58 @@
+// launch.h -- host-side interface between the C ABI (abi.cu), the dispatcher
+// (plan.cpp) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <stdint.h>
+
+#include "softmax.h"
+
+struct CUstream_st;
+
+namespace osd {
+
+// Chunk counts and limits the dispatcher and the kernels agree on.
+constexpr int kRowgroupThreads = 256;   // CTA size of the lanes-per-row kernel
+constexpr int kRowgroupMaxFloats = 32;  // V * E cached per lane (registers)
+constexpr int kBlockMaxChunks = 16;     // V of the block-per-row kernel
+constexpr int kStreamThreads = 512;     // CTA size of the streaming and split-k kernels
+constexpr int kStreamUnroll = 8;        // 16-byte loads in flight per thread per step
+constexpr int kMaxCluster = 16;         // non-portable cluster size limit
+constexpr int kTmaConsumerWarps = 16;   // BLOCK_TMA: consumer warps per CTA
+constexpr int kTmaThreads = 32 * (1 + kTmaConsumerWarps);  // + one producer warp
+constexpr int kTmaMaxStagesHost = 8;    // BLOCK_TMA ring depth limit
+constexpr int kTmaStaticSmem = 4096;    // BLOCK_TMA static shared memory (barriers, slots), upper bound
+
+// Largest CTA size the block kernel is compiled for at a given V.  V >= 8 is
+// compiled for two resident CTAs per SM, so that one CTA's loads overlap the
+// other's reductions; the register file then bounds threads x registers.
+constexpr int block_max_threads_ct(int v) { return v >= 16 ? 256 : (v >= 8 ? 512 : 1024); }
+inline int block_max_threads(int v) { return block_max_threads_ct(v); }
+
+struct Launch {
+    const void *x;
+    void *y;
+    int64_t rows;
+    int64_t cols;
+    int dtype;
+    softmax_launch_plan plan;
+    CUstream_st *stream;
+    unsigned int *dev_err;  // device address of the library's error word
+};
+
+// Each returns the cudaError_t of its launch (0 = success).
+int launch_rowgroup(const Launch &l);
+int launch_block(const Launch &l);
+int launch_block_tma(const Launch &l);
+int launch_stream(const Launch &l);
+int launch_splitk(const Launch &l);
+
+// Validation shared by every entry point (no CUDA calls).
+int validate_args(const void *x, const void *y, int64_t rows, int64_t cols, int dtype);
+
+// Checks that a plan can serve this shape without any out-of-bounds access.
+int validate_plan(const softmax_device_info &dev, const void *x, const void *y, int64_t rows,
+                  int64_t cols, int dtype, const softmax_launch_plan &p);
+
+inline int dtype_bytes(int dtype) { return dtype == SOFTMAX_F32 ? 4 : 2; }
+
+}  // namespace osd

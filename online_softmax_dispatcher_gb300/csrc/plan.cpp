@@ -1,0 +1,348 @@
+// plan.cpp -- argument validation and the cols-based dispatcher, as pure host
+// code (no CUDA calls), so that it runs and is tested on a machine without a
+// GPU.
+//
+// The HIP softmax tutorial (forum.sourcefind.cn), section 7, switches on cols
+// alone (cols <= 4096: one block per row, else a multi-block pipeline), and
+// section 5 sizes the block from cols; "[CUDA] safe online softmax", sections
+// 4.2-4.3, measures that no single kernel wins everywhere and leaves the
+// choice open.  Here the choice is made on the 16-byte chunks a row spans
+// (cols * sizeof(dtype)), the row count against the SM count, and alignment:
+//
+//   row fits 32 lanes' registers      -> ROWGROUP   (G lanes per row, G = 1..32)
+//   few rows, long rows, clusters     -> SPLITK     (cluster of CTAs per row)
+//   two tiles of one row fit in smem  -> BLOCK_TMA  (bulk-copy staged row tiles)
+//   row fits one CTA's registers      -> BLOCK      (one CTA per row)
+//   otherwise                         -> SPLITK if rows < SMs, else STREAM
+#include <stdint.h>
+
+#include "launch.h"
+
+namespace osd {
+
+namespace {
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t next_pow2(int64_t v)
+{
+    int64_t p = 1;
+    while (p < v)
+        p <<= 1;
+    return p;
+}
+
+int64_t pow2_floor(int64_t v)
+{
+    int64_t p = 1;
+    while (p * 2 <= v)
+        p <<= 1;
+    return p;
+}
+
+struct Geometry {
+    int S;            // element bytes
+    int E;            // elements per 16-byte chunk
+    int64_t row_bytes;
+    bool aligned;     // every x and y row starts on the 16-byte grid and spans whole chunks
+    bool y_vec;       // y rows have the same 16-byte phase as x rows
+    int64_t nch_max;  // most 16-byte chunks any row spans
+};
+
+Geometry geometry(const void *x, const void *y, int64_t cols, int dtype)
+{
+    Geometry g;
+    g.S = dtype_bytes(dtype);
+    g.E = 16 / g.S;
+    g.row_bytes = cols * g.S;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
+    g.aligned = (xa % 16 == 0) && (ya % 16 == 0) && (g.row_bytes % 16 == 0);
+    g.y_vec = ((ya - xa) % 16) == 0;
+    // an unaligned row starts up to 16 - S bytes into its first chunk
+    g.nch_max = g.aligned ? g.row_bytes / 16 : ceil_div(g.row_bytes + 16 - g.S, 16);
+    return g;
+}
+
+bool rowgroup_fits(const Geometry &g) { return g.nch_max <= 32 * (kRowgroupMaxFloats / g.E); }
+
+bool block_fits(const Geometry &g) { return g.nch_max <= int64_t(block_max_threads(kBlockMaxChunks)) * kBlockMaxChunks; }
+
+void plan_rowgroup(const Geometry &g, int64_t rows, softmax_launch_plan &p)
+{
+    const int64_t lanes = next_pow2(g.nch_max);
+    const int G = (int)(lanes < 32 ? lanes : 32);
+    const int V = (int)next_pow2(ceil_div(g.nch_max, G));
+    p.variant = SOFTMAX_VARIANT_ROWGROUP;
+    p.lanes_per_row = G;
+    p.chunks_per_thread = V;
+    p.block_threads = kRowgroupThreads;
+    const int64_t groups = kRowgroupThreads / G;
+    const int64_t ctas = ceil_div(rows, groups);
+    p.grid_x = ctas < INT32_MAX ? ctas : INT32_MAX;
+}
+
+void plan_block(const Geometry &g, int64_t rows, softmax_launch_plan &p)
+{
+    // Smallest V (>= 4, to keep several 16-byte loads in flight per thread)
+    // whose CTA stays within 512 threads (V = 16: the 256 it is compiled for),
+    // so that at least two CTAs -- two rows -- are resident per SM.
+    int V = 4;
+    while (V < kBlockMaxChunks && ceil_div(g.nch_max, V) > (V * 2 > kBlockMaxChunks ? 256 : 512))
+        V *= 2;
+    int64_t threads = ceil_div(ceil_div(g.nch_max, V), 32) * 32;
+    if (threads < 64)
+        threads = 64;
+    p.variant = SOFTMAX_VARIANT_BLOCK;
+    p.chunks_per_thread = V;
+    p.block_threads = (int)threads;
+    p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
+}
+
+// Bytes of shared memory one BLOCK_TMA tile of R rows needs: the 16-byte
+// chunks it spans from the aligned address below its start, rounded to 128.
+int64_t tma_stage_bytes(const Geometry &g, int64_t R)
+{
+    const int64_t lead_max = g.aligned ? 0 : 16 - g.S;
+    const int64_t chunks = ceil_div(lead_max + R * g.row_bytes, 16);
+    return ceil_div(chunks * 16, 128) * 128;
+}
+
+int tma_budget(const softmax_device_info &dev) { return dev.max_smem_optin - kTmaStaticSmem; }
+
+// BLOCK_TMA shape: about 32 KB per tile; rows of 32 KB and more get a tile of
+// their own and all 16 consumer warps; shorter rows share a tile, and the
+// consumer warps split into row groups (one warp per row below 2 KB).
+bool plan_tma(const Geometry &g, int64_t rows, const softmax_device_info &dev, softmax_launch_plan &p)
+{
+    const int64_t target = 32 * 1024;
+    int64_t R = 1, W = kTmaConsumerWarps;
+    if (g.row_bytes < target) {
+        R = pow2_floor(target / g.row_bytes);
+        if (R > 256)
+            R = 256;
+        W = kTmaConsumerWarps / (R < kTmaConsumerWarps ? R : kTmaConsumerWarps);
+    }
+    if (R > rows)
+        R = next_pow2(rows);
+    int64_t stage = tma_stage_bytes(g, R);
+    int64_t stages = tma_budget(dev) / stage;
+    if (stages > kTmaMaxStagesHost)
+        stages = kTmaMaxStagesHost;
+    if (stages < 2)
+        return false;
+    const int64_t tiles = ceil_div(rows, R);
+    p.variant = SOFTMAX_VARIANT_BLOCK_TMA;
+    p.lanes_per_row = (int)(32 * W);
+    p.rows_per_tile = (int)R;
+    p.stages = (int)stages;
+    p.smem_bytes = (int)(stages * stage);
+    p.block_threads = kTmaThreads;
+    p.grid_x = tiles < dev.sm_count ? tiles : dev.sm_count;
+    return true;
+}
+
+bool tma_fits(const Geometry &g, const softmax_device_info &dev)
+{
+    return tma_stage_bytes(g, 1) * 2 <= tma_budget(dev);
+}
+
+void plan_stream(int64_t rows, softmax_launch_plan &p)
+{
+    p.variant = SOFTMAX_VARIANT_STREAM;
+    p.chunks_per_thread = kStreamUnroll;
+    p.block_threads = kStreamThreads;
+    p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
+}
+
+// Cluster size: enough CTAs to cover the SMs, at most 16, and at least two
+// full streaming steps of work per CTA.
+int splitk_cluster(const Geometry &g, int64_t rows, const softmax_device_info &dev)
+{
+    int64_t c = pow2_floor(dev.sm_count / (rows > 0 ? rows : 1));
+    const int64_t by_work = pow2_floor(g.nch_max / (2 * int64_t(kStreamThreads) * kStreamUnroll));
+    if (c > by_work)
+        c = by_work;
+    if (c > kMaxCluster)
+        c = kMaxCluster;
+    if (c < 1)
+        c = 1;
+    return (int)c;
+}
+
+void plan_splitk(const Geometry &g, int64_t rows, const softmax_device_info &dev, softmax_launch_plan &p)
+{
+    const int c = splitk_cluster(g, rows, dev);
+    p.variant = SOFTMAX_VARIANT_SPLITK;
+    p.chunks_per_thread = kStreamUnroll;
+    p.block_threads = kStreamThreads;
+    p.cluster_x = c;
+    p.grid_x = c;
+    p.grid_y = rows;
+}
+
+bool splitk_possible(int64_t rows, const softmax_device_info &dev)
+{
+    return dev.cluster_launch && rows >= 1 && rows <= 65535;
+}
+
+}  // namespace
+
+int validate_args(const void *x, const void *y, int64_t rows, int64_t cols, int dtype)
+{
+    if (dtype < SOFTMAX_F32 || dtype > SOFTMAX_BF16)
+        return SOFTMAX_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || cols < 0)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    if (!x || !y)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int64_t S = dtype_bytes(dtype);
+    if (cols > INT64_MAX / S || rows > INT64_MAX / (cols * S))
+        return SOFTMAX_ERR_INVALID_ARG;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
+    if (xa % S || ya % S)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const uint64_t bytes = (uint64_t)(rows * cols * S);
+    const uint64_t gap = xa <= ya ? (uint64_t)(ya - xa) : (uint64_t)(xa - ya);
+    if (gap < bytes)
+        return SOFTMAX_ERR_ALIAS;
+    return SOFTMAX_OK;
+}
+
+int validate_plan(const softmax_device_info &dev, const void *x, const void *y, int64_t rows,
+                  int64_t cols, int dtype, const softmax_launch_plan &p)
+{
+    const Geometry g = geometry(x, y, cols, dtype);
+    if ((p.aligned != 0) != g.aligned || (p.y_vector != 0) != g.y_vec)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (p.block_threads < 32 || p.block_threads % 32 || p.block_threads > 1024)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (p.grid_x < 1 || p.grid_x > INT32_MAX || p.smem_bytes < 0)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int V = p.chunks_per_thread;
+    switch (p.variant) {
+    case SOFTMAX_VARIANT_ROWGROUP: {
+        const int G = p.lanes_per_row;
+        if (G < 1 || G > 32 || (G & (G - 1)) || V < 1 || V > 8 || (V & (V - 1)))
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (V * g.E > kRowgroupMaxFloats || int64_t(G) * V < g.nch_max || (G < 32 && V != 1))
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.block_threads != kRowgroupThreads || p.grid_y != 1 || p.cluster_x != 1)
+            return SOFTMAX_ERR_INVALID_ARG;
+        return SOFTMAX_OK;
+    }
+    case SOFTMAX_VARIANT_BLOCK:
+        if (V < 1 || V > kBlockMaxChunks || (V & (V - 1)))
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.block_threads > block_max_threads(V) || int64_t(p.block_threads) * V < g.nch_max)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.grid_y != 1 || p.cluster_x != 1)
+            return SOFTMAX_ERR_INVALID_ARG;
+        return SOFTMAX_OK;
+    case SOFTMAX_VARIANT_BLOCK_TMA: {
+        const int W = p.lanes_per_row / 32;
+        if (p.lanes_per_row % 32 || W < 1 || W > kTmaConsumerWarps || (W & (W - 1)))
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.block_threads != kTmaThreads || p.grid_y != 1 || p.cluster_x != 1)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.rows_per_tile < 1 || p.stages < 2 || p.stages > kTmaMaxStagesHost)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.smem_bytes % p.stages || (p.smem_bytes / p.stages) % 128 || p.smem_bytes > tma_budget(dev))
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.smem_bytes / p.stages < tma_stage_bytes(g, p.rows_per_tile))
+            return SOFTMAX_ERR_INVALID_ARG;
+        return SOFTMAX_OK;
+    }
+    case SOFTMAX_VARIANT_STREAM:
+        if (V != kStreamUnroll || p.block_threads > kStreamThreads || p.grid_y != 1 || p.cluster_x != 1)
+            return SOFTMAX_ERR_INVALID_ARG;
+        return SOFTMAX_OK;
+    case SOFTMAX_VARIANT_SPLITK:
+        if (V != kStreamUnroll || p.block_threads > kStreamThreads)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.cluster_x < 1 || p.cluster_x > kMaxCluster || p.grid_x != p.cluster_x || p.grid_y != rows)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (rows > 65535 || (p.cluster_x > 1 && !dev.cluster_launch))
+            return SOFTMAX_ERR_INVALID_ARG;
+        return SOFTMAX_OK;
+    default:
+        return SOFTMAX_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace osd
+
+using namespace osd;
+
+extern "C" __attribute__((visibility("default"))) int softmax_plan(
+    const softmax_device_info *dev, const void *x, const void *y, int64_t rows, int64_t cols,
+    int dtype, int variant, softmax_launch_plan *plan)
+{
+    if (!dev || !plan)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int rc = validate_args(x, y, rows, cols, dtype);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (variant < SOFTMAX_VARIANT_AUTO || variant >= SOFTMAX_VARIANT_COUNT)
+        return SOFTMAX_ERR_INVALID_ARG;
+    softmax_launch_plan p = {};
+    p.grid_x = 1;
+    p.grid_y = 1;
+    p.cluster_x = 1;
+    if (rows == 0 || cols == 0) {
+        p.variant = variant == SOFTMAX_VARIANT_AUTO ? SOFTMAX_VARIANT_ROWGROUP : variant;
+        p.grid_x = 0;
+        *plan = p;
+        return SOFTMAX_OK;
+    }
+    const Geometry g = geometry(x, y, cols, dtype);
+    p.aligned = g.aligned;
+    p.y_vector = g.y_vec;
+
+    int v = variant;
+    if (v == SOFTMAX_VARIANT_AUTO) {
+        const bool few_rows = rows * 2 <= dev->sm_count;
+        const bool long_rows = g.nch_max >= int64_t(4) * kStreamThreads * kStreamUnroll;
+        if (rowgroup_fits(g))
+            v = SOFTMAX_VARIANT_ROWGROUP;
+        else if (few_rows && long_rows && splitk_possible(rows, *dev))
+            v = SOFTMAX_VARIANT_SPLITK;
+        else if (tma_fits(g, *dev))
+            v = SOFTMAX_VARIANT_BLOCK_TMA;
+        else if (block_fits(g))
+            v = SOFTMAX_VARIANT_BLOCK;
+        else if (rows < dev->sm_count && splitk_possible(rows, *dev))
+            v = SOFTMAX_VARIANT_SPLITK;
+        else
+            v = SOFTMAX_VARIANT_STREAM;
+    }
+    switch (v) {
+    case SOFTMAX_VARIANT_ROWGROUP:
+        if (!rowgroup_fits(g))
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        plan_rowgroup(g, rows, p);
+        break;
+    case SOFTMAX_VARIANT_BLOCK:
+        if (!block_fits(g))
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        plan_block(g, rows, p);
+        break;
+    case SOFTMAX_VARIANT_BLOCK_TMA:
+        if (!tma_fits(g, *dev) || !plan_tma(g, rows, *dev, p))
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        break;
+    case SOFTMAX_VARIANT_STREAM:
+        plan_stream(rows, p);
+        break;
+    case SOFTMAX_VARIANT_SPLITK:
+        if (!splitk_possible(rows, *dev))
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        plan_splitk(g, rows, *dev, p);
+        break;
+    default:
+        return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+    }
+    *plan = p;
+    return SOFTMAX_OK;
+}

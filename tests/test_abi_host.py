@@ -1,0 +1,196 @@
+"""Host-only checks of the C ABI: the library loads, exports exactly what
+include/softmax.h declares, rejects bad arguments before touching CUDA, and
+its dispatcher (softmax_plan, pure host code) picks launch shapes that cover
+every row.  No call here reaches a CUDA runtime function."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from online_softmax_dispatcher_gb300 import _binding as B
+from online_softmax_dispatcher_gb300 import build as build_mod
+from online_softmax_dispatcher_gb300.workloads import WORKLOADS
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "softmax.h")
+
+# A GB300 as the dispatcher sees it (152 SMs, 227 KB opt-in shared memory).
+GB300 = B.DeviceInfo(sm_count=152, max_smem_optin=232448, cluster_launch=1, l2_bytes=132644864,
+                     cc_major=10, cc_minor=3)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(softmax_\w+)\s*\(", text))
+
+
+def exported_symbols(path):
+    import subprocess
+
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    return {line.split()[-1] for line in out.splitlines() if " T " in line and line.split()[-1].startswith("softmax_")}
+
+
+def test_exports_match_header(lib):
+    declared = declared_functions()
+    assert declared == set(B.EXPORTS)
+    assert exported_symbols(B.LIB_PATH) == declared
+    for name in declared:
+        assert hasattr(lib, name)
+
+
+def test_strings_and_version(lib):
+    assert B.softmax_abi_version() == 1
+    assert B.softmax_strerror(0) == "ok"
+    assert "overlap" in B.softmax_strerror(B.ERR_ALIAS)
+    assert B.softmax_strerror(12345) == "unknown status"
+    names = [B.softmax_variant_name(v) for v in range(B.VARIANT_COUNT)]
+    assert names == list(B.VARIANTS)
+
+
+BASE = 1 << 40  # fake, 256-byte aligned "device" addresses: validation only looks at them
+
+
+@pytest.mark.parametrize("args,want", [
+    ((BASE, BASE + 4096, 2, 3, 7), B.ERR_UNSUPPORTED_DTYPE),
+    ((BASE, BASE + 4096, -1, 3, 0), B.ERR_INVALID_ARG),
+    ((BASE, BASE + 4096, 2, -3, 0), B.ERR_INVALID_ARG),
+    ((0, BASE, 2, 3, 0), B.ERR_INVALID_ARG),
+    ((BASE, 0, 2, 3, 0), B.ERR_INVALID_ARG),
+    ((BASE + 2, BASE + 4096, 2, 3, 0), B.ERR_INVALID_ARG),       # fp32 needs 4-byte alignment
+    ((BASE + 1, BASE + 4097, 2, 3, 1), B.ERR_INVALID_ARG),       # fp16 needs 2-byte alignment
+    ((BASE, BASE + 20, 2, 3, 0), B.ERR_ALIAS),                   # 24 bytes of x overlap y
+    ((BASE + 20, BASE, 2, 3, 0), B.ERR_ALIAS),                   # y overlaps the start of x
+    ((BASE, BASE, 2, 3, 0), B.ERR_ALIAS),
+    ((BASE, BASE + 64, 2**40, 2**40, 0), B.ERR_INVALID_ARG),     # rows*cols*4 overflows int64
+    ((0, 0, 0, 5, 0), B.OK),                                     # empty: no launch, no device
+    ((0, 0, 5, 0, 2), B.OK),
+])
+def test_argument_validation(lib, args, want):
+    x, y, rows, cols, dt = args
+    assert B.softmax_fwd(x, y, rows, cols, dt, 0) == want
+    assert B.softmax_fwd_variant(x, y, rows, cols, dt, 0, 0) == want
+    rc, _ = B.softmax_plan(GB300, x, y, rows, cols, dt)
+    assert rc == want
+
+
+def test_adjacent_buffers_are_not_aliases(lib):
+    # x = [BASE, BASE+24), y starts right after: no overlap
+    rc, p = B.softmax_plan(GB300, BASE, BASE + 24, 2, 3, 0)
+    assert rc == B.OK
+
+
+def test_bad_variant_and_null_out(lib):
+    assert B.softmax_fwd_variant(BASE, BASE + 4096, 2, 3, 0, 99, 0) == B.ERR_INVALID_ARG
+    assert B.softmax_fwd_variant(BASE, BASE + 4096, 2, 3, 0, -1, 0) == B.ERR_INVALID_ARG
+    assert lib.softmax_query_variant(BASE, BASE + 4096, 2, 3, 0, None) == B.ERR_INVALID_ARG
+    assert lib.softmax_plan(None, BASE, BASE + 4096, 2, 3, 0, 0, None) == B.ERR_INVALID_ARG
+    assert lib.softmax_device_query(None) == B.ERR_INVALID_ARG
+    assert lib.softmax_get_device_error(None, None) == B.ERR_INVALID_ARG
+    assert lib.softmax_fwd_plan(BASE, BASE + 4096, 2, 3, 0, None, None) == B.ERR_INVALID_ARG
+
+
+def _nch_max(cols, elem, aligned):
+    rb = cols * elem
+    return rb // 16 if aligned else -(-(rb + 16 - elem) // 16)
+
+
+def _covers(p, rows, cols, elem, aligned):
+    """The plan's threads cover every 16-byte chunk of a row."""
+    n = _nch_max(cols, elem, aligned)
+    if p.variant == B.VARIANT_ROWGROUP:
+        return p.lanes_per_row * p.chunks_per_thread >= n and (p.lanes_per_row == 32 or p.chunks_per_thread == 1)
+    if p.variant == B.VARIANT_BLOCK:
+        return p.block_threads * p.chunks_per_thread >= n
+    if p.variant == B.VARIANT_BLOCK_TMA:
+        stage = p.smem_bytes // p.stages
+        lead = 0 if aligned else 16 - elem
+        return stage * 1 >= -(-(lead + p.rows_per_tile * cols * elem) // 16) * 16
+    return p.variant in (B.VARIANT_STREAM, B.VARIANT_SPLITK)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_dispatch_of_workloads(lib, name):
+    w = WORKLOADS[name]
+    x = BASE
+    y = BASE + (1 << 36)
+    rc, p = B.softmax_plan(GB300, x, y, w.rows, w.cols, w.dtype_code)
+    assert rc == B.OK
+    aligned = (w.cols * w.elem_bytes) % 16 == 0
+    assert p.aligned == int(aligned) and p.y_vector == 1
+    assert _covers(p, w.rows, w.cols, w.elem_bytes, aligned)
+    expect = {
+        "fp32_128x1000": B.VARIANT_ROWGROUP,
+        "attn_fp16_65536x512": B.VARIANT_ROWGROUP,
+        "awkward_fp16_8192x5003": B.VARIANT_BLOCK_TMA,
+        "vocab_bf16_32768x32000": B.VARIANT_BLOCK_TMA,
+        "splitk_fp32_4x4194304": B.VARIANT_SPLITK,
+        "splitk_fp16_4x4194304": B.VARIANT_SPLITK,
+    }[name]
+    assert p.variant == expect, B.softmax_variant_name(p.variant)
+    if p.variant == B.VARIANT_SPLITK:
+        assert p.cluster_x == 16 and p.grid_x == 16 and p.grid_y == w.rows
+
+
+@pytest.mark.parametrize("dt,elem", [(0, 4), (1, 2), (2, 2)])
+def test_dispatch_sweep_covers_rows(lib, dt, elem):
+    for cols in list(range(1, 70)) + [127, 128, 129, 255, 256, 257, 511, 512, 513, 1000, 1023, 1024, 1025,
+                                      2047, 2048, 4096, 5003, 8191, 8192, 16384, 32000, 50000, 65536,
+                                      100000, 131072, 1 << 20, (1 << 22) + 3]:
+        for rows in (1, 3, 77, 4096):
+            for xoff, yoff in ((0, 0), (elem, elem), (0, elem), (2 * elem, 6 * elem)):
+                x, y = BASE + xoff, BASE + (1 << 38) + yoff
+                for v in range(B.VARIANT_COUNT):
+                    rc, p = B.softmax_plan(GB300, x, y, rows, cols, dt, v)
+                    if rc == B.ERR_UNSUPPORTED_SHAPE:
+                        assert v != B.VARIANT_AUTO and v != B.VARIANT_STREAM
+                        continue
+                    assert rc == B.OK, (cols, rows, v)
+                    aligned = x % 16 == 0 and y % 16 == 0 and (cols * elem) % 16 == 0
+                    assert p.aligned == int(aligned)
+                    assert p.y_vector == int((y - x) % 16 == 0)
+                    assert _covers(p, rows, cols, elem, aligned), (cols, rows, v, p.as_dict())
+                    if v != B.VARIANT_AUTO:
+                        assert p.variant == v
+                    assert p.grid_x >= 1
+
+
+def test_splitk_needs_clusters(lib):
+    no_clusters = B.DeviceInfo(sm_count=152, max_smem_optin=232448, cluster_launch=0,
+                               l2_bytes=1 << 27, cc_major=10, cc_minor=3)
+    rc, p = B.softmax_plan(no_clusters, BASE, BASE + (1 << 36), 4, 1 << 22, 0)
+    assert rc == B.OK and p.variant == B.VARIANT_STREAM
+    rc, _ = B.softmax_plan(no_clusters, BASE, BASE + (1 << 36), 4, 1 << 22, 0, B.VARIANT_SPLITK)
+    assert rc == B.ERR_UNSUPPORTED_SHAPE
+
+
+def test_forced_variants_reject_rows_too_long(lib):
+    rc, _ = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 8, 1 << 20, 1, B.VARIANT_ROWGROUP)
+    assert rc == B.ERR_UNSUPPORTED_SHAPE
+    rc, _ = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 8, 1 << 20, 1, B.VARIANT_BLOCK)
+    assert rc == B.ERR_UNSUPPORTED_SHAPE
+    rc, _ = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 8, 1 << 20, 1, B.VARIANT_BLOCK_TMA)
+    assert rc == B.ERR_UNSUPPORTED_SHAPE
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 8, 1 << 20, 1, B.VARIANT_STREAM)
+    assert rc == B.OK and p.variant == B.VARIANT_STREAM
+
+
+def test_library_refuses_to_load_when_missing(tmp_path, monkeypatch):
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(B.SoftmaxLibraryMissing):
+        B.lib()
+
+
+def test_plan_struct_layout():
+    # the ctypes mirror must match the C struct (ints, then int64 grid dims)
+    assert ctypes.sizeof(B.LaunchPlan) == 56
+    assert B.LaunchPlan.grid_x.offset == 24 and B.LaunchPlan.cluster_x.offset == 40
+    assert ctypes.sizeof(B.DeviceInfo) == 24
