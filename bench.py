@@ -144,10 +144,11 @@ class ClockSampler:
             try:
                 ts = time.mktime(time.strptime(rec[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
                 frac = float("0." + rec[0].strip().split(".")[1]) if "." in rec[0] else 0.0
+                active = [v.strip() == "Active" for v in rec[5:9]]
                 rows.append({"t": ts + frac, "sm": float(rec[1]), "sm_max": float(rec[2]),
                              "power": float(rec[3]) if rec[3].strip() not in ("[N/A]", "") else None,
-                             "hw_slowdown": "Active" in rec[5], "hw_thermal": "Active" in rec[6],
-                             "sw_thermal": "Active" in rec[7], "sw_power_cap": "Active" in rec[8]})
+                             "hw_slowdown": active[0], "hw_thermal": active[1],
+                             "sw_thermal": active[2], "sw_power_cap": active[3]})
             except (ValueError, IndexError):
                 continue
         return rows

@@ -284,12 +284,35 @@ __device__ __forceinline__ void opaque(uint4 &c)
     asm volatile("" : "+r"(c.x), "+r"(c.y), "+r"(c.z), "+r"(c.w));
 }
 
+// Replace the slots of a chunk whose element index (t0 + slot) falls outside
+// [lo, hi) with -inf.
+template <int DT>
+__device__ __forceinline__ uint4 mask_chunk(const uint4 &c, int64_t t0, int64_t lo, int64_t hi)
+{
+    uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    if constexpr (DT == kF32) {
+#pragma unroll
+        for (int e = 0; e < 4; e++)
+            if (t0 + e < lo || t0 + e >= hi)
+                w[e] = kNegInfF32;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; e++)
+            if (t0 + e < lo || t0 + e >= hi) {
+                const int sh = 16 * (e & 1);
+                w[e >> 1] = (w[e >> 1] & ~(0xFFFFu << sh)) | (Fmt<DT>::kNegInf << sh);
+            }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // ---------------------------------------------------------------- exp and sums
 
-__device__ __forceinline__ float ex2_approx(float v)
+// 2^v on the SFU, subnormal results flushed to zero (one instruction).
+__device__ __forceinline__ float ex2_ftz(float v)
 {
     float r;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
     return r;
 }
 
@@ -308,15 +331,28 @@ struct CSum {
 };
 
 // Per-dtype arithmetic policy.  Acc is the running sum type.
+//
+// fp16 / bf16: exp_shift(v, m) = 2^(kExpBias) * exp(v - m), with the SFU's
+// flush-to-zero 2^x.  Every consumer divides by a sum of the same scaled terms,
+// so the scale cancels in y; it exists for bf16, whose outputs reach subnormals
+// (down to 2^-133): without it exp(v - m) would flush below 2^-126 and lose
+// them, with it only terms below 2^-190 flush, which bf16 rounds to 0 anyway.
+// fp16 outputs underflow to 0 below 2^-25, so fp16 needs no scale.
+// v - m is computed first (exact for inputs on a common dyadic grid), so a
+// shifted input gives bit-identical results.
 template <int DT>
 struct Math {
     using Acc = float;
+    static constexpr float kExpBias = DT == kBF16 ? 64.f : 0.f;
     static __device__ __forceinline__ float exp_shift(float v, float m)
     {
-        return ex2_approx((v - m) * kLog2e);
+        if constexpr (DT == kBF16)
+            return ex2_ftz(fmaf(v - m, kLog2e, kExpBias));
+        else
+            return ex2_ftz((v - m) * kLog2e);
     }
-    // exp(a) for a <= 0, used to rescale partial sums.
-    static __device__ __forceinline__ float exp_of(float a) { return ex2_approx(a * kLog2e); }
+    // exp(a) for a <= 0, the ratio used to rescale partial sums (unscaled).
+    static __device__ __forceinline__ float exp_of(float a) { return ex2_ftz(a * kLog2e); }
     static __device__ __forceinline__ Acc zero() { return 0.f; }
     static __device__ __forceinline__ void add(Acc &a, float v) { a += v; }
     static __device__ __forceinline__ Acc merge(const Acc &a, const Acc &b) { return a + b; }
@@ -361,6 +397,33 @@ struct Math<kF32> {
         return CSum{__shfl_xor_sync(0xFFFFFFFFu, a.s, o), __shfl_xor_sync(0xFFFFFFFFu, a.c, o)};
     }
 };
+
+// Max over the slots of a chunk.  16-bit formats compare packed pairs (the max
+// of two representable values is exact in any format).
+template <int DT>
+__device__ __forceinline__ float chunk_max(const uint4 &c)
+{
+    if constexpr (DT == kF32) {
+        return fmaxf(fmaxf(__uint_as_float(c.x), __uint_as_float(c.y)),
+                     fmaxf(__uint_as_float(c.z), __uint_as_float(c.w)));
+    } else if constexpr (DT == kF16) {
+        __half2 a, b, cc, d;
+        *reinterpret_cast<uint32_t *>(&a) = c.x;
+        *reinterpret_cast<uint32_t *>(&b) = c.y;
+        *reinterpret_cast<uint32_t *>(&cc) = c.z;
+        *reinterpret_cast<uint32_t *>(&d) = c.w;
+        const __half2 h = __hmax2(__hmax2(a, b), __hmax2(cc, d));
+        return fmaxf(__low2float(h), __high2float(h));
+    } else {
+        __nv_bfloat162 a, b, cc, d;
+        *reinterpret_cast<uint32_t *>(&a) = c.x;
+        *reinterpret_cast<uint32_t *>(&b) = c.y;
+        *reinterpret_cast<uint32_t *>(&cc) = c.z;
+        *reinterpret_cast<uint32_t *>(&d) = c.w;
+        const __nv_bfloat162 h = __hmax2(__hmax2(a, b), __hmax2(cc, d));
+        return fmaxf(__low2float(h), __high2float(h));
+    }
+}
 
 // ---------------------------------------------------------------- warp / block reductions
 

@@ -40,16 +40,15 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
             raw[i] = load_chunk<DT, ALIGNED>(g, t + (int64_t)i * T, cols);
 
         if constexpr (kKeepE) {
-            float v[V][E];
             float m = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < V; i++) {
-                unpack<DT>(raw[i], v[i]);
-#pragma unroll
-                for (int e = 0; e < E; e++)
-                    m = fmaxf(m, v[i][e]);
-            }
+            for (int i = 0; i < V; i++)
+                m = fmaxf(m, chunk_max<DT>(raw[i]));
             m = block_max(m, smax);
+            float v[V][E];
+#pragma unroll
+            for (int i = 0; i < V; i++)
+                unpack<DT>(raw[i], v[i]);
             Acc acc = M::zero();
 #pragma unroll
             for (int i = 0; i < V; i++)
@@ -74,13 +73,8 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
         } else {
             float m = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < V; i++) {
-                float f[E];
-                unpack<DT>(raw[i], f);
-#pragma unroll
-                for (int e = 0; e < E; e++)
-                    m = fmaxf(m, f[e]);
-            }
+            for (int i = 0; i < V; i++)
+                m = fmaxf(m, chunk_max<DT>(raw[i]));
             m = block_max(m, smax);
 #pragma unroll
             for (int i = 0; i < V; i++)

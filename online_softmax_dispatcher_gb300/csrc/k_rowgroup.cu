@@ -59,17 +59,15 @@ __global__ void __launch_bounds__(kRowgroupThreads)
         }
         const bool valid = r < rows;
 
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < V; i++)
+            m = fmaxf(m, chunk_max<DT>(cur[i]));
+        m = group_max<G>(m);
         float v[V][E];
 #pragma unroll
         for (int i = 0; i < V; i++)
             unpack<DT>(cur[i], v[i]);
-        float m = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < V; i++)
-#pragma unroll
-            for (int e = 0; e < E; e++)
-                m = fmaxf(m, v[i][e]);
-        m = group_max<G>(m);
 
         typename M::Acc acc = M::zero();
 #pragma unroll

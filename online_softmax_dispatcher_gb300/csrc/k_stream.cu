@@ -56,13 +56,8 @@ __device__ MD pass_online(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols
         load_step<DT, ALIGNED>(g, k0, ke, cols, raw);
         float mt = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < U; u++) {
-            float f[E];
-            unpack<DT>(raw[u], f);
-#pragma unroll
-            for (int e = 0; e < E; e++)
-                mt = fmaxf(mt, f[e]);
-        }
+        for (int u = 0; u < U; u++)
+            mt = fmaxf(mt, chunk_max<DT>(raw[u]));
         if (mt > md.m) {
             md.d = md.m == -INFINITY ? 0.f : md.d * M::exp_of(md.m - mt);
             md.m = mt;
@@ -87,20 +82,14 @@ __device__ MD pass_online(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols
 template <int DT, bool ALIGNED>
 __device__ float pass_max(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols)
 {
-    constexpr int E = Fmt<DT>::kPerChunk;
     float m = -INFINITY;
     const int64_t T = blockDim.x;
     for (int64_t k0 = kb + threadIdx.x; k0 < ke; k0 += T * U) {
         uint4 raw[U];
         load_step<DT, ALIGNED>(g, k0, ke, cols, raw);
 #pragma unroll
-        for (int u = 0; u < U; u++) {
-            float f[E];
-            unpack<DT>(raw[u], f);
-#pragma unroll
-            for (int e = 0; e < E; e++)
-                m = fmaxf(m, f[e]);
-        }
+        for (int u = 0; u < U; u++)
+            m = fmaxf(m, chunk_max<DT>(raw[u]));
     }
     return m;
 }

@@ -28,6 +28,8 @@
 // * Every mbarrier wait is bounded (tma.cuh).  A consumer group agrees on a
 //   give-up with a barrier-AND before it enters any named barrier, so no warp
 //   is left waiting for one that left.
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tma.cuh"
@@ -150,32 +152,20 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma(const TmaParams p)
             const int64_t e_lo = j * p.cols, e_hi = e_lo + p.cols;  // row j's tile elements
             const int64_t cf = (e_lo + h0) / E, cl = (e_hi - 1 + h0) / E;
 
-            // chunk c of the tile as floats, slots outside row j set to -inf
-            auto read = [&](int64_t c, float (&f)[E]) {
-                uint4 raw;
-                if (ALIGNED || (c >= c_lo && c < c_hi)) {
-                    raw = lds_chunk(sbase + 16 * (uint32_t)c);
-                } else {
-                    raw = ld_partial<DT>(ts, c * E - h0, tile_elems);
-                }
-                unpack<DT>(raw, f);
-                if (!ALIGNED) {
-                    const int64_t t0 = c * E - h0;
-#pragma unroll
-                    for (int e = 0; e < E; e++)
-                        if (t0 + e < e_lo || t0 + e >= e_hi)
-                            f[e] = -INFINITY;
-                }
+            // chunk c of the tile, slots outside row j set to -inf
+            auto read_raw = [&](int64_t c) -> uint4 {
+                if (ALIGNED)
+                    return lds_chunk(sbase + 16 * (uint32_t)c);
+                const uint4 raw = (c >= c_lo && c < c_hi) ? lds_chunk(sbase + 16 * (uint32_t)c)
+                                                          : ld_partial<DT>(ts, c * E - h0, tile_elems);
+                const int64_t t0 = c * E - h0;
+                return (t0 >= e_lo && t0 + E <= e_hi) ? raw : mask_chunk<DT>(raw, t0, e_lo, e_hi);
             };
+            auto read = [&](int64_t c, float (&f)[E]) { unpack<DT>(read_raw(c), f); };
 
             float m = -INFINITY;
-            for (int64_t c = cf + gt; c <= cl; c += GT) {
-                float f[E];
-                read(c, f);
-#pragma unroll
-                for (int e = 0; e < E; e++)
-                    m = fmaxf(m, f[e]);
-            }
+            for (int64_t c = cf + gt; c <= cl; c += GT)
+                m = fmaxf(m, chunk_max<DT>(read_raw(c)));
             m = group_max<32>(m);
             if (W > 1) {
                 if (lane == 0)
@@ -235,16 +225,38 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma(const TmaParams p)
 
 namespace {
 
+// Opt the kernel in to `bytes` of dynamic shared memory on the current device
+// (static shared memory counts against the same 48 KB default, so every launch
+// checks); the largest value set so far is cached per device.
+template <int DT, bool A>
+int ensure_dynamic_smem(int bytes)
+{
+    static std::atomic<int> granted[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return (int)e;
+    if (dev < 0 || dev >= 64)
+        return (int)cudaErrorInvalidDevice;
+    if (granted[dev].load(std::memory_order_relaxed) >= bytes)
+        return 0;
+    e = cudaFuncSetAttribute(&k_tma<DT, A>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess)
+        return (int)e;
+    int cur = granted[dev].load();
+    while (cur < bytes && !granted[dev].compare_exchange_weak(cur, bytes)) {
+    }
+    return 0;
+}
+
 template <int DT, bool A>
 int launch_one(const Launch &l)
 {
     auto *kern = &k_tma<DT, A>;
     const softmax_launch_plan &pl = l.plan;
-    if (pl.smem_bytes > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
-        if (e != cudaSuccess)
-            return (int)e;
-    }
+    const int e = ensure_dynamic_smem<DT, A>(pl.smem_bytes);
+    if (e != 0)
+        return e;
     TmaParams p;
     p.x = (const char *)l.x;
     p.y = (char *)l.y;
