@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import dataclasses
 import hashlib
 import io
 import json
@@ -251,6 +252,8 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     from online_softmax_dispatcher_gb300 import workloads as W
 
     w = W.WORKLOADS[args.workload]
+    if args.rows is not None:
+        w = dataclasses.replace(w, rows=min(args.rows, w.rows))
     dev = torch.device("cuda")
     x_np = W.generate(w)
     x_host = W.as_torch(x_np, w.dtype).pin_memory()
@@ -398,6 +401,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--rows", type=int, default=None,
+                    help="time only the first ROWS rows of the workload (for small profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

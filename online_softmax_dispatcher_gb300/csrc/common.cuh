@@ -344,13 +344,15 @@ template <int DT>
 struct Math {
     using Acc = float;
     static constexpr float kExpBias = DT == kBF16 ? 64.f : 0.f;
-    static __device__ __forceinline__ float exp_shift(float v, float m)
+    // the scaled exp of an already shifted value t = v - m
+    static __device__ __forceinline__ float exp_t(float t)
     {
         if constexpr (DT == kBF16)
-            return ex2_ftz(fmaf(v - m, kLog2e, kExpBias));
+            return ex2_ftz(fmaf(t, kLog2e, kExpBias));
         else
-            return ex2_ftz((v - m) * kLog2e);
+            return ex2_ftz(t * kLog2e);
     }
+    static __device__ __forceinline__ float exp_shift(float v, float m) { return exp_t(v - m); }
     // exp(a) for a <= 0, the ratio used to rescale partial sums (unscaled).
     static __device__ __forceinline__ float exp_of(float a) { return ex2_ftz(a * kLog2e); }
     static __device__ __forceinline__ Acc zero() { return 0.f; }
@@ -398,6 +400,27 @@ struct Math<kF32> {
     }
 };
 
+// x - m in fp32 for the two 16-bit values packed in w (low half first): one
+// mixed-precision FMA each (16-bit x times 1, plus the fp32 -m), which is the
+// correctly rounded x - m -- the same value as converting x and subtracting.
+template <int DT>
+__device__ __forceinline__ void sub_pair(uint32_t w, float neg_m, float &t0, float &t1)
+{
+    if constexpr (DT == kF16) {
+        const unsigned short one = 0x3C00u;
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "fma.rn.f32.f16 %0, lo, %3, %4;\n\tfma.rn.f32.f16 %1, hi, %3, %4;\n\t}"
+            : "=f"(t0), "=f"(t1)
+            : "r"(w), "h"(one), "f"(neg_m));
+    } else {
+        const unsigned short one = 0x3F80u;
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, lo, %3, %4;\n\tfma.rn.f32.bf16 %1, hi, %3, %4;\n\t}"
+            : "=f"(t0), "=f"(t1)
+            : "r"(w), "h"(one), "f"(neg_m));
+    }
+}
+
 // Max over the slots of a chunk.  16-bit formats compare packed pairs (the max
 // of two representable values is exact in any format).
 template <int DT>
@@ -425,7 +448,39 @@ __device__ __forceinline__ float chunk_max(const uint4 &c)
     }
 }
 
+// f[e] = exp_shift(slot e of chunk c, m) for every slot.  16-bit formats go
+// straight from the packed words (sub_pair), skipping the separate convert.
+template <int DT>
+__device__ __forceinline__ void chunk_exp(const uint4 &c, float m, float (&f)[Fmt<DT>::kPerChunk])
+{
+    if constexpr (DT == kF32) {
+        unpack<DT>(c, f);
+#pragma unroll
+        for (int e = 0; e < 4; e++)
+            f[e] = Math<DT>::exp_shift(f[e], m);
+    } else {
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+        const float nm = -m;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float t0, t1;
+            sub_pair<DT>(w[i], nm, t0, t1);
+            f[2 * i] = Math<DT>::exp_t(t0);
+            f[2 * i + 1] = Math<DT>::exp_t(t1);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- warp / block reductions
+
+// Max over the full warp in one instruction (sm_100-family redux on f32; a
+// NaN input is ignored, as fmaxf ignores it).
+__device__ __forceinline__ float warp_max_redux(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
 
 // Max over aligned groups of G lanes (xor butterfly; all 32 lanes must call).
 template <int G>

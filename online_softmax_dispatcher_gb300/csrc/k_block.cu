@@ -46,17 +46,14 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
                 m = fmaxf(m, chunk_max<DT>(raw[i]));
             m = block_max(m, smax);
             float v[V][E];
-#pragma unroll
-            for (int i = 0; i < V; i++)
-                unpack<DT>(raw[i], v[i]);
             Acc acc = M::zero();
 #pragma unroll
-            for (int i = 0; i < V; i++)
+            for (int i = 0; i < V; i++) {
+                chunk_exp<DT>(raw[i], m, v[i]);
 #pragma unroll
-                for (int e = 0; e < E; e++) {
-                    v[i][e] = M::exp_shift(v[i][e], m);
+                for (int e = 0; e < E; e++)
                     M::add(acc, v[i][e]);
-                }
+            }
             acc = block_sum<DT>(acc, ssum);
             const float inv = 1.0f / M::value(acc);
 #pragma unroll
@@ -83,10 +80,10 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
 #pragma unroll
             for (int i = 0; i < V; i++) {
                 float f[E];
-                unpack<DT>(raw[i], f);
+                chunk_exp<DT>(raw[i], m, f);
 #pragma unroll
                 for (int e = 0; e < E; e++)
-                    M::add(acc, M::exp_shift(f[e], m));
+                    M::add(acc, f[e]);
             }
             acc = block_sum<DT>(acc, ssum);
             const float inv = 1.0f / M::value(acc);
@@ -98,10 +95,10 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
                 const int64_t k = t + (int64_t)i * T;
                 if (k < g.nch) {
                     float f[E];
-                    unpack<DT>(raw[i], f);
+                    chunk_exp<DT>(raw[i], m, f);
 #pragma unroll
                     for (int e = 0; e < E; e++)
-                        f[e] = M::exp_shift(f[e], m) * inv;
+                        f[e] *= inv;
                     store_chunk<DT, ALIGNED>(g, k, cols, pack<DT>(f), y_vec != 0);
                 }
             }

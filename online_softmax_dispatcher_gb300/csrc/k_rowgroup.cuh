@@ -1,5 +1,7 @@
-// k_rowgroup.cu -- G lanes per row (G = 1, 2, ..., 32), the row cached in
-// registers, one HBM read and one HBM write per element.
+// k_rowgroup.cuh -- G lanes per row (G = 1, 2, ..., 32), the row cached in
+// registers, one HBM read and one HBM write per element.  Instantiated once
+// per dtype (k_rowgroup_f32.cu, k_rowgroup_f16.cu, k_rowgroup_bf16.cu) so the
+// instances compile in parallel.
 //
 // Prior art: the wavefront-per-row kernel of "Softmax on DCU", section 4.1
 // (one 64-lane wavefront per row, shuffle-reduced max), and the block-per-row
@@ -16,6 +18,8 @@
 // then write e * (1 / d) as 16-byte stores.  Each group walks rows with a grid
 // stride and issues the loads of its next row before working on the current
 // one, so a row's HBM latency overlaps the previous row's arithmetic.
+#pragma once
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -63,20 +67,16 @@ __global__ void __launch_bounds__(kRowgroupThreads)
 #pragma unroll
         for (int i = 0; i < V; i++)
             m = fmaxf(m, chunk_max<DT>(cur[i]));
-        m = group_max<G>(m);
+        m = G == 32 ? warp_max_redux(m) : group_max<G>(m);
         float v[V][E];
-#pragma unroll
-        for (int i = 0; i < V; i++)
-            unpack<DT>(cur[i], v[i]);
-
         typename M::Acc acc = M::zero();
 #pragma unroll
-        for (int i = 0; i < V; i++)
+        for (int i = 0; i < V; i++) {
+            chunk_exp<DT>(cur[i], m, v[i]);
 #pragma unroll
-            for (int e = 0; e < E; e++) {
-                v[i][e] = M::exp_shift(v[i][e], m);
+            for (int e = 0; e < E; e++)
                 M::add(acc, v[i][e]);
-            }
+        }
         acc = group_sum<DT, G>(acc);
         const float inv = 1.0f / M::value(acc);
 
@@ -97,10 +97,8 @@ __global__ void __launch_bounds__(kRowgroupThreads)
     }
 }
 
-namespace {
-
 template <int DT, int G, int V, bool A>
-int launch_one(const Launch &l)
+int rowgroup_launch_one(const Launch &l)
 {
     k_rowgroup<DT, G, V, A><<<(unsigned)l.plan.grid_x, kRowgroupThreads, 0, (cudaStream_t)l.stream>>>(
         (const char *)l.x, (char *)l.y, l.rows, l.cols, l.plan.y_vector);
@@ -108,69 +106,49 @@ int launch_one(const Launch &l)
 }
 
 template <int DT, int G, int V>
-int launch_a(const Launch &l)
+int rowgroup_launch_a(const Launch &l)
 {
-    return l.plan.aligned ? launch_one<DT, G, V, true>(l) : launch_one<DT, G, V, false>(l);
+    return l.plan.aligned ? rowgroup_launch_one<DT, G, V, true>(l) : rowgroup_launch_one<DT, G, V, false>(l);
 }
 
-// V chunks per lane; V * E <= 32 floats.
+// V chunks per lane, V * E <= 32 floats: V in {1, 2, 4} (and 8 for fp32).
 template <int DT, int G>
-int launch_v(const Launch &l)
+int rowgroup_launch_v(const Launch &l)
 {
     constexpr int E = Fmt<DT>::kPerChunk;
     switch (l.plan.chunks_per_thread) {
     case 1:
-        return launch_a<DT, G, 1>(l);
+        return rowgroup_launch_a<DT, G, 1>(l);
     case 2:
-        return launch_a<DT, G, 2>(l);
+        return rowgroup_launch_a<DT, G, 2>(l);
     case 4:
-        return launch_a<DT, G, 4>(l);
+        return rowgroup_launch_a<DT, G, 4>(l);
     case 8:
         if constexpr (8 * E <= kRowgroupMaxFloats)
-            return launch_a<DT, G, 8>(l);
+            return rowgroup_launch_a<DT, G, 8>(l);
         return (int)cudaErrorInvalidValue;
     default:
         return (int)cudaErrorInvalidValue;
     }
 }
 
-// Groups narrower than a warp only ever need one chunk per lane (the planner
-// widens G first), so only G = 32 is compiled with V > 1.
+// A single lane per row only serves rows of one chunk.
 template <int DT>
-int launch_g(const Launch &l)
+int rowgroup_launch_dt(const Launch &l)
 {
-    const int G = l.plan.lanes_per_row, V = l.plan.chunks_per_thread;
-    if (G < 32 && V != 1)
-        return (int)cudaErrorInvalidValue;
-    switch (G) {
+    switch (l.plan.lanes_per_row) {
     case 1:
-        return launch_a<DT, 1, 1>(l);
+        return l.plan.chunks_per_thread == 1 ? rowgroup_launch_a<DT, 1, 1>(l) : (int)cudaErrorInvalidValue;
     case 2:
-        return launch_a<DT, 2, 1>(l);
+        return rowgroup_launch_v<DT, 2>(l);
     case 4:
-        return launch_a<DT, 4, 1>(l);
+        return rowgroup_launch_v<DT, 4>(l);
     case 8:
-        return launch_a<DT, 8, 1>(l);
+        return rowgroup_launch_v<DT, 8>(l);
     case 16:
-        return launch_a<DT, 16, 1>(l);
+        return rowgroup_launch_v<DT, 16>(l);
     case 32:
-        return launch_v<DT, 32>(l);
-    default:
-        return (int)cudaErrorInvalidValue;
-    }
-}
-
-}  // namespace
-
-int launch_rowgroup(const Launch &l)
-{
-    switch (l.dtype) {
-    case kF32:
-        return launch_g<kF32>(l);
-    case kF16:
-        return launch_g<kF16>(l);
-    case kBF16:
-        return launch_g<kBF16>(l);
+        return rowgroup_launch_v<DT, 32>(l);
     default:
         return (int)cudaErrorInvalidValue;
     }

@@ -69,10 +69,10 @@ __device__ MD pass_online(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols
 #pragma unroll
         for (int u = 0; u < U; u++) {
             float f[E];
-            unpack<DT>(raw[u], f);
+            chunk_exp<DT>(raw[u], md.m, f);
 #pragma unroll
             for (int e = 0; e < E; e++)
-                s += M::exp_shift(f[e], md.m);
+                s += f[e];
         }
         md.d += s;
     }
@@ -107,10 +107,10 @@ __device__ typename Math<DT>::Acc pass_sum(const RowGeom &g, int64_t kb, int64_t
 #pragma unroll
         for (int u = 0; u < U; u++) {
             float f[E];
-            unpack<DT>(raw[u], f);
+            chunk_exp<DT>(raw[u], m, f);
 #pragma unroll
             for (int e = 0; e < E; e++)
-                M::add(acc, M::exp_shift(f[e], m));
+                M::add(acc, f[e]);
         }
     }
     return acc;
@@ -131,10 +131,10 @@ __device__ void pass_write(const RowGeom &g, int64_t kb, int64_t ke, int64_t col
             const int64_t k = k0 + u * T;
             if (k < ke) {
                 float f[E];
-                unpack<DT>(raw[u], f);
+                chunk_exp<DT>(raw[u], m, f);
 #pragma unroll
                 for (int e = 0; e < E; e++)
-                    f[e] = M::exp_shift(f[e], m) * inv;
+                    f[e] *= inv;
                 store_chunk<DT, ALIGNED>(g, k, cols, pack<DT>(f), y_vec);
             }
         }

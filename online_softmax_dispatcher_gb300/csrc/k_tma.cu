@@ -161,7 +161,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma(const TmaParams p)
                 const int64_t t0 = c * E - h0;
                 return (t0 >= e_lo && t0 + E <= e_hi) ? raw : mask_chunk<DT>(raw, t0, e_lo, e_hi);
             };
-            auto read = [&](int64_t c, float (&f)[E]) { unpack<DT>(read_raw(c), f); };
 
             float m = -INFINITY;
             for (int64_t c = cf + gt; c <= cl; c += GT)
@@ -177,10 +176,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma(const TmaParams p)
             Acc acc = M::zero();
             for (int64_t c = cf + gt; c <= cl; c += GT) {
                 float f[E];
-                read(c, f);
+                chunk_exp<DT>(read_raw(c), m, f);
 #pragma unroll
                 for (int e = 0; e < E; e++)
-                    M::add(acc, M::exp_shift(f[e], m));
+                    M::add(acc, f[e]);
             }
             acc = group_sum<DT, 32>(acc);
             if (W > 1) {
@@ -193,10 +192,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma(const TmaParams p)
 
             for (int64_t c = cf + gt; c <= cl; c += GT) {
                 float f[E];
-                read(c, f);
+                chunk_exp<DT>(read_raw(c), m, f);
 #pragma unroll
                 for (int e = 0; e < E; e++)
-                    f[e] = M::exp_shift(f[e], m) * inv;
+                    f[e] *= inv;
                 const uint4 o = pack<DT>(f);
                 const int64_t t0 = c * E - h0;
                 if (ALIGNED || (p.y_vec && t0 >= e_lo && t0 + E <= e_hi)) {

@@ -13,6 +13,7 @@ namespace osd {
 // Chunk counts and limits the dispatcher and the kernels agree on.
 constexpr int kRowgroupThreads = 256;   // CTA size of the lanes-per-row kernel
 constexpr int kRowgroupMaxFloats = 32;  // V * E cached per lane (registers)
+constexpr int kRowgroupCtasPerSm = 16;  // grid cap of the lanes-per-row kernel, per SM
 constexpr int kBlockMaxChunks = 16;     // V of the block-per-row kernel
 constexpr int kStreamThreads = 512;     // CTA size of the streaming and split-k kernels
 constexpr int kStreamUnroll = 8;        // 16-byte loads in flight per thread per step
@@ -40,7 +41,14 @@ struct Launch {
 };
 
 // Each returns the cudaError_t of its launch (0 = success).
-int launch_rowgroup(const Launch &l);
+int launch_rowgroup_f32(const Launch &l);
+int launch_rowgroup_f16(const Launch &l);
+int launch_rowgroup_bf16(const Launch &l);
+inline int launch_rowgroup(const Launch &l)
+{
+    return l.dtype == SOFTMAX_F32 ? launch_rowgroup_f32(l)
+                                  : (l.dtype == SOFTMAX_F16 ? launch_rowgroup_f16(l) : launch_rowgroup_bf16(l));
+}
 int launch_block(const Launch &l);
 int launch_block_tma(const Launch &l);
 int launch_stream(const Launch &l);

@@ -11,8 +11,8 @@
 //
 //   row fits 32 lanes' registers      -> ROWGROUP   (G lanes per row, G = 1..32)
 //   few rows, long rows, clusters     -> SPLITK     (cluster of CTAs per row)
-//   two tiles of one row fit in smem  -> BLOCK_TMA  (bulk-copy staged row tiles)
 //   row fits one CTA's registers      -> BLOCK      (one CTA per row)
+//   two tiles of one row fit in smem  -> BLOCK_TMA  (bulk-copy staged row tiles)
 //   otherwise                         -> SPLITK if rows < SMs, else STREAM
 #include <stdint.h>
 
@@ -67,27 +67,47 @@ bool rowgroup_fits(const Geometry &g) { return g.nch_max <= 32 * (kRowgroupMaxFl
 
 bool block_fits(const Geometry &g) { return g.nch_max <= int64_t(block_max_threads(kBlockMaxChunks)) * kBlockMaxChunks; }
 
-void plan_rowgroup(const Geometry &g, int64_t rows, softmax_launch_plan &p)
+// G lanes per row with V chunks each: aim for 32 cached floats per lane (4
+// chunks of fp16 / bf16, 8 of fp32) so that the per-row shuffles and the
+// reciprocal are spread over many elements; rows of up to 4 chunks get one
+// chunk per lane.  The grid is capped at 16 CTAs per SM: each group then walks
+// several rows, prefetching the next while it works on the current one.
+void plan_rowgroup(const Geometry &g, int64_t rows, const softmax_device_info &dev, softmax_launch_plan &p)
 {
-    const int64_t lanes = next_pow2(g.nch_max);
-    const int G = (int)(lanes < 32 ? lanes : 32);
-    const int V = (int)next_pow2(ceil_div(g.nch_max, G));
+    int64_t G, V;
+    if (g.nch_max <= 4) {
+        G = next_pow2(g.nch_max);
+        V = 1;
+    } else {
+        const int64_t vt = kRowgroupMaxFloats / g.E;
+        G = next_pow2(ceil_div(g.nch_max, vt));
+        if (G < 2)
+            G = 2;
+        if (G > 32)
+            G = 32;
+        V = next_pow2(ceil_div(g.nch_max, G));
+    }
     p.variant = SOFTMAX_VARIANT_ROWGROUP;
-    p.lanes_per_row = G;
-    p.chunks_per_thread = V;
+    p.lanes_per_row = (int)G;
+    p.chunks_per_thread = (int)V;
     p.block_threads = kRowgroupThreads;
     const int64_t groups = kRowgroupThreads / G;
-    const int64_t ctas = ceil_div(rows, groups);
+    int64_t ctas = ceil_div(rows, groups);
+    const int64_t cap = int64_t(kRowgroupCtasPerSm) * (dev.sm_count > 0 ? dev.sm_count : 1);
+    if (ctas > cap)
+        ctas = cap;
     p.grid_x = ctas < INT32_MAX ? ctas : INT32_MAX;
 }
 
 void plan_block(const Geometry &g, int64_t rows, softmax_launch_plan &p)
 {
     // Smallest V (>= 4, to keep several 16-byte loads in flight per thread)
-    // whose CTA stays within 512 threads (V = 16: the 256 it is compiled for),
-    // so that at least two CTAs -- two rows -- are resident per SM.
+    // whose CTA stays within 256 threads, so that several CTAs -- several
+    // rows -- are resident per SM and one's loads overlap another's reductions
+    // (measured on the [32768, 32000] bf16 rows: V = 16 x 256 threads beats
+    // V = 8 x 512).
     int V = 4;
-    while (V < kBlockMaxChunks && ceil_div(g.nch_max, V) > (V * 2 > kBlockMaxChunks ? 256 : 512))
+    while (V < kBlockMaxChunks && ceil_div(g.nch_max, V) > 256)
         V *= 2;
     int64_t threads = ceil_div(ceil_div(g.nch_max, V), 32) * 32;
     if (threads < 64)
@@ -226,7 +246,7 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
         const int G = p.lanes_per_row;
         if (G < 1 || G > 32 || (G & (G - 1)) || V < 1 || V > 8 || (V & (V - 1)))
             return SOFTMAX_ERR_INVALID_ARG;
-        if (V * g.E > kRowgroupMaxFloats || int64_t(G) * V < g.nch_max || (G < 32 && V != 1))
+        if (V * g.E > kRowgroupMaxFloats || int64_t(G) * V < g.nch_max || (G == 1 && V != 1))
             return SOFTMAX_ERR_INVALID_ARG;
         if (p.block_threads != kRowgroupThreads || p.grid_y != 1 || p.cluster_x != 1)
             return SOFTMAX_ERR_INVALID_ARG;
@@ -308,10 +328,10 @@ extern "C" __attribute__((visibility("default"))) int softmax_plan(
             v = SOFTMAX_VARIANT_ROWGROUP;
         else if (few_rows && long_rows && splitk_possible(rows, *dev))
             v = SOFTMAX_VARIANT_SPLITK;
-        else if (tma_fits(g, *dev))
-            v = SOFTMAX_VARIANT_BLOCK_TMA;
         else if (block_fits(g))
             v = SOFTMAX_VARIANT_BLOCK;
+        else if (tma_fits(g, *dev))
+            v = SOFTMAX_VARIANT_BLOCK_TMA;
         else if (rows < dev->sm_count && splitk_possible(rows, *dev))
             v = SOFTMAX_VARIANT_SPLITK;
         else
@@ -321,7 +341,7 @@ extern "C" __attribute__((visibility("default"))) int softmax_plan(
     case SOFTMAX_VARIANT_ROWGROUP:
         if (!rowgroup_fits(g))
             return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
-        plan_rowgroup(g, rows, p);
+        plan_rowgroup(g, rows, *dev, p);
         break;
     case SOFTMAX_VARIANT_BLOCK:
         if (!block_fits(g))

@@ -106,7 +106,7 @@ def _covers(p, rows, cols, elem, aligned):
     """The plan's threads cover every 16-byte chunk of a row."""
     n = _nch_max(cols, elem, aligned)
     if p.variant == B.VARIANT_ROWGROUP:
-        return p.lanes_per_row * p.chunks_per_thread >= n and (p.lanes_per_row == 32 or p.chunks_per_thread == 1)
+        return p.lanes_per_row * p.chunks_per_thread >= n and (p.lanes_per_row > 1 or p.chunks_per_thread == 1)
     if p.variant == B.VARIANT_BLOCK:
         return p.block_threads * p.chunks_per_thread >= n
     if p.variant == B.VARIANT_BLOCK_TMA:
@@ -129,8 +129,8 @@ def test_dispatch_of_workloads(lib, name):
     expect = {
         "fp32_128x1000": B.VARIANT_ROWGROUP,
         "attn_fp16_65536x512": B.VARIANT_ROWGROUP,
-        "awkward_fp16_8192x5003": B.VARIANT_BLOCK_TMA,
-        "vocab_bf16_32768x32000": B.VARIANT_BLOCK_TMA,
+        "awkward_fp16_8192x5003": B.VARIANT_BLOCK,
+        "vocab_bf16_32768x32000": B.VARIANT_BLOCK,
         "splitk_fp32_4x4194304": B.VARIANT_SPLITK,
         "splitk_fp16_4x4194304": B.VARIANT_SPLITK,
     }[name]
