@@ -25,8 +25,9 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
     using M = Math<DT>;
     using Acc = typename M::Acc;
     constexpr int E = Fmt<DT>::kPerChunk;
-    // keep e = exp(x - m) in registers when it fits, else recompute it
-    constexpr bool kKeepE = V * E <= 32;
+    // keep e = exp(x - m) in registers when it fits next to the cached chunks,
+    // else recompute it
+    constexpr bool kKeepE = V * E <= 32 && V <= 4;
     __shared__ float smax[32];
     __shared__ Acc ssum[32];
     const int T = blockDim.x;

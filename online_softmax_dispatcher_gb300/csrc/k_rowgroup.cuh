@@ -15,9 +15,10 @@
 // Per row: the group's lanes load their 16-byte chunks (chunk k of the row goes
 // to lane k mod G), take the max with a G-lane xor butterfly, compute
 // e = exp(x - m) once per element and keep it in registers, butterfly-sum e,
-// then write e * (1 / d) as 16-byte stores.  Each group walks rows with a grid
-// stride and issues the loads of its next row before working on the current
-// one, so a row's HBM latency overlaps the previous row's arithmetic.
+// then write e * (1 / d) as 16-byte stores.  The grid normally covers every
+// row once (many small CTAs: HBM latency is hidden by occupancy, and the tail
+// of the launch is one short CTA); a smaller grid walks the rows with a
+// stride.
 #pragma once
 
 #include "common.cuh"
@@ -31,48 +32,32 @@ __global__ void __launch_bounds__(kRowgroupThreads)
 {
     using M = Math<DT>;
     constexpr int E = Fmt<DT>::kPerChunk;
-    constexpr int kGroups = kRowgroupThreads / G;
+    const int groups = blockDim.x / G;  // rows per CTA per step
     const int gl = threadIdx.x & (G - 1);
-    const int64_t stride = (int64_t)gridDim.x * kGroups;
-    int64_t r = (int64_t)blockIdx.x * kGroups + threadIdx.x / G;
+    const int64_t stride = (int64_t)gridDim.x * groups;
     // every thread of a CTA runs the same number of iterations (the loop bound
     // is the CTA's first row), so the butterflies see converged warps.
-    int64_t base = (int64_t)blockIdx.x * kGroups;
-
-    uint4 nxt[V];
-#pragma unroll
-    for (int i = 0; i < V; i++)
-        nxt[i] = neg_inf_chunk<DT>();
-    if (r < rows) {
-        const RowGeom g = row_geom<DT, ALIGNED>(x, y, r, cols);
-#pragma unroll
-        for (int i = 0; i < V; i++)
-            nxt[i] = load_chunk<DT, ALIGNED>(g, gl + i * G, cols);
-    }
-    for (; base < rows; base += stride, r += stride) {
-        uint4 cur[V];
-#pragma unroll
-        for (int i = 0; i < V; i++)
-            cur[i] = nxt[i];
-        const int64_t rn = r + stride;
-        if (rn < rows) {
-            const RowGeom gn = row_geom<DT, ALIGNED>(x, y, rn, cols);
-#pragma unroll
-            for (int i = 0; i < V; i++)
-                nxt[i] = load_chunk<DT, ALIGNED>(gn, gl + i * G, cols);
-        }
+    for (int64_t base = (int64_t)blockIdx.x * groups; base < rows; base += stride) {
+        const int64_t r = base + threadIdx.x / G;
         const bool valid = r < rows;
+        const RowGeom g = row_geom<DT, ALIGNED>(x, y, valid ? r : 0, cols);
+
+        uint4 raw[V];
+#pragma unroll
+        for (int i = 0; i < V; i++)
+            raw[i] = valid ? load_chunk<DT, ALIGNED>(g, gl + i * G, cols) : neg_inf_chunk<DT>();
 
         float m = -INFINITY;
 #pragma unroll
         for (int i = 0; i < V; i++)
-            m = fmaxf(m, chunk_max<DT>(cur[i]));
+            m = fmaxf(m, chunk_max<DT>(raw[i]));
         m = G == 32 ? warp_max_redux(m) : group_max<G>(m);
+
         float v[V][E];
         typename M::Acc acc = M::zero();
 #pragma unroll
         for (int i = 0; i < V; i++) {
-            chunk_exp<DT>(cur[i], m, v[i]);
+            chunk_exp<DT>(raw[i], m, v[i]);
 #pragma unroll
             for (int e = 0; e < E; e++)
                 M::add(acc, v[i][e]);
@@ -81,7 +66,6 @@ __global__ void __launch_bounds__(kRowgroupThreads)
         const float inv = 1.0f / M::value(acc);
 
         if (valid) {
-            const RowGeom g = row_geom<DT, ALIGNED>(x, y, r, cols);
 #pragma unroll
             for (int i = 0; i < V; i++) {
                 const int64_t k = gl + i * G;
@@ -100,7 +84,7 @@ __global__ void __launch_bounds__(kRowgroupThreads)
 template <int DT, int G, int V, bool A>
 int rowgroup_launch_one(const Launch &l)
 {
-    k_rowgroup<DT, G, V, A><<<(unsigned)l.plan.grid_x, kRowgroupThreads, 0, (cudaStream_t)l.stream>>>(
+    k_rowgroup<DT, G, V, A><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
         (const char *)l.x, (char *)l.y, l.rows, l.cols, l.plan.y_vector);
     return (int)cudaGetLastError();
 }

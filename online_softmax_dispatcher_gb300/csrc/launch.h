@@ -11,9 +11,8 @@ struct CUstream_st;
 namespace osd {
 
 // Chunk counts and limits the dispatcher and the kernels agree on.
-constexpr int kRowgroupThreads = 256;   // CTA size of the lanes-per-row kernel
+constexpr int kRowgroupThreads = 256;   // largest CTA of the lanes-per-row kernel (the default)
 constexpr int kRowgroupMaxFloats = 32;  // V * E cached per lane (registers)
-constexpr int kRowgroupCtasPerSm = 16;  // grid cap of the lanes-per-row kernel, per SM
 constexpr int kBlockMaxChunks = 16;     // V of the block-per-row kernel
 constexpr int kStreamThreads = 512;     // CTA size of the streaming and split-k kernels
 constexpr int kStreamUnroll = 8;        // 16-byte loads in flight per thread per step
