@@ -512,9 +512,9 @@ __device__ __forceinline__ MD md_merge(const MD &a, const MD &b)
     const float m = fmaxf(a.m, b.m);
     if (m == -INFINITY)
         return MD{m, 0.f};
-    const float fa = (a.m == -INFINITY) ? 0.f : Math<DT>::exp_of(a.m - m);
-    const float fb = (b.m == -INFINITY) ? 0.f : Math<DT>::exp_of(b.m - m);
-    return MD{m, a.d * fa + b.d * fb};
+    const float da = (a.m == -INFINITY) ? 0.f : a.d * Math<DT>::exp_of(a.m - m);
+    const float db = (b.m == -INFINITY) ? 0.f : b.d * Math<DT>::exp_of(b.m - m);
+    return MD{m, da + db};
 }
 
 template <int DT>

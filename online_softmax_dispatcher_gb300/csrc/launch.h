@@ -14,9 +14,13 @@ namespace osd {
 constexpr int kRowgroupThreads = 256;   // largest CTA of the lanes-per-row kernel (the default)
 constexpr int kRowgroupMaxFloats = 32;  // V * E cached per lane (registers)
 constexpr int kBlockMaxChunks = 16;     // V of the block-per-row kernel
-constexpr int kStreamThreads = 512;     // CTA size of the streaming and split-k kernels
+constexpr int kStreamThreads = 512;     // CTA size of the streaming kernel
 constexpr int kStreamUnroll = 8;        // 16-byte loads in flight per thread per step
 constexpr int kMaxCluster = 16;         // non-portable cluster size limit
+constexpr int kSplitStages = 6;         // SPLITK: shared-memory ring depth
+constexpr int kSplitStageBytes = 32768; // SPLITK: bytes per stage (one bulk copy)
+constexpr int kSplitConsumerWarps = 16; // SPLITK: consumer warps per CTA
+constexpr int kSplitThreads = 32 * (1 + kSplitConsumerWarps);  // + one producer warp
 constexpr int kTmaConsumerWarps = 16;   // BLOCK_TMA: consumer warps per CTA
 constexpr int kTmaThreads = 32 * (1 + kTmaConsumerWarps);  // + one producer warp
 constexpr int kTmaMaxStagesHost = 8;    // BLOCK_TMA ring depth limit

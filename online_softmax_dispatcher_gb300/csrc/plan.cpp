@@ -173,12 +173,12 @@ void plan_stream(int64_t rows, softmax_launch_plan &p)
     p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
 }
 
-// Cluster size: enough CTAs to cover the SMs, at most 16, and at least two
-// full streaming steps of work per CTA.
+// Cluster size (power of two, <= 16): about two CTAs per SM over all rows,
+// and at least two full shared-memory stages of work per CTA.
 int splitk_cluster(const Geometry &g, int64_t rows, const softmax_device_info &dev)
 {
-    int64_t c = pow2_floor(dev.sm_count / (rows > 0 ? rows : 1));
-    const int64_t by_work = pow2_floor(g.nch_max / (2 * int64_t(kStreamThreads) * kStreamUnroll));
+    int64_t c = next_pow2(ceil_div(2 * int64_t(dev.sm_count > 0 ? dev.sm_count : 1), rows > 0 ? rows : 1));
+    const int64_t by_work = pow2_floor(g.nch_max / (2 * int64_t(kSplitStageBytes / 16)));
     if (c > by_work)
         c = by_work;
     if (c > kMaxCluster)
@@ -192,8 +192,9 @@ void plan_splitk(const Geometry &g, int64_t rows, const softmax_device_info &dev
 {
     const int c = splitk_cluster(g, rows, dev);
     p.variant = SOFTMAX_VARIANT_SPLITK;
-    p.chunks_per_thread = kStreamUnroll;
-    p.block_threads = kStreamThreads;
+    p.stages = kSplitStages;
+    p.smem_bytes = kSplitStages * kSplitStageBytes;
+    p.block_threads = kSplitThreads;
     p.cluster_x = c;
     p.grid_x = c;
     p.grid_y = rows;
@@ -201,7 +202,8 @@ void plan_splitk(const Geometry &g, int64_t rows, const softmax_device_info &dev
 
 bool splitk_possible(int64_t rows, const softmax_device_info &dev)
 {
-    return dev.cluster_launch && rows >= 1 && rows <= 65535;
+    return dev.cluster_launch && rows >= 1 && rows <= 65535 &&
+           dev.max_smem_optin >= kSplitStages * kSplitStageBytes + 1024;
 }
 
 }  // namespace
@@ -278,11 +280,12 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
             return SOFTMAX_ERR_INVALID_ARG;
         return SOFTMAX_OK;
     case SOFTMAX_VARIANT_SPLITK:
-        if (V != kStreamUnroll || p.block_threads > kStreamThreads)
+        if (p.block_threads != kSplitThreads || p.stages != kSplitStages ||
+            p.smem_bytes != kSplitStages * kSplitStageBytes)
             return SOFTMAX_ERR_INVALID_ARG;
         if (p.cluster_x < 1 || p.cluster_x > kMaxCluster || p.grid_x != p.cluster_x || p.grid_y != rows)
             return SOFTMAX_ERR_INVALID_ARG;
-        if (rows > 65535 || (p.cluster_x > 1 && !dev.cluster_launch))
+        if (rows > 65535 || !splitk_possible(rows, dev))
             return SOFTMAX_ERR_INVALID_ARG;
         return SOFTMAX_OK;
     default:
@@ -322,7 +325,7 @@ extern "C" __attribute__((visibility("default"))) int softmax_plan(
     int v = variant;
     if (v == SOFTMAX_VARIANT_AUTO) {
         const bool few_rows = rows * 2 <= dev->sm_count;
-        const bool long_rows = g.nch_max >= int64_t(4) * kStreamThreads * kStreamUnroll;
+        const bool long_rows = g.nch_max >= int64_t(8) * (kSplitStageBytes / 16);
         if (rowgroup_fits(g))
             v = SOFTMAX_VARIANT_ROWGROUP;
         else if (few_rows && long_rows && splitk_possible(rows, *dev))

@@ -18,6 +18,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // device error codes (low byte: which wait gave up)
 constexpr unsigned kErrFullWait = 1u;   // waiting for a bulk copy to land
 constexpr unsigned kErrEmptyWait = 2u;  // waiting for consumers to release a stage
+constexpr unsigned kErrPeerWait = 3u;   // waiting for a cluster peer's partial statistics
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -82,6 +83,78 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
                 return false;
         }
     }
+}
+
+// Wait with cluster-scope acquire (the phase was completed by arrivals of
+// other CTAs of the cluster); bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const volatile int *abort)
+{
+    if (mbar_try_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t n = 1;; n++) {
+        if (mbar_try_cluster(bar, parity))
+            return true;
+        if ((n & 15u) == 0) {
+            if (*abort)
+                return false;
+            if (global_ns() - t0 > kWaitLimitNs)
+                return false;
+        }
+    }
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Store two floats into a (possibly remote) CTA's shared memory.
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t raddr, float a, float b)
+{
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(raddr), "f"(a), "f"(b) : "memory");
+}
+
+// Arrive on a (possibly remote) CTA's mbarrier, releasing this thread's prior
+// writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t raddr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+
+// Full-cluster barrier (every thread of every CTA of the cluster).
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.

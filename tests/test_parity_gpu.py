@@ -176,6 +176,25 @@ def test_special_values():
                 assert np.isfinite(yd[[0, 4, 5]]).all()
 
 
+def test_long_runs_of_minus_inf():
+    """Whole thread / CTA shares of -inf next to finite values: the online
+    (m, d) passes must treat an all -inf share as empty, not as NaN."""
+    rng = np.random.default_rng(21)
+    for dt in (0, 1, 2):
+        for cols in (3000, 70000, 300000):
+            x = rng.normal(0, 3, (3, cols))
+            x[0, : cols // 2] = -np.inf       # first half
+            x[1, cols // 3:] = -np.inf        # last two thirds
+            x[2, ::2] = -np.inf               # every other element
+            x = x.astype(NUMPY[dt]) if dt != 2 else W._round_to(x, "bf16")
+            for v in variants_for(3, cols, dt):
+                rc, y = run(x, dt, variant=v)
+                assert rc == 0
+                check(x, y, dt)
+                yd = oracle.decode(y, dt)
+                assert (yd[oracle.decode(x, dt) == -np.inf] == 0).all(), NAMES[v]
+
+
 def test_extreme_magnitudes():
     for dt, big in ((0, 3.0e38), (1, 65504.0), (2, 3.0e38)):
         x = np.array([[big, -big, 0.0, big / 2], [-big, -big, -big, -big / 2], [1.0, -big, 2.0, 3.0]])
