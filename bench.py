@@ -188,18 +188,19 @@ def gpu_id_for_nvsmi() -> str | None:
 def kernel_fingerprint(variant: str) -> str:
     """Hash of the sources the dominant kernel is built from (invalidates stale ncu traffic)."""
     csrc = os.path.join(ROOT, "online_softmax_dispatcher_gb300", "csrc")
-    files = {"rowgroup": "k_rowgroup.cu", "block": "k_block.cu", "block_tma": "k_tma.cu",
-             "stream": "k_stream.cu", "splitk": "k_stream.cu"}
+    files = {"rowgroup": "k_rowgroup.cuh", "block": "k_block.cu", "block_tma": "k_tma.cu",
+             "stream": "k_stream.cu", "splitk": "k_splitk.cu"}
     h = hashlib.sha256()
-    for name in (files.get(variant, ""), "common.cuh", "tma.cuh", "launch.h", "plan.cpp"):
+    for name in (files.get(variant, ""), "common.cuh", "tma.cuh", "launch.h"):
         p = os.path.join(csrc, name)
         if name and os.path.exists(p):
             h.update(open(p, "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, variant: str) -> tuple[float | None, str]:
-    """dram bytes per launch from a committed ncu summary, if it matches the current kernel source."""
+def recorded_traffic(workload: str, variant: str, plan: dict) -> tuple[float | None, str]:
+    """dram bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source with the same launch plan."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -208,8 +209,8 @@ def recorded_traffic(workload: str, variant: str) -> tuple[float | None, str]:
         return None, "no ncu record"
     if not rec or rec.get("variant") != variant:
         return None, "no ncu record for this kernel"
-    if rec.get("fingerprint") != kernel_fingerprint(variant):
-        return None, "kernel changed since the ncu capture"
+    if rec.get("fingerprint") != kernel_fingerprint(variant) or rec.get("plan") != plan:
+        return None, "kernel or launch plan changed since the ncu capture"
     return float(rec["dram_bytes_per_launch"]), rec.get("source", "")
 
 
@@ -335,7 +336,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     peaks = load_peaks()
     per_launch_ms = ms / args.steps
     achieved = set_bytes / (per_launch_ms / 1e3) / 1e9
-    traffic, tsrc = recorded_traffic(w.name, variant)
+    traffic, tsrc = recorded_traffic(w.name, variant, plan.as_dict())
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
