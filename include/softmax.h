@@ -189,6 +189,16 @@ int softmax_device_query(softmax_device_info *dev);
  */
 int softmax_get_device_error(softmax_stream_t stream, unsigned int *code);
 
+/*
+ * softmax_selftest_bounded_wait -- diagnostic for the bounded-wait path above:
+ * enqueues on `stream` a one-CTA kernel whose thread waits on a shared-memory
+ * mbarrier that nothing arrives on, gives up after limit_us microseconds
+ * (1 .. 1000000), records code 1 in the device error word and returns -- no
+ * fault, no hang.  A following softmax_get_device_error(stream, &code) then
+ * reports SOFTMAX_ERR_DEVICE_TIMEOUT with code 1 and clears the word.
+ */
+int softmax_selftest_bounded_wait(softmax_stream_t stream, unsigned int limit_us);
+
 /* softmax_last_cuda_error -- the cudaError_t of the last failing CUDA call made
  * by this library on the calling thread (0 if none). */
 int softmax_last_cuda_error(void);

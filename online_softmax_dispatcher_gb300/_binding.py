@@ -43,6 +43,7 @@ EXPORTS = (
     "softmax_fwd", "softmax_fwd_variant", "softmax_fwd_plan", "softmax_query_variant",
     "softmax_plan", "softmax_device_query", "softmax_get_device_error",
     "softmax_last_cuda_error", "softmax_strerror", "softmax_variant_name", "softmax_abi_version",
+    "softmax_selftest_bounded_wait",
 )
 
 
@@ -104,6 +105,7 @@ def lib() -> ctypes.CDLL:
                 "softmax_strerror": [i32],
                 "softmax_variant_name": [i32],
                 "softmax_abi_version": [],
+                "softmax_selftest_bounded_wait": [vp, ctypes.c_uint],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -155,6 +157,10 @@ def softmax_get_device_error(stream: int = 0) -> tuple[int, int]:
     code = ctypes.c_uint(0)
     rc = lib().softmax_get_device_error(stream or None, ctypes.byref(code))
     return rc, code.value
+
+
+def softmax_selftest_bounded_wait(stream: int = 0, limit_us: int = 20000) -> int:
+    return lib().softmax_selftest_bounded_wait(stream or None, limit_us)
 
 
 def softmax_last_cuda_error() -> int:

@@ -9,6 +9,7 @@
 
 #include "launch.h"
 #include "softmax.h"
+#include "tma.cuh"
 
 #define OSD_API extern "C" __attribute__((visibility("default")))
 
@@ -18,6 +19,24 @@ namespace osd {
 // wait gives up.  Its device address is looked up once per device and passed
 // to the kernels (separate translation units cannot name it directly).
 __device__ unsigned int g_device_error;
+
+// Self-test of the bounded-wait machinery: one thread waits on an mbarrier
+// that nothing arrives on, gives up after `limit_ns`, records kErrFullWait in
+// the error word and returns (the same path a kernel takes when a bulk copy
+// never lands).
+__global__ void k_selftest_wait(unsigned *err, uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, &abort_flag, true, limit_ns))
+        atomicOr(err, kErrFullWait);
+}
 
 namespace {
 
@@ -214,6 +233,19 @@ OSD_API int softmax_get_device_error(softmax_stream_t stream, unsigned int *code
         return cuda_fail(e);
     *code = v;
     return v ? SOFTMAX_ERR_DEVICE_TIMEOUT : SOFTMAX_OK;
+}
+
+OSD_API int softmax_selftest_bounded_wait(softmax_stream_t stream, unsigned int limit_us)
+{
+    if (limit_us == 0 || limit_us > 1000000)
+        return SOFTMAX_ERR_INVALID_ARG;
+    DeviceCache *dc = nullptr;
+    const int rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    k_selftest_wait<<<1, 32, 0, (cudaStream_t)stream>>>(dc->error_word, (uint64_t)limit_us * 1000u);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SOFTMAX_OK : cuda_fail(e);
 }
 
 OSD_API int softmax_last_cuda_error(void) { return t_last_cuda_error; }

@@ -68,7 +68,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
 // Wait for the phase of parity `parity` to complete.  false: gave up (time
 // limit, or *abort raised by another thread when check_abort is set).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort,
-                                          bool check_abort = true)
+                                          bool check_abort = true, uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try(bar, parity))
         return true;
@@ -79,7 +79,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
         if ((n & 15u) == 0) {
             if (check_abort && *abort)
                 return false;
-            if (global_ns() - t0 > kWaitLimitNs)
+            if (global_ns() - t0 > limit_ns)
                 return false;
         }
     }

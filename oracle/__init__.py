@@ -20,6 +20,9 @@ module only builds that file and marshals numpy arrays into it:
                                with round-to-nearest-even from binary64.
 * ``check``                 -- streaming comparison of a candidate output with
                                the definition, row by row, over OpenMP threads.
+* ``softmax_bwd_f64``       -- the backward pass dx = y * (dy - sum dy*y), the
+                               derivative of the definition.
+* ``check_bwd``             -- streaming comparison of a candidate dx.
 
 bf16 arrays travel as ``numpy.uint16`` bit patterns (numpy has no bfloat16);
 fp16 arrays may be ``numpy.float16`` or ``numpy.uint16`` bit patterns.
@@ -127,8 +130,12 @@ class Oracle:
                                    ctypes.c_double, i64, ctypes.c_double, ctypes.c_double,
                                    ctypes.POINTER(CheckResult)]
         L.oracle_num_threads.argtypes = []
+        L.oracle_softmax_bwd_f64.argtypes = [vp, vp, i64, i64, vp]
+        L.oracle_check_bwd.argtypes = [vp, vp, vp, i32, i64, i64, ctypes.c_double, i64, ctypes.c_double,
+                                       ctypes.POINTER(CheckResult)]
         for name in ("oracle_decode", "oracle_encode", "oracle_softmax_f64", "oracle_softmax",
-                     "oracle_online_softmax_f64", "oracle_check", "oracle_num_threads"):
+                     "oracle_online_softmax_f64", "oracle_check", "oracle_num_threads",
+                     "oracle_softmax_bwd_f64", "oracle_check_bwd"):
             getattr(L, name).restype = ctypes.c_int
         self.lib = L
         self.path = path
@@ -204,6 +211,32 @@ class Oracle:
             raise ValueError("oracle_check rejected its arguments")
         return res.as_dict()
 
+    def softmax_bwd_f64(self, y: np.ndarray, dy: np.ndarray) -> np.ndarray:
+        """dx = y * (dy - sum(dy * y)) per row, binary64."""
+        y = np.ascontiguousarray(y, dtype=np.float64)
+        dy = np.ascontiguousarray(dy, dtype=np.float64)
+        if y.shape != dy.shape:
+            raise ValueError("y and dy shapes differ")
+        rows, cols = _rows_cols(y)
+        dx = np.empty_like(y)
+        rc = self.lib.oracle_softmax_bwd_f64(_ptr(y), _ptr(dy), rows, cols, _ptr(dx))
+        assert rc == 0
+        return dx
+
+    def check_bwd(self, y: np.ndarray, dy: np.ndarray, dx: np.ndarray, dtype: int, *, rel_tol: float = 0.0,
+                  max_ulp: int = 0, k_eps: float = 0.0) -> dict:
+        """Compare a candidate dx with the backward definition on the decoded y, dy."""
+        yb, dyb, dxb = _as_bits(y, dtype), _as_bits(dy, dtype), _as_bits(dx, dtype)
+        if not (yb.shape == dyb.shape == dxb.shape):
+            raise ValueError("shape mismatch")
+        rows, cols = _rows_cols(yb)
+        res = CheckResult()
+        rc = self.lib.oracle_check_bwd(_ptr(yb), _ptr(dyb), _ptr(dxb), dtype, rows, cols, float(rel_tol),
+                                       int(max_ulp), float(k_eps), ctypes.byref(res))
+        if rc != 0:
+            raise ValueError("oracle_check_bwd rejected its arguments")
+        return res.as_dict()
+
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
 
@@ -247,3 +280,11 @@ def check(x, y, dtype, **kw):
 
 def num_threads():
     return default().num_threads()
+
+
+def softmax_bwd_f64(y, dy):
+    return default().softmax_bwd_f64(y, dy)
+
+
+def check_bwd(y, dy, dx, dtype, **kw):
+    return default().check_bwd(y, dy, dx, dtype, **kw)

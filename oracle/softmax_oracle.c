@@ -471,3 +471,145 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------ */
+/* backward: dx = y * (dy - sum_k dy_k y_k)                                   */
+/* ------------------------------------------------------------------------ */
+
+/* The gradient of L(x) through y = softmax(x): dL/dx_j = sum_i dy_i dy_i/dx_j
+ * with dy_i/dx_j = y_i (delta_ij - y_j), i.e. dx_j = y_j (dy_j - s), s = sum_k
+ * dy_k y_k.  The pages name the backward pass as separate work ("Softmax on
+ * DCU", section 5.4, accuracy validation beyond inference); the formula is
+ * this derivative of the definition, written out. */
+static void softmax_bwd_row(const double *yr, const double *dyr, int64_t cols, double *dxr)
+{
+    double s = 0.0, c = 0.0;
+    for (int64_t j = 0; j < cols; j++) {
+        double t = dyr[j] * yr[j];
+        double u = s + t;
+        if (fabs(s) >= fabs(t))
+            c += (s - u) + t;
+        else
+            c += (t - u) + s;
+        s = u;
+    }
+    s += c;
+    for (int64_t j = 0; j < cols; j++)
+        dxr[j] = yr[j] * (dyr[j] - s);
+}
+
+int oracle_softmax_bwd_f64(const double *y, const double *dy, int64_t rows, int64_t cols, double *dx)
+{
+    if (rows < 0 || cols < 0 || (rows > 0 && cols > 0 && (!y || !dy || !dx)))
+        return ORACLE_EINVAL;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++)
+        softmax_bwd_row(y + r * cols, dy + r * cols, cols, dx + r * cols);
+    return ORACLE_OK;
+}
+
+/* spacing of the dtype at |v| (the ulp a value of that magnitude has) */
+static double dtype_ulp(double v, int dtype)
+{
+    int fbits = dtype == ORACLE_F32 ? 23 : (dtype == ORACLE_F16 ? 10 : 7);
+    int min_exp = dtype == ORACLE_F32 ? -126 : (dtype == ORACLE_F16 ? -14 : -126);
+    double a = fabs(v);
+    int k;
+    if (a == 0.0 || !isfinite(a))
+        return ldexp(1.0, min_exp - fbits);
+    frexp(a, &k);
+    int e = k - 1;
+    if (e < min_exp)
+        e = min_exp;
+    return ldexp(1.0, e - fbits);
+}
+
+/* Compare a candidate dx (dtype) with the backward definition applied to the
+ * decoded y and dy.  Element j passes when
+ *     |dx_j - dx*_j| <= max_ulp * ulp_dtype(dx*_j) + rel_tol * |dx*_j|
+ *                       + k_eps * 2^-24 * |y_j| * (|dy_j| + sum_k |dy_k y_k|)
+ * The last term is the fp32 cancellation budget of dy_j - s: it is the
+ * error an fp32 evaluation of s and of the difference carries relative to the
+ * magnitudes involved, which can exceed any relative bound on dx*_j when the
+ * difference nearly cancels. */
+int oracle_check_bwd(const void *y, const void *dy, const void *dx, int dtype, int64_t rows, int64_t cols,
+                     double rel_tol, int64_t max_ulp, double k_eps, oracle_check_result *res)
+{
+    if (!res || rows < 0 || cols < 0 || dtype < 0 || dtype > 2)
+        return ORACLE_EINVAL;
+    memset(res, 0, sizeof *res);
+    res->first_bad = -1;
+    if (rows == 0 || cols == 0)
+        return ORACLE_OK;
+    if (!y || !dy || !dx)
+        return ORACLE_EINVAL;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *ys = (double *)malloc((size_t)cols * sizeof(double));
+        double *dys = (double *)malloc((size_t)cols * sizeof(double));
+        double *want = (double *)malloc((size_t)cols * sizeof(double));
+        oracle_check_result loc;
+        memset(&loc, 0, sizeof loc);
+        loc.first_bad = -1;
+        if (!ys || !dys || !want) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; r++) {
+            if (!ys || !dys || !want)
+                continue;
+            double sabs = 0.0;
+            for (int64_t j = 0; j < cols; j++) {
+                ys[j] = decode_at(y, dtype, r * cols + j);
+                dys[j] = decode_at(dy, dtype, r * cols + j);
+                sabs += fabs(ys[j] * dys[j]);
+            }
+            softmax_bwd_row(ys, dys, cols, want);
+            for (int64_t j = 0; j < cols; j++) {
+                int64_t flat = r * cols + j;
+                double got = decode_at(dx, dtype, flat);
+                double w = want[j];
+                int bad;
+                if (isnan(w) || isnan(got)) {
+                    bad = !(isnan(w) && isnan(got));
+                } else {
+                    double err = fabs(got - w);
+                    double bound = (double)max_ulp * dtype_ulp(w, dtype) + rel_tol * fabs(w) +
+                                   k_eps * ldexp(1.0, -24) * fabs(ys[j]) * (fabs(dys[j]) + sabs);
+                    bad = !(err <= bound);
+                    if (!isfinite(got))
+                        loc.nonfinite++;
+                    double ulps = err / dtype_ulp(w, dtype);
+                    if ((int64_t)ulps > loc.max_ulp)
+                        loc.max_ulp = (int64_t)ulps;
+                    if (w != 0.0 && err / fabs(w) > loc.max_rel)
+                        loc.max_rel = err / fabs(w);
+                }
+                if (bad) {
+                    if (loc.first_bad < 0 || flat < loc.first_bad)
+                        loc.first_bad = flat;
+                    loc.violations++;
+                }
+                loc.checked++;
+            }
+        }
+#pragma omp critical
+        {
+            res->checked += loc.checked;
+            res->violations += loc.violations;
+            res->nonfinite += loc.nonfinite;
+            if (loc.first_bad >= 0 && (res->first_bad < 0 || loc.first_bad < res->first_bad))
+                res->first_bad = loc.first_bad;
+            if (loc.max_rel > res->max_rel)
+                res->max_rel = loc.max_rel;
+            if (loc.max_ulp > res->max_ulp)
+                res->max_ulp = loc.max_ulp;
+        }
+        free(ys);
+        free(dys);
+        free(want);
+    }
+    return failed ? ORACLE_EINVAL : ORACLE_OK;
+}

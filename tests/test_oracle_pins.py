@@ -274,6 +274,66 @@ def pin_check_helper(o):
     assert sel["violations"] == 0 and sel["checked"] == 100
 
 
+def pin_bwd_finite_difference(o):
+    # dx_i = d/dx_i sum_j softmax(x)_j dy_j, by central differences of the
+    # (separately pinned) forward definition
+    rng = np.random.default_rng(19)
+    x = rng.normal(0, 2, (3, 9))
+    dy = rng.normal(0, 1, (3, 9))
+    dx = o.softmax_bwd_f64(o.softmax_f64(x), dy)
+    h = 1e-6
+    for r in range(3):
+        for i in range(9):
+            xp, xm = x[r].copy(), x[r].copy()
+            xp[i] += h
+            xm[i] -= h
+            fd = (o.softmax_f64(xp[None]) @ dy[r] - o.softmax_f64(xm[None]) @ dy[r]) / (2 * h)
+            assert abs(fd[0] - dx[r, i]) <= 1e-8, (r, i, fd, dx[r, i])
+
+
+def pin_bwd_closed_forms(o):
+    rng = np.random.default_rng(20)
+    x = rng.normal(0, 3, (50, 2))
+    dy = rng.normal(0, 1, (50, 2))
+    y = o.softmax_f64(x)
+    dx = o.softmax_bwd_f64(y, dy)
+    want0 = y[:, 0] * y[:, 1] * (dy[:, 0] - dy[:, 1])
+    # dy_0 - s cancels when y_1 is small: the error budget is absolute in y |dy|
+    tol = 8 * 2.0**-52 * y[:, 0] * (np.abs(dy).sum(axis=1))
+    assert (np.abs(dx[:, 0] - want0) <= tol).all()
+    assert (np.abs(dx[:, 1] + want0) <= 8 * 2.0**-52 * y[:, 1] * np.abs(dy).sum(axis=1)).all()
+    # a constant upstream gradient has zero gradient; every row of dx sums to 0
+    y = o.softmax_f64(rng.normal(0, 5, (8, 300)))
+    assert np.abs(o.softmax_bwd_f64(y, np.full_like(y, 3.5))).max() <= 1e-14
+    dx = o.softmax_bwd_f64(y, rng.normal(0, 1, y.shape))
+    assert np.abs(dx.sum(axis=1)).max() <= 1e-14
+
+
+def pin_bwd_compensated_sum(o):
+    # one dominant entry and 1e5 entries of e^-40 relative to it, dy = 1: the
+    # exact gradient is 0, and s = sum dy*y = 1 only if the tiny terms are kept
+    n = 100_000
+    x = np.full((1, n + 1), -40.0)
+    x[0, 0] = 0.0
+    y = o.softmax_f64(x)
+    dx = o.softmax_bwd_f64(y, np.ones_like(y))
+    assert np.abs(dx).max() <= 1e-15, np.abs(dx).max()
+
+
+def pin_bwd_check_helper(o):
+    rng = np.random.default_rng(22)
+    y16 = o.softmax_rounded(rng.normal(0, 2, (4, 64)).astype(np.float16), F16)
+    dy16 = rng.normal(0, 1, (4, 64)).astype(np.float16).view(np.uint16)
+    want = o.softmax_bwd_f64(o.decode(y16, F16), o.decode(dy16, F16))
+    dx16 = o.encode(want, F16)
+    assert o.check_bwd(y16, dy16, dx16, F16, max_ulp=1, k_eps=4)["violations"] == 0
+    bad = dx16.copy()
+    j = int(np.argmax(np.abs(want[2])))
+    bad[2, j] ^= 0x0004  # 4 ulp away at the largest |dx|
+    r = o.check_bwd(y16, dy16, bad, F16, max_ulp=1, k_eps=4)
+    assert r["violations"] == 1 and r["first_bad"] == 2 * 64 + j
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
@@ -294,7 +354,9 @@ MUTANTS = [
     ("max_skips_first", "    double m = -INFINITY;\n    for (int64_t j = 0; j < cols; j++) {\n"
      "        if (isnan(xr[j]))", "    double m = -INFINITY;\n    for (int64_t j = 1; j < cols; j++) {\n"
      "        if (isnan(xr[j]))"),
-    ("compensation_sign", "            c += (s - u) + t;", "            c -= (s - u) + t;"),
+    ("compensation_sign", "        double t = exp(xr[j] - m);\n        double u = s + t;\n        if (fabs(s) >= fabs(t))\n"
+     "            c += (s - u) + t;", "        double t = exp(xr[j] - m);\n        double u = s + t;\n"
+     "        if (fabs(s) >= fabs(t))\n            c -= (s - u) + t;"),
     ("no_compensation", "    return s + c;\n}\n\n/* One row", "    return s;\n}\n\n/* One row"),
     ("ties_away", "(frac == 0.5 && fmod(r, 2.0) != 0.0)", "(frac == 0.5)"),
     ("f16_bias", "e - 25); /* (1 + f/1024)", "e - 24); /* (1 + f/1024)"),
@@ -306,6 +368,10 @@ MUTANTS = [
     ("check_off_by_one", "bad = dist > max_ulp;", "bad = dist > max_ulp + 1;"),
     ("subnormal_quantum", "q = ldexp(1.0, min_exp - fbits); /* subnormal quantum */",
      "q = ldexp(1.0, min_exp - fbits + 1); /* subnormal quantum */"),
+    ("bwd_sign", "dxr[j] = yr[j] * (dyr[j] - s);", "dxr[j] = yr[j] * (dyr[j] + s);"),
+    ("bwd_missing_y", "double t = dyr[j] * yr[j];", "double t = dyr[j];"),
+    ("bwd_drops_compensation", "    s += c;\n    for (int64_t j = 0; j < cols; j++)\n        dxr[j]",
+     "    for (int64_t j = 0; j < cols; j++)\n        dxr[j]"),
 ]
 
 

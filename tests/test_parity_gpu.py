@@ -279,6 +279,22 @@ def test_device_error_word_is_clear():
     assert rc == 0 and code == 0
 
 
+def test_bounded_wait_gives_up_and_reports():
+    """A wait that nothing satisfies gives up after its limit, the error word
+    reports it, and the context stays usable."""
+    s = torch.cuda.current_stream().cuda_stream
+    rc, code = osd.softmax_get_device_error(s)
+    assert rc == 0 and code == 0
+    assert osd.softmax_selftest_bounded_wait(s, 20000) == 0
+    rc, code = osd.softmax_get_device_error(s)
+    assert rc == -6 and code == 1
+    rc, code = osd.softmax_get_device_error(s)  # read-and-clear
+    assert rc == 0 and code == 0
+    x = torch.randn(64, 1000, device="cuda")
+    check(x.cpu().numpy(), osd.softmax(x).cpu().numpy(), 0)
+    assert osd.softmax_selftest_bounded_wait(s, 0) == -1
+
+
 def test_query_variant_matches_plan():
     x = torch.randn(65536, 512, device="cuda", dtype=torch.float16)
     y = torch.empty_like(x)
