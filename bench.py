@@ -270,12 +270,29 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     rows, cols, dt = w.rows, w.cols, w.dtype_code
     ptrs = [(a.data_ptr(), b.data_ptr()) for a, b in zip(xs, ys)]
     fwd = osd.lib().softmax_fwd
+    if args.op == "backward":
+        # y = softmax(x) (our forward), dy ~ N(0, 1); each step writes dx
+        for a, b in zip(xs, ys):
+            osd.softmax(a, out=b)
+        dys = [torch.randn(xs[0].shape, device=dev).to(xs[0].dtype) for _ in range(nbuf)]
+        dxs = [torch.empty_like(xs[0]) for _ in range(nbuf)]
+        ptrs3 = [(b.data_ptr(), d.data_ptr(), o.data_ptr()) for b, d, o in zip(ys, dys, dxs)]
+        set_bytes = set_bytes // 2 * 3
+        bwd = osd.lib().softmax_bwd
+        variant = "backward"
+        plan = osd.LaunchPlan()
 
-    def step(i):
-        xp, yp = ptrs[i % nbuf]
-        rc = fwd(xp, yp, rows, cols, dt, s)
-        if rc != 0:
-            raise osd.SoftmaxError(rc)
+        def step(i):
+            yp, dyp, dxp = ptrs3[i % nbuf]
+            rc = bwd(yp, dyp, dxp, rows, cols, dt, s)
+            if rc != 0:
+                raise osd.SoftmaxError(rc)
+    else:
+        def step(i):
+            xp, yp = ptrs[i % nbuf]
+            rc = fwd(xp, yp, rows, cols, dt, s)
+            if rc != 0:
+                raise osd.SoftmaxError(rc)
 
     for i in range(args.warmup):
         step(i)
@@ -341,7 +358,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "about": w.about,
+        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "about": w.about, "op": args.op,
                    "variant": variant, "plan": plan.as_dict(),
                    "l2": f"rotating {nbuf} buffer sets, {nbuf * set_bytes / 2**20:.0f} MiB > 2x L2 "
                          f"({l2 / 2**20:.0f} MiB)",
@@ -404,6 +421,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--rows", type=int, default=None,
                     help="time only the first ROWS rows of the workload (for small profiling captures)")
+    ap.add_argument("--op", choices=("forward", "backward"), default="forward",
+                    help="backward times softmax_bwd (dx = y*(dy - sum dy*y)) on the workload's shape; "
+                         "bytes = rows*cols*(2 reads + 1 write)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -115,6 +115,34 @@ int softmax_fwd_variant(const void *x, void *y, int64_t rows, int64_t cols, int 
                         int variant, softmax_stream_t stream);
 
 /*
+ * softmax_bwd -- the backward pass of softmax along the last dimension:
+ *     s_r = sum_k dy[r, k] * y[r, k];   dx[r, j] = y[r, j] * (dy[r, j] - s_r)
+ * the derivative of the definition above (dy_i/dx_j = y_i (delta_ij - y_j));
+ * "Softmax on DCU", section 5.4, names the backward pass as the work that
+ * follows the forward one.
+ *   y      device pointer, [rows, cols] of `dtype`: the forward output.
+ *   dy     device pointer, [rows, cols] of `dtype`: the upstream gradient.
+ *   dx     device pointer, [rows, cols] of `dtype`: written in full.
+ * s is accumulated in fp32 with compensated (TwoSum) additions; dx is rounded
+ * to nearest-even into `dtype`.  Accuracy against the exact result dx*:
+ *     |dx - dx*| <= u(dx*) + 8 * 2^-24 * y_j * (|dy_j| + sum_k |dy_k y_k|)
+ * with u = 1 ulp of the dtype at dx* for fp16 / bf16 and 2e-6 * |dx*| for
+ * fp32; the second term is the fp32 cancellation budget of dy_j - s.
+ * y and dy are only read (they may be the same buffer); dx must not overlap
+ * either (SOFTMAX_ERR_ALIAS).  Alignment, streams, errors: as softmax_fwd.
+ * Kernels: ROWGROUP (rows of up to 128 chunks of 16 bytes), BLOCK (up to 4096),
+ * STREAM (any).
+ */
+int softmax_bwd(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, int dtype,
+                softmax_stream_t stream);
+
+/* softmax_bwd_variant -- softmax_bwd with the kernel forced (ROWGROUP, BLOCK or
+ * STREAM; AUTO = softmax_bwd); SOFTMAX_ERR_UNSUPPORTED_SHAPE when it cannot
+ * serve the shape. */
+int softmax_bwd_variant(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, int dtype,
+                        int variant, softmax_stream_t stream);
+
+/*
  * softmax_query_variant -- the variant softmax_fwd would launch for these
  * arguments on the current device, written to *variant.  Validates the
  * arguments exactly as softmax_fwd does; launches nothing.

@@ -43,7 +43,7 @@ EXPORTS = (
     "softmax_fwd", "softmax_fwd_variant", "softmax_fwd_plan", "softmax_query_variant",
     "softmax_plan", "softmax_device_query", "softmax_get_device_error",
     "softmax_last_cuda_error", "softmax_strerror", "softmax_variant_name", "softmax_abi_version",
-    "softmax_selftest_bounded_wait",
+    "softmax_selftest_bounded_wait", "softmax_bwd", "softmax_bwd_variant",
 )
 
 
@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
                 "softmax_variant_name": [i32],
                 "softmax_abi_version": [],
                 "softmax_selftest_bounded_wait": [vp, ctypes.c_uint],
+                "softmax_bwd": [vp, vp, vp, i64, i64, i32, vp],
+                "softmax_bwd_variant": [vp, vp, vp, i64, i64, i32, i32, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -132,6 +134,15 @@ def softmax_fwd_variant(x: int, y: int, rows: int, cols: int, dtype: int, varian
 def softmax_fwd_plan(x: int, y: int, rows: int, cols: int, dtype: int, plan: LaunchPlan,
                      stream: int = 0) -> int:
     return lib().softmax_fwd_plan(x, y, rows, cols, dtype, ctypes.byref(plan), stream or None)
+
+
+def softmax_bwd(y: int, dy: int, dx: int, rows: int, cols: int, dtype: int, stream: int = 0) -> int:
+    return lib().softmax_bwd(y, dy, dx, rows, cols, dtype, stream or None)
+
+
+def softmax_bwd_variant(y: int, dy: int, dx: int, rows: int, cols: int, dtype: int, variant: int,
+                        stream: int = 0) -> int:
+    return lib().softmax_bwd_variant(y, dy, dx, rows, cols, dtype, variant, stream or None)
 
 
 def softmax_query_variant(x: int, y: int, rows: int, cols: int, dtype: int) -> tuple[int, int]:
@@ -236,6 +247,32 @@ def softmax(x, *, out=None, variant: int | str = VARIANT_AUTO, plan: LaunchPlan 
     if rc != OK:
         raise SoftmaxError(rc)
     return y
+
+
+def softmax_backward(y, dy, *, out=None, variant: int | str = VARIANT_AUTO, stream=None):
+    """dx = y * (dy - sum(dy * y, -1)) for contiguous CUDA tensors y (a softmax
+    output) and dy (its upstream gradient)."""
+    import torch
+
+    for name, t in (("y", y), ("dy", dy)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise SoftmaxError(ERR_INVALID_ARG, f"{name} must be a contiguous CUDA tensor")
+    if dy.shape != y.shape or dy.dtype != y.dtype or dy.device != y.device or y.dim() == 0:
+        raise SoftmaxError(ERR_INVALID_ARG, "y and dy must match in shape, dtype and device")
+    dt = dtype_code(y.dtype)
+    dx = torch.empty_like(y) if out is None else out
+    if dx.shape != y.shape or dx.dtype != y.dtype or not dx.is_contiguous() or dx.device != y.device:
+        raise SoftmaxError(ERR_INVALID_ARG, "out must match y in shape, dtype and device and be contiguous")
+    cols = y.shape[-1]
+    rows = y.numel() // cols if cols else 0
+    s = (stream or torch.cuda.current_stream(y.device)).cuda_stream
+    if isinstance(variant, str):
+        variant = VARIANTS[variant]
+    with torch.cuda.device(y.device):
+        rc = softmax_bwd_variant(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), rows, cols, dt, variant, s)
+    if rc != OK:
+        raise SoftmaxError(rc)
+    return dx
 
 
 def plan_for(x, y, variant: int | str = VARIANT_AUTO) -> LaunchPlan:

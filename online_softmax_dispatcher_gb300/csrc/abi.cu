@@ -161,6 +161,34 @@ OSD_API int softmax_fwd_variant(const void *x, void *y, int64_t rows, int64_t co
     return launch(*dc, x, y, rows, cols, dtype, plan, stream);
 }
 
+OSD_API int softmax_bwd_variant(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, int dtype,
+                                int variant, softmax_stream_t stream)
+{
+    int rc = validate_bwd_args(y, dy, dx, rows, cols, dtype);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (variant < SOFTMAX_VARIANT_AUTO || variant >= SOFTMAX_VARIANT_COUNT)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    DeviceCache *dc = nullptr;
+    rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    BwdLaunch l{y, dy, dx, rows, cols, dtype, {}, stream, 0, 0};
+    rc = plan_bwd(dc->info, y, dy, dx, rows, cols, dtype, variant, &l.plan, &l.dy_vec, &l.dx_vec);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    const int e = launch_bwd(l);
+    return e == 0 ? SOFTMAX_OK : cuda_fail((cudaError_t)e);
+}
+
+OSD_API int softmax_bwd(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, int dtype,
+                        softmax_stream_t stream)
+{
+    return softmax_bwd_variant(y, dy, dx, rows, cols, dtype, SOFTMAX_VARIANT_AUTO, stream);
+}
+
 OSD_API int softmax_fwd(const void *x, void *y, int64_t rows, int64_t cols, int dtype, softmax_stream_t stream)
 {
     return softmax_fwd_variant(x, y, rows, cols, dtype, SOFTMAX_VARIANT_AUTO, stream);

@@ -43,6 +43,29 @@ struct Launch {
     unsigned int *dev_err;  // device address of the library's error word
 };
 
+// Backward launch: dx = y * (dy - sum dy*y).  plan.aligned: y, dy and dx rows
+// all 16-byte aligned and whole chunks; dy_vec / dx_vec: that tensor's rows
+// share y's 16-byte phase.
+struct BwdLaunch {
+    const void *y;
+    const void *dy;
+    void *dx;
+    int64_t rows;
+    int64_t cols;
+    int dtype;
+    softmax_launch_plan plan;
+    CUstream_st *stream;
+    int dy_vec;
+    int dx_vec;
+};
+
+int launch_bwd(const BwdLaunch &l);
+
+// Backward dispatcher and validation (plan.cpp).
+int plan_bwd(const softmax_device_info &dev, const void *y, const void *dy, const void *dx, int64_t rows,
+             int64_t cols, int dtype, int variant, softmax_launch_plan *plan, int *dy_vec, int *dx_vec);
+int validate_bwd_args(const void *y, const void *dy, const void *dx, int64_t rows, int64_t cols, int dtype);
+
 // Each returns the cudaError_t of its launch (0 = success).
 int launch_rowgroup_f32(const Launch &l);
 int launch_rowgroup_f16(const Launch &l);

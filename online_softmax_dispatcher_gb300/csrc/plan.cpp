@@ -16,6 +16,8 @@
 //   otherwise                         -> SPLITK if rows < SMs, else STREAM
 #include <stdint.h>
 
+#include <initializer_list>
+
 #include "launch.h"
 
 namespace osd {
@@ -291,6 +293,99 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
     default:
         return SOFTMAX_ERR_INVALID_ARG;
     }
+}
+
+// ---------------------------------------------------------------- backward
+
+namespace {
+
+bool overlaps(const void *a, const void *b, uint64_t bytes)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    const uint64_t gap = x <= y ? (uint64_t)(y - x) : (uint64_t)(x - y);
+    return gap < bytes;
+}
+
+}  // namespace
+
+int validate_bwd_args(const void *y, const void *dy, const void *dx, int64_t rows, int64_t cols, int dtype)
+{
+    if (dtype < SOFTMAX_F32 || dtype > SOFTMAX_BF16)
+        return SOFTMAX_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || cols < 0)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    if (!y || !dy || !dx)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int64_t S = dtype_bytes(dtype);
+    if (cols > INT64_MAX / S || rows > INT64_MAX / (cols * S))
+        return SOFTMAX_ERR_INVALID_ARG;
+    for (const void *p : {y, dy, (const void *)dx})
+        if (reinterpret_cast<uintptr_t>(p) % S)
+            return SOFTMAX_ERR_INVALID_ARG;
+    const uint64_t bytes = (uint64_t)(rows * cols * S);
+    // y and dy are only read and may overlap; dx must not overlap either
+    if (overlaps(dx, y, bytes) || overlaps(dx, dy, bytes))
+        return SOFTMAX_ERR_ALIAS;
+    return SOFTMAX_OK;
+}
+
+// Backward dispatcher: lanes per row while y and dy fit 4 chunks per lane,
+// one CTA per row up to 2048 chunks (4 of each per thread: more spills
+// registers), then the two-pass streaming kernel.
+int plan_bwd(const softmax_device_info &dev, const void *y, const void *dy, const void *dx, int64_t rows,
+             int64_t cols, int dtype, int variant, softmax_launch_plan *plan, int *dy_vec, int *dx_vec)
+{
+    (void)dev;
+    const Geometry g = geometry(y, dx, cols, dtype);
+    const uintptr_t ya = reinterpret_cast<uintptr_t>(y), da = reinterpret_cast<uintptr_t>(dy);
+    const bool aligned = g.aligned && da % 16 == 0;
+    const int64_t nch = aligned ? g.row_bytes / 16 : ceil_div(g.row_bytes + 16 - g.S, 16);
+    softmax_launch_plan p = {};
+    p.grid_y = 1;
+    p.cluster_x = 1;
+    p.aligned = aligned;
+    p.y_vector = g.y_vec;
+    *dy_vec = ((da - ya) % 16) == 0;
+    *dx_vec = g.y_vec;
+    const bool rg_fits = nch <= 32 * 4;
+    const bool blk_fits = nch <= 512 * 4;
+    int v = variant;
+    if (v == SOFTMAX_VARIANT_AUTO)
+        v = rg_fits ? SOFTMAX_VARIANT_ROWGROUP : (blk_fits ? SOFTMAX_VARIANT_BLOCK : SOFTMAX_VARIANT_STREAM);
+    if (v == SOFTMAX_VARIANT_ROWGROUP) {
+        if (!rg_fits)
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        int64_t G = nch <= 4 ? next_pow2(nch) : next_pow2(ceil_div(nch, 4));
+        if (G > 32)
+            G = 32;
+        const int64_t V = next_pow2(ceil_div(nch, G));
+        p.variant = v;
+        p.lanes_per_row = (int)G;
+        p.chunks_per_thread = (int)V;
+        p.block_threads = kRowgroupThreads;
+        const int64_t ctas = ceil_div(rows, kRowgroupThreads / G);
+        p.grid_x = ctas < INT32_MAX ? ctas : INT32_MAX;
+    } else if (v == SOFTMAX_VARIANT_BLOCK) {
+        if (!blk_fits)
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        const int V = ceil_div(nch, 4) >= 32 ? 4 : 2;
+        int64_t T = ceil_div(ceil_div(nch, V), 32) * 32;
+        p.variant = v;
+        p.chunks_per_thread = V;
+        p.block_threads = (int)T;
+        p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
+    } else if (v == SOFTMAX_VARIANT_STREAM) {
+        p.variant = v;
+        p.chunks_per_thread = 4;
+        p.block_threads = kStreamThreads;
+        p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
+    } else {
+        return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+    }
+    *plan = p;
+    return SOFTMAX_OK;
 }
 
 }  // namespace osd
