@@ -85,7 +85,10 @@ typedef enum {
                                       any cols */
     SOFTMAX_VARIANT_SPLITK = 5,    /* a thread-block cluster per row; partial (m, d) merged
                                       through distributed shared memory */
-    SOFTMAX_VARIANT_COUNT = 6
+    SOFTMAX_VARIANT_SPLITK_WIDE = 6, /* P CTAs per row over all SMs, partials merged through a
+                                        global workspace in a second launch (softmax_fwd_ws
+                                        only: it needs the workspace) */
+    SOFTMAX_VARIANT_COUNT = 7
 } softmax_variant;
 
 /*
@@ -141,6 +144,34 @@ int softmax_bwd(const void *y, const void *dy, void *dx, int64_t rows, int64_t c
  * serve the shape. */
 int softmax_bwd_variant(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, int dtype,
                         int variant, softmax_stream_t stream);
+
+/*
+ * softmax_fwd_ws -- softmax_fwd with a caller-provided device workspace, which
+ * lets few, very long rows use every SM: each row is split over P CTAs (about
+ * two CTAs per SM over all rows) whose partial statistics are written to the
+ * workspace by a first launch and merged by every CTA of the row in a second
+ * launch that also writes y (SPLITK_WIDE; the split of "[CUDA] safe online
+ * softmax", section 3.2, with the caller owning the partials' memory).  For
+ * shapes that do not need it, or when workspace_bytes is smaller than
+ * softmax_workspace_size reports, it behaves exactly like softmax_fwd.
+ *   workspace        device pointer, 16-byte aligned, not overlapping x or y;
+ *                    NULL only with workspace_bytes == 0.  Its contents on
+ *                    entry do not matter; it is scratch until the second
+ *                    launch has finished (stream order).  Calls that share a
+ *                    workspace must not overlap on the GPU.
+ *   workspace_bytes  its size.
+ * Returns as softmax_fwd; SOFTMAX_ERR_ALIAS if the workspace overlaps x or y.
+ */
+int softmax_fwd_ws(const void *x, void *y, int64_t rows, int64_t cols, int dtype, void *workspace,
+                   uint64_t workspace_bytes, softmax_stream_t stream);
+
+/*
+ * softmax_workspace_size -- bytes of workspace softmax_fwd_ws uses for these
+ * arguments on the current device (0 when its choice needs none): rows * P *
+ * 16 with P the CTAs per row.  Validates the arguments as softmax_fwd does.
+ */
+int softmax_workspace_size(const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
+                           uint64_t *bytes);
 
 /*
  * softmax_query_variant -- the variant softmax_fwd would launch for these

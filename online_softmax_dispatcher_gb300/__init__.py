@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     SoftmaxLibraryMissing, dtype_code, lib, plan_for, softmax, softmax_abi_version,
     softmax_device_query, softmax_fwd, softmax_fwd_plan, softmax_fwd_variant,
     softmax_get_device_error, softmax_last_cuda_error, softmax_plan, softmax_query_variant,
-    softmax_selftest_bounded_wait, softmax_backward, softmax_bwd, softmax_bwd_variant,
+    softmax_selftest_bounded_wait, softmax_backward, softmax_bwd, softmax_bwd_variant, softmax_fwd_ws,
+    softmax_workspace_size,
     softmax_strerror, softmax_variant_name,
 )

@@ -31,8 +31,9 @@ VARIANT_BLOCK = 2
 VARIANT_BLOCK_TMA = 3
 VARIANT_STREAM = 4
 VARIANT_SPLITK = 5
-VARIANT_COUNT = 6
-VARIANTS = {"auto": 0, "rowgroup": 1, "block": 2, "block_tma": 3, "stream": 4, "splitk": 5}
+VARIANT_SPLITK_WIDE = 6
+VARIANT_COUNT = 7
+VARIANTS = {"auto": 0, "rowgroup": 1, "block": 2, "block_tma": 3, "stream": 4, "splitk": 5, "splitk_wide": 6}
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libosd_softmax.so")
@@ -43,7 +44,8 @@ EXPORTS = (
     "softmax_fwd", "softmax_fwd_variant", "softmax_fwd_plan", "softmax_query_variant",
     "softmax_plan", "softmax_device_query", "softmax_get_device_error",
     "softmax_last_cuda_error", "softmax_strerror", "softmax_variant_name", "softmax_abi_version",
-    "softmax_selftest_bounded_wait", "softmax_bwd", "softmax_bwd_variant",
+    "softmax_selftest_bounded_wait", "softmax_bwd", "softmax_bwd_variant", "softmax_fwd_ws",
+    "softmax_workspace_size",
 )
 
 
@@ -108,6 +110,8 @@ def lib() -> ctypes.CDLL:
                 "softmax_selftest_bounded_wait": [vp, ctypes.c_uint],
                 "softmax_bwd": [vp, vp, vp, i64, i64, i32, vp],
                 "softmax_bwd_variant": [vp, vp, vp, i64, i64, i32, i32, vp],
+                "softmax_fwd_ws": [vp, vp, i64, i64, i32, vp, ctypes.c_uint64, vp],
+                "softmax_workspace_size": [vp, vp, i64, i64, i32, ctypes.POINTER(ctypes.c_uint64)],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -134,6 +138,17 @@ def softmax_fwd_variant(x: int, y: int, rows: int, cols: int, dtype: int, varian
 def softmax_fwd_plan(x: int, y: int, rows: int, cols: int, dtype: int, plan: LaunchPlan,
                      stream: int = 0) -> int:
     return lib().softmax_fwd_plan(x, y, rows, cols, dtype, ctypes.byref(plan), stream or None)
+
+
+def softmax_fwd_ws(x: int, y: int, rows: int, cols: int, dtype: int, workspace: int, workspace_bytes: int,
+                   stream: int = 0) -> int:
+    return lib().softmax_fwd_ws(x, y, rows, cols, dtype, workspace or None, workspace_bytes, stream or None)
+
+
+def softmax_workspace_size(x: int, y: int, rows: int, cols: int, dtype: int) -> tuple[int, int]:
+    b = ctypes.c_uint64(0)
+    rc = lib().softmax_workspace_size(x, y, rows, cols, dtype, ctypes.byref(b))
+    return rc, b.value
 
 
 def softmax_bwd(y: int, dy: int, dx: int, rows: int, cols: int, dtype: int, stream: int = 0) -> int:
@@ -215,12 +230,14 @@ def dtype_code(t_dtype) -> int:
 
 
 def softmax(x, *, out=None, variant: int | str = VARIANT_AUTO, plan: LaunchPlan | None = None,
-            stream=None):
+            stream=None, workspace=None):
     """y = softmax(x) over the last dimension of a contiguous CUDA tensor.
 
     `out` (same shape and dtype, contiguous, not overlapping x) receives the
     result when given; `variant` forces a kernel; `plan` launches a
-    caller-built plan; `stream` is a torch.cuda.Stream (default: current).
+    caller-built plan; `stream` is a torch.cuda.Stream (default: current);
+    `workspace` (a CUDA tensor of at least softmax_workspace_size bytes) lets
+    few, very long rows use every SM (softmax_fwd_ws).
     """
     import torch
 
@@ -240,7 +257,12 @@ def softmax(x, *, out=None, variant: int | str = VARIANT_AUTO, plan: LaunchPlan 
     if isinstance(variant, str):
         variant = VARIANTS[variant]
     with torch.cuda.device(x.device):
-        if plan is not None:
+        if workspace is not None:
+            if plan is not None or variant != VARIANT_AUTO:
+                raise SoftmaxError(ERR_INVALID_ARG, "workspace goes with the dispatcher's choice only")
+            rc = softmax_fwd_ws(x.data_ptr(), y.data_ptr(), rows, cols, dt, workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), s)
+        elif plan is not None:
             rc = softmax_fwd_plan(x.data_ptr(), y.data_ptr(), rows, cols, dt, plan, s)
         else:
             rc = softmax_fwd_variant(x.data_ptr(), y.data_ptr(), rows, cols, dt, variant, s)

@@ -103,7 +103,8 @@ int current_device(DeviceCache **out)
 }
 
 int launch(const DeviceCache &dc, const void *x, void *y, int64_t rows, int64_t cols, int dtype,
-           const softmax_launch_plan &plan, softmax_stream_t stream)
+           const softmax_launch_plan &plan, softmax_stream_t stream, void *workspace = nullptr,
+           uint64_t workspace_bytes = 0)
 {
     // every plan, the dispatcher's own included, is checked before it runs
     const int rc = validate_plan(dc.info, x, y, rows, cols, dtype, plan);
@@ -112,6 +113,12 @@ int launch(const DeviceCache &dc, const void *x, void *y, int64_t rows, int64_t 
     Launch l{x, y, rows, cols, dtype, plan, stream, dc.error_word};
     int e;
     switch (plan.variant) {
+    case SOFTMAX_VARIANT_SPLITK_WIDE:
+        // needs the workspace only softmax_fwd_ws supplies
+        if (!workspace || workspace_bytes < wide_workspace_bytes(plan))
+            return SOFTMAX_ERR_INVALID_ARG;
+        e = launch_wide(l, workspace);
+        break;
     case SOFTMAX_VARIANT_ROWGROUP:
         e = launch_rowgroup(l);
         break;
@@ -209,6 +216,85 @@ OSD_API int softmax_fwd_plan(const void *x, void *y, int64_t rows, int64_t cols,
     if (rc != SOFTMAX_OK)
         return rc;
     return launch(*dc, x, y, rows, cols, dtype, *plan, stream);
+}
+
+namespace {
+
+// The plan softmax_fwd_ws launches: the dispatcher's choice, widened to
+// SPLITK_WIDE when it picked the cluster split (few, very long rows).
+int plan_ws(const DeviceCache &dc, const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
+            softmax_launch_plan *plan)
+{
+    int rc = softmax_plan(&dc.info, x, y, rows, cols, dtype, SOFTMAX_VARIANT_AUTO, plan);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (plan->variant == SOFTMAX_VARIANT_SPLITK) {
+        softmax_launch_plan wide;
+        if (softmax_plan(&dc.info, x, y, rows, cols, dtype, SOFTMAX_VARIANT_SPLITK_WIDE, &wide) == SOFTMAX_OK)
+            *plan = wide;
+    }
+    return SOFTMAX_OK;
+}
+
+bool ranges_overlap(const void *a, uint64_t na, const void *b, uint64_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+OSD_API int softmax_workspace_size(const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
+                                   uint64_t *bytes)
+{
+    if (!bytes)
+        return SOFTMAX_ERR_INVALID_ARG;
+    int rc = validate_args(x, y, rows, cols, dtype);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    *bytes = 0;
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    DeviceCache *dc = nullptr;
+    rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    softmax_launch_plan plan;
+    rc = plan_ws(*dc, x, y, rows, cols, dtype, &plan);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    *bytes = wide_workspace_bytes(plan);
+    return SOFTMAX_OK;
+}
+
+OSD_API int softmax_fwd_ws(const void *x, void *y, int64_t rows, int64_t cols, int dtype, void *workspace,
+                           uint64_t workspace_bytes, softmax_stream_t stream)
+{
+    int rc = validate_args(x, y, rows, cols, dtype);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if ((!workspace && workspace_bytes) || reinterpret_cast<uintptr_t>(workspace) % 16)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    const uint64_t nbytes = (uint64_t)(rows * cols * dtype_bytes(dtype));
+    if (workspace && workspace_bytes &&
+        (ranges_overlap(workspace, workspace_bytes, x, nbytes) || ranges_overlap(workspace, workspace_bytes, y, nbytes)))
+        return SOFTMAX_ERR_ALIAS;
+    DeviceCache *dc = nullptr;
+    rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    softmax_launch_plan plan;
+    rc = plan_ws(*dc, x, y, rows, cols, dtype, &plan);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (plan.variant == SOFTMAX_VARIANT_SPLITK_WIDE && (!workspace || workspace_bytes < wide_workspace_bytes(plan))) {
+        rc = softmax_plan(&dc->info, x, y, rows, cols, dtype, SOFTMAX_VARIANT_AUTO, &plan);
+        if (rc != SOFTMAX_OK)
+            return rc;
+    }
+    return launch(*dc, x, y, rows, cols, dtype, plan, stream, workspace, workspace_bytes);
 }
 
 OSD_API int softmax_query_variant(const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
@@ -315,6 +401,8 @@ OSD_API const char *softmax_variant_name(int variant)
         return "stream";
     case SOFTMAX_VARIANT_SPLITK:
         return "splitk";
+    case SOFTMAX_VARIANT_SPLITK_WIDE:
+        return "splitk_wide";
     default:
         return "unknown";
     }

@@ -1,0 +1,151 @@
+// k_wide.cu -- few rows, huge cols, on every SM: SPLITK_WIDE.
+//
+// A thread-block cluster holds at most 16 CTAs, so the cluster split (k_splitk)
+// puts at most 16 SMs on a row: 4 rows use 64 of 152 SMs.  This path splits
+// each row over P CTAs (about two per SM over all rows) and merges the partial
+// statistics through a small workspace in global memory, in two launches on
+// the caller's stream -- the split of "[CUDA] safe online softmax", section
+// 3.2 (pass 1 writes per-block partials, pass 2 merges them and writes), with
+// the partials merged by every CTA of the row in the same fixed order instead
+// of redundantly re-reduced per block:
+//
+// * k_wide_stats: CTA (p, r) reduces chunks [p * per, (p + 1) * per) of row r
+//   to one partial: fp16 / bf16 the online pair (m_p, d_p); fp32 its max m_p
+//   and then the compensated sum of exp(x - m_p) (a second pass over the
+//   segment, served by L2 on these shapes), so each partial is rescaled once
+//   in the merge and no rescale errors pile up.
+// * k_wide_write: every CTA of row r merges the P partials (lane i takes
+//   partials i, i + 32, ...; a fixed butterfly finishes), giving bit-identical
+//   (m, d) in all of them, then re-reads its segment and writes exp(x - m) / d.
+//
+// Workspace: rows * P slots of 16 bytes (float4: m, d or s, c, unused),
+// written by the first launch and read by the second; the caller provides it
+// (softmax_fwd_ws).
+#include "common.cuh"
+#include "launch.h"
+#include "stream_passes.cuh"
+
+namespace osd {
+
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(kStreamThreads)
+    k_wide_stats(const char *__restrict__ x, int64_t rows, int64_t cols, int P, float4 *__restrict__ ws)
+{
+    using M = Math<DT>;
+    __shared__ float smax[32];
+    __shared__ typename M::Acc ssum[32];
+    __shared__ MD smd[32];
+    const int64_t r = blockIdx.y;
+    const int p = blockIdx.x;
+    const RowGeom g = row_geom<DT, ALIGNED>(x, const_cast<char *>(x), r, cols);
+    const int64_t per = (g.nch + P - 1) / P;
+    const int64_t kb = per * p < g.nch ? per * p : g.nch;
+    const int64_t ke = kb + per < g.nch ? kb + per : g.nch;
+    float4 out;
+    if constexpr (DT == kF32) {
+        const float m = block_max(pass_max<DT, ALIGNED>(g, kb, ke, cols), smax);
+        CSum acc{0.f, 0.f};
+        if (m != -INFINITY)
+            acc = pass_sum<DT, ALIGNED>(g, kb, ke, cols, m);
+        acc = block_sum<DT>(acc, ssum);
+        out = make_float4(m, acc.s, acc.c, 0.f);
+    } else {
+        const MD md = block_md<DT>(pass_online<DT, ALIGNED>(g, kb, ke, cols), smd);
+        out = make_float4(md.m, md.d, 0.f, 0.f);
+    }
+    if (threadIdx.x == 0)
+        ws[r * P + p] = out;
+}
+
+// Merge the P partials of row r; every warp does it, identically.
+template <int DT>
+__device__ __forceinline__ void merge_partials(const float4 *ws, int64_t r, int P, float &m, float &inv)
+{
+    const int lane = threadIdx.x & 31;
+    if constexpr (DT == kF32) {
+        float mloc = -INFINITY;
+        for (int i = lane; i < P; i += 32)
+            mloc = fmaxf(mloc, ws[r * P + i].x);
+        m = group_max<32>(mloc);
+        CSum acc{0.f, 0.f};
+        for (int i = lane; i < P; i += 32) {
+            const float4 q = ws[r * P + i];
+            if (q.x != -INFINITY) {
+                // one rescale per partial: (s + c) * exp(m_p - m), exp_shift keeps
+                // m_p - m exact
+                const float f = Math<kF32>::exp_shift(q.x, m);
+                Math<kF32>::add(acc, q.y * f);
+                Math<kF32>::add(acc, q.z * f);
+            }
+        }
+        acc = group_sum<kF32, 32>(acc);
+        inv = 1.0f / (acc.s + acc.c);
+    } else {
+        MD md{-INFINITY, 0.f};
+        for (int i = lane; i < P; i += 32) {
+            const float4 q = ws[r * P + i];
+            md = md_merge<DT>(md, MD{q.x, q.y});
+        }
+        md = warp_md<DT>(md);
+        m = md.m;
+        inv = 1.0f / md.d;
+    }
+}
+
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(kStreamThreads)
+    k_wide_write(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int P,
+                 const float4 *__restrict__ ws, int y_vec)
+{
+    const int64_t r = blockIdx.y;
+    const int p = blockIdx.x;
+    const RowGeom g = row_geom<DT, ALIGNED>(x, y, r, cols);
+    const int64_t per = (g.nch + P - 1) / P;
+    const int64_t kb = per * p < g.nch ? per * p : g.nch;
+    const int64_t ke = kb + per < g.nch ? kb + per : g.nch;
+    float m, inv;
+    merge_partials<DT>(ws, r, P, m, inv);
+    pass_write<DT, ALIGNED>(g, kb, ke, cols, m, inv, y_vec != 0);
+}
+
+namespace {
+
+template <int DT, bool A>
+int wide_one(const Launch &l, float4 *ws)
+{
+    const dim3 grid((unsigned)l.plan.grid_x, (unsigned)l.plan.grid_y, 1);
+    const int P = (int)l.plan.grid_x;
+    k_wide_stats<DT, A><<<grid, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>((const char *)l.x, l.rows,
+                                                                                  l.cols, P, ws);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return (int)e;
+    k_wide_write<DT, A><<<grid, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
+        (const char *)l.x, (char *)l.y, l.rows, l.cols, P, ws, l.plan.y_vector);
+    return (int)cudaGetLastError();
+}
+
+template <int DT>
+int wide_dt(const Launch &l, float4 *ws)
+{
+    return l.plan.aligned ? wide_one<DT, true>(l, ws) : wide_one<DT, false>(l, ws);
+}
+
+}  // namespace
+
+int launch_wide(const Launch &l, void *workspace)
+{
+    float4 *ws = static_cast<float4 *>(workspace);
+    switch (l.dtype) {
+    case kF32:
+        return wide_dt<kF32>(l, ws);
+    case kF16:
+        return wide_dt<kF16>(l, ws);
+    case kBF16:
+        return wide_dt<kBF16>(l, ws);
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace osd

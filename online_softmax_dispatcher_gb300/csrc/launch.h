@@ -61,6 +61,10 @@ struct BwdLaunch {
 
 int launch_bwd(const BwdLaunch &l);
 
+// SPLITK_WIDE: two launches, partials in `workspace` (rows * grid_x float4).
+int launch_wide(const Launch &l, void *workspace);
+uint64_t wide_workspace_bytes(const softmax_launch_plan &p);
+
 // Backward dispatcher and validation (plan.cpp).
 int plan_bwd(const softmax_device_info &dev, const void *y, const void *dy, const void *dx, int64_t rows,
              int64_t cols, int dtype, int variant, softmax_launch_plan *plan, int *dy_vec, int *dx_vec);

@@ -202,6 +202,25 @@ void plan_splitk(const Geometry &g, int64_t rows, const softmax_device_info &dev
     p.grid_y = rows;
 }
 
+// SPLITK_WIDE: P CTAs per row, about two per SM over all rows, each with at
+// least one full streaming step per thread.
+void plan_wide(const Geometry &g, int64_t rows, const softmax_device_info &dev, softmax_launch_plan &p)
+{
+    int64_t P = ceil_div(2 * int64_t(dev.sm_count > 0 ? dev.sm_count : 1), rows > 0 ? rows : 1);
+    const int64_t by_work = g.nch_max / (int64_t(kStreamThreads) * kStreamUnroll);
+    if (P > by_work)
+        P = by_work;
+    if (P > 1024)
+        P = 1024;
+    if (P < 1)
+        P = 1;
+    p.variant = SOFTMAX_VARIANT_SPLITK_WIDE;
+    p.chunks_per_thread = kStreamUnroll;
+    p.block_threads = kStreamThreads;
+    p.grid_x = P;
+    p.grid_y = rows;
+}
+
 bool splitk_possible(int64_t rows, const softmax_device_info &dev)
 {
     return dev.cluster_launch && rows >= 1 && rows <= 65535 &&
@@ -281,6 +300,12 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
         if (V != kStreamUnroll || p.block_threads > kStreamThreads || p.grid_y != 1 || p.cluster_x != 1)
             return SOFTMAX_ERR_INVALID_ARG;
         return SOFTMAX_OK;
+    case SOFTMAX_VARIANT_SPLITK_WIDE:
+        if (V != kStreamUnroll || p.block_threads > kStreamThreads || p.cluster_x != 1)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.grid_y != rows || rows > 65535 || p.grid_x > 65535)
+            return SOFTMAX_ERR_INVALID_ARG;
+        return SOFTMAX_OK;
     case SOFTMAX_VARIANT_SPLITK:
         if (p.block_threads != kSplitThreads || p.stages != kSplitStages ||
             p.smem_bytes != kSplitStages * kSplitStageBytes)
@@ -293,6 +318,11 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
     default:
         return SOFTMAX_ERR_INVALID_ARG;
     }
+}
+
+uint64_t wide_workspace_bytes(const softmax_launch_plan &p)
+{
+    return p.variant == SOFTMAX_VARIANT_SPLITK_WIDE ? (uint64_t)p.grid_x * (uint64_t)p.grid_y * 16u : 0u;
 }
 
 // ---------------------------------------------------------------- backward
@@ -456,6 +486,11 @@ extern "C" __attribute__((visibility("default"))) int softmax_plan(
         if (!splitk_possible(rows, *dev))
             return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
         plan_splitk(g, rows, *dev, p);
+        break;
+    case SOFTMAX_VARIANT_SPLITK_WIDE:
+        if (rows > 65535)
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        plan_wide(g, rows, *dev, p);
         break;
     default:
         return SOFTMAX_ERR_UNSUPPORTED_SHAPE;

@@ -113,7 +113,7 @@ def _covers(p, rows, cols, elem, aligned):
         stage = p.smem_bytes // p.stages
         lead = 0 if aligned else 16 - elem
         return stage * 1 >= -(-(lead + p.rows_per_tile * cols * elem) // 16) * 16
-    return p.variant in (B.VARIANT_STREAM, B.VARIANT_SPLITK)
+    return p.variant in (B.VARIANT_STREAM, B.VARIANT_SPLITK, B.VARIANT_SPLITK_WIDE)
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
