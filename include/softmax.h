@@ -174,6 +174,32 @@ int softmax_workspace_size(const void *x, const void *y, int64_t rows, int64_t c
                            uint64_t *bytes);
 
 /*
+ * softmax_fwd_noalloc -- the SPLITK_WIDE path of softmax_fwd_ws for callers
+ * that may not allocate device memory themselves (a plugin whose host engine
+ * owns every device allocation and passes it only x and y; a latency-critical
+ * path where cudaMalloc, which may synchronise the device, is not allowed).
+ * It takes its scratch from a fixed array inside the library instead of a
+ * caller workspace and calls no allocating routine.  There is no counterpart
+ * on the pages: they allocate their split-k partials per call.
+ *   x, y, rows, cols, dtype, stream   as softmax_fwd.
+ * Always runs the two-launch wide split: each row is split over P CTAs
+ * (about 2 x SMs / rows, at least one 16-byte load step per thread, at most
+ * 1024) whose partial statistics go to the array.
+ * Limit: rows x P <= 4096 partial slots (the array is 64 KiB, held on every
+ * GPU that loads the library until the process exits); larger shapes return
+ * SOFTMAX_ERR_UNSUPPORTED_SHAPE.  On a 152-SM GB300 any rows <= 4096 fits.
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call shares the array and it keeps the last call's
+ * contents; nothing in it needs to start at zero (the first launch writes
+ * every slot the second reads).  Calls that overlap on the GPU -- on
+ * different streams, or from different host threads -- race on the array and
+ * must be serialised by the caller.
+ */
+int softmax_fwd_noalloc(const void *x, void *y, int64_t rows, int64_t cols, int dtype,
+                        softmax_stream_t stream);
+
+/*
  * softmax_query_variant -- the variant softmax_fwd would launch for these
  * arguments on the current device, written to *variant.  Validates the
  * arguments exactly as softmax_fwd does; launches nothing.

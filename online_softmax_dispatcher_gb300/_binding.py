@@ -45,7 +45,7 @@ EXPORTS = (
     "softmax_plan", "softmax_device_query", "softmax_get_device_error",
     "softmax_last_cuda_error", "softmax_strerror", "softmax_variant_name", "softmax_abi_version",
     "softmax_selftest_bounded_wait", "softmax_bwd", "softmax_bwd_variant", "softmax_fwd_ws",
-    "softmax_workspace_size",
+    "softmax_workspace_size", "softmax_fwd_noalloc",
 )
 
 
@@ -112,6 +112,7 @@ def lib() -> ctypes.CDLL:
                 "softmax_bwd_variant": [vp, vp, vp, i64, i64, i32, i32, vp],
                 "softmax_fwd_ws": [vp, vp, i64, i64, i32, vp, ctypes.c_uint64, vp],
                 "softmax_workspace_size": [vp, vp, i64, i64, i32, ctypes.POINTER(ctypes.c_uint64)],
+                "softmax_fwd_noalloc": [vp, vp, i64, i64, i32, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -143,6 +144,10 @@ def softmax_fwd_plan(x: int, y: int, rows: int, cols: int, dtype: int, plan: Lau
 def softmax_fwd_ws(x: int, y: int, rows: int, cols: int, dtype: int, workspace: int, workspace_bytes: int,
                    stream: int = 0) -> int:
     return lib().softmax_fwd_ws(x, y, rows, cols, dtype, workspace or None, workspace_bytes, stream or None)
+
+
+def softmax_fwd_noalloc(x: int, y: int, rows: int, cols: int, dtype: int, stream: int = 0) -> int:
+    return lib().softmax_fwd_noalloc(x, y, rows, cols, dtype, stream or None)
 
 
 def softmax_workspace_size(x: int, y: int, rows: int, cols: int, dtype: int) -> tuple[int, int]:

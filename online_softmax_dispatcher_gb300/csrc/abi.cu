@@ -143,6 +143,9 @@ int launch(const DeviceCache &dc, const void *x, void *y, int64_t rows, int64_t 
 }
 
 }  // namespace
+
+int record_cuda_error(int cuda_error) { return cuda_fail((cudaError_t)cuda_error); }
+
 }  // namespace osd
 
 using namespace osd;

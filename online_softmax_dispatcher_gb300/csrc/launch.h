@@ -61,6 +61,10 @@ struct BwdLaunch {
 
 int launch_bwd(const BwdLaunch &l);
 
+// Remember a failing cudaError_t for softmax_last_cuda_error (this thread) and
+// return SOFTMAX_ERR_CUDA.
+int record_cuda_error(int cuda_error);
+
 // SPLITK_WIDE: two launches, partials in `workspace` (rows * grid_x float4).
 int launch_wide(const Launch &l, void *workspace);
 uint64_t wide_workspace_bytes(const softmax_launch_plan &p);
