@@ -23,6 +23,9 @@ module only builds that file and marshals numpy arrays into it:
 * ``softmax_bwd_f64``       -- the backward pass dx = y * (dy - sum dy*y), the
                                derivative of the definition.
 * ``check_bwd``             -- streaming comparison of a candidate dx.
+* ``softmax_masked``        -- softmax(scale * x + mask) with an optional causal
+                               mask (attention scores).
+* ``check_masked``          -- streaming comparison against the masked form.
 
 bf16 arrays travel as ``numpy.uint16`` bit patterns (numpy has no bfloat16);
 fp16 arrays may be ``numpy.float16`` or ``numpy.uint16`` bit patterns.
@@ -131,11 +134,16 @@ class Oracle:
                                    ctypes.POINTER(CheckResult)]
         L.oracle_num_threads.argtypes = []
         L.oracle_softmax_bwd_f64.argtypes = [vp, vp, i64, i64, vp]
+        L.oracle_softmax_masked.argtypes = [vp, i32, i64, i64, ctypes.c_double, vp, i64, i64, vp]
+        L.oracle_check_masked.argtypes = [vp, vp, i32, i64, i64, ctypes.c_double, vp, i64, i64, ctypes.c_double,
+                                          ctypes.c_double, i64, ctypes.c_double, ctypes.c_double,
+                                          ctypes.c_double, ctypes.POINTER(CheckResult)]
         L.oracle_check_bwd.argtypes = [vp, vp, vp, i32, i64, i64, ctypes.c_double, i64, ctypes.c_double,
                                        ctypes.POINTER(CheckResult)]
         for name in ("oracle_decode", "oracle_encode", "oracle_softmax_f64", "oracle_softmax",
                      "oracle_online_softmax_f64", "oracle_check", "oracle_num_threads",
-                     "oracle_softmax_bwd_f64", "oracle_check_bwd"):
+                     "oracle_softmax_bwd_f64", "oracle_check_bwd", "oracle_softmax_masked",
+                     "oracle_check_masked"):
             getattr(L, name).restype = ctypes.c_int
         self.lib = L
         self.path = path
@@ -237,6 +245,40 @@ class Oracle:
             raise ValueError("oracle_check_bwd rejected its arguments")
         return res.as_dict()
 
+    def softmax_masked(self, x: np.ndarray, dtype: int, scale: float, mask: np.ndarray | None = None,
+                       causal_q: int = 0) -> np.ndarray:
+        """softmax(scale * x + mask) with an optional causal mask, binary64.
+        mask: [mask_rows, cols] in x's dtype; row r uses mask row r % mask_rows."""
+        xb = _as_bits(x, dtype)
+        rows, cols = _rows_cols(xb)
+        mb, mrows = None, 0
+        if mask is not None:
+            mb = _as_bits(mask, dtype)
+            mrows = _rows_cols(mb)[0]
+        y = np.empty((rows, cols), dtype=np.float64)
+        rc = self.lib.oracle_softmax_masked(_ptr(xb), dtype, rows, cols, float(scale),
+                                            _ptr(mb) if mb is not None else None, mrows, int(causal_q), _ptr(y))
+        assert rc == 0
+        return y
+
+    def check_masked(self, x, y, dtype, scale, mask=None, causal_q=0, *, rel_tol=0.0, abs_floor=0.0, max_ulp=0,
+                     rowsum_a=0.0, rowsum_b=0.0, zrel=0.0) -> dict:
+        """Compare a candidate with softmax(scale * x + mask) (+ causal mask)."""
+        xb, yb = _as_bits(x, dtype), _as_bits(y, dtype)
+        rows, cols = _rows_cols(xb)
+        mb, mrows = None, 0
+        if mask is not None:
+            mb = _as_bits(mask, dtype)
+            mrows = _rows_cols(mb)[0]
+        res = CheckResult()
+        rc = self.lib.oracle_check_masked(_ptr(xb), _ptr(yb), dtype, rows, cols, float(scale),
+                                          _ptr(mb) if mb is not None else None, mrows, int(causal_q),
+                                          float(rel_tol), float(abs_floor), int(max_ulp), float(rowsum_a),
+                                          float(rowsum_b), float(zrel), ctypes.byref(res))
+        if rc != 0:
+            raise ValueError("oracle_check_masked rejected its arguments")
+        return res.as_dict()
+
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
 
@@ -280,6 +322,14 @@ def check(x, y, dtype, **kw):
 
 def num_threads():
     return default().num_threads()
+
+
+def softmax_masked(x, dtype, scale, mask=None, causal_q=0):
+    return default().softmax_masked(x, dtype, scale, mask, causal_q)
+
+
+def check_masked(x, y, dtype, scale, mask=None, causal_q=0, **kw):
+    return default().check_masked(x, y, dtype, scale, mask, causal_q, **kw)
 
 
 def softmax_bwd_f64(y, dy):

@@ -341,14 +341,100 @@ static int row_is_finite(const double *xr, int64_t cols)
     return 1;
 }
 
-/* Compare y (same dtype and layout as x) with the definition applied to x.
- *   fp32:        |y - y*| <= rel_tol * y* + abs_floor
- *   fp16, bf16:  |bits(y) - bits(RNE_dtype(y*))| <= max_ulp  (outputs are >= 0,
+/* Tolerance parameters of a forward comparison. */
+typedef struct {
+    double rel_tol, abs_floor;
+    int64_t max_ulp;
+    double rowsum_a, rowsum_b;
+    double zrel; /* masked form: extra relative allowance zrel * max_j |z_j| */
+} oracle_tol;
+
+/* Compare row r of a candidate output y with the wanted row `want`:
+ *   fp32:        |y - y*| <= rel_tol * y* + abs_floor (+ zrel * zmax * y*)
+ *   fp16, bf16:  |bits(y) - bits(RNE_dtype(y*))| <= max_ulp (outputs are >= 0,
  *                so the bit distance is the distance in ulps, subnormals and
- *                zero included); a NaN matches only a NaN.
+ *                zero included), or |y - y*| <= zrel * zmax * y*; a NaN
+ *                matches only a NaN.
  *   row sums:    |sum_j y_j - 1| <= rowsum_a + cols * rowsum_b on rows with
- *                finite inputs, y_j decoded exactly and summed in binary64.
- * rows_sel (length n_sel) picks rows to check; NULL checks all rows. */
+ *                finite inputs, y_j decoded exactly and summed in binary64. */
+static void compare_row(const double *want, const void *y, int dtype, int64_t r, int64_t cols, int finite_row,
+                        double zmax, const oracle_tol *t, oracle_check_result *loc)
+{
+    double s = 0.0, c = 0.0;
+    for (int64_t j = 0; j < cols; j++) {
+        int64_t flat = r * cols + j;
+        double w = want[j];
+        double got = decode_at(y, dtype, flat);
+        double zallow = t->zrel * zmax * fabs(w);
+        int bad = 0;
+        if (finite_row && !isfinite(got))
+            loc->nonfinite++;
+        if (dtype == ORACLE_F32) {
+            if (isnan(w) || isnan(got)) {
+                bad = !(isnan(w) && isnan(got));
+            } else {
+                double err = fabs(got - w);
+                bad = !(err <= t->rel_tol * fabs(w) + t->abs_floor + zallow);
+                if (fabs(w) >= t->abs_floor && w != 0.0 && err / fabs(w) > loc->max_rel)
+                    loc->max_rel = err / fabs(w);
+            }
+        } else {
+            uint16_t gb = ((const uint16_t *)y)[flat];
+            uint16_t wb = dtype == ORACLE_F16 ? oracle_f64_to_f16(w) : oracle_f64_to_bf16(w);
+            if (isnan(w) || isnan(got)) {
+                bad = !(isnan(w) && isnan(got));
+            } else if ((gb | wb) & 0x8000u) {
+                bad = gb != wb; /* a negative output matches only exactly */
+            } else {
+                int64_t dist = gb > wb ? (int64_t)gb - wb : (int64_t)wb - gb;
+                if (dist > loc->max_ulp)
+                    loc->max_ulp = dist;
+                bad = dist > t->max_ulp && !(fabs(got - w) <= zallow);
+            }
+        }
+        if (bad) {
+            if (loc->first_bad < 0 || flat < loc->first_bad)
+                loc->first_bad = flat;
+            loc->violations++;
+        }
+        loc->checked++;
+        if (finite_row) {
+            double u = s + got;
+            if (fabs(s) >= fabs(got))
+                c += (s - u) + got;
+            else
+                c += (got - u) + s;
+            s = u;
+        }
+    }
+    if (finite_row) {
+        double dev = fabs((s + c) - 1.0);
+        if (!(dev <= t->rowsum_a + (double)cols * t->rowsum_b))
+            loc->rowsum_violations++;
+        if (dev > loc->max_rowsum_dev || isnan(dev))
+            loc->max_rowsum_dev = isnan(dev) ? INFINITY : dev;
+    }
+}
+
+static void merge_result(oracle_check_result *res, const oracle_check_result *loc)
+{
+    res->checked += loc->checked;
+    res->violations += loc->violations;
+    res->nonfinite += loc->nonfinite;
+    res->rowsum_violations += loc->rowsum_violations;
+    if (loc->first_bad >= 0 && (res->first_bad < 0 || loc->first_bad < res->first_bad))
+        res->first_bad = loc->first_bad;
+    if (loc->max_rel > res->max_rel)
+        res->max_rel = loc->max_rel;
+    if (loc->max_ulp > res->max_ulp)
+        res->max_ulp = loc->max_ulp;
+    if (loc->max_rowsum_dev > res->max_rowsum_dev)
+        res->max_rowsum_dev = loc->max_rowsum_dev;
+}
+
+/* Compare y (same dtype and layout as x) with the definition applied to x
+ * (compare_row gives the tolerances).  rows_sel (length n_sel) picks rows to
+ * check; NULL checks all rows. */
 int oracle_check(const void *x, const void *y, int dtype, int64_t rows, int64_t cols,
                  const int64_t *rows_sel, int64_t n_sel, double rel_tol, double abs_floor,
                  int64_t max_ulp, double rowsum_a, double rowsum_b, oracle_check_result *res)
@@ -365,6 +451,7 @@ int oracle_check(const void *x, const void *y, int dtype, int64_t rows, int64_t 
     for (int64_t i = 0; rows_sel && i < n; i++)
         if (rows_sel[i] < 0 || rows_sel[i] >= rows)
             return ORACLE_EINVAL;
+    const oracle_tol tol = {rel_tol, abs_floor, max_ulp, rowsum_a, rowsum_b, 0.0};
     int failed = 0;
 #pragma omp parallel
     {
@@ -385,77 +472,120 @@ int oracle_check(const void *x, const void *y, int dtype, int64_t rows, int64_t 
             for (int64_t j = 0; j < cols; j++)
                 xs[j] = decode_at(x, dtype, r * cols + j);
             softmax_row(xs, cols, ys);
-            int finite_row = row_is_finite(xs, cols);
-            double s = 0.0, c = 0.0;
-            for (int64_t j = 0; j < cols; j++) {
-                int64_t flat = r * cols + j;
-                double want = ys[j];
-                double got = decode_at(y, dtype, flat);
-                int bad = 0;
-                if (finite_row && !isfinite(got))
-                    loc.nonfinite++;
-                if (dtype == ORACLE_F32) {
-                    if (isnan(want) || isnan(got)) {
-                        bad = !(isnan(want) && isnan(got));
-                    } else {
-                        double err = fabs(got - want);
-                        bad = !(err <= rel_tol * fabs(want) + abs_floor);
-                        if (fabs(want) >= abs_floor && want != 0.0 && err / fabs(want) > loc.max_rel)
-                            loc.max_rel = err / fabs(want);
-                    }
-                } else {
-                    uint16_t gb = ((const uint16_t *)y)[flat];
-                    uint16_t wb = dtype == ORACLE_F16 ? oracle_f64_to_f16(want) : oracle_f64_to_bf16(want);
-                    if (isnan(want) || isnan(got)) {
-                        bad = !(isnan(want) && isnan(got));
-                    } else if ((gb | wb) & 0x8000u) {
-                        bad = gb != wb; /* a negative output matches only exactly */
-                    } else {
-                        int64_t dist = gb > wb ? (int64_t)gb - wb : (int64_t)wb - gb;
-                        if (dist > loc.max_ulp)
-                            loc.max_ulp = dist;
-                        bad = dist > max_ulp;
-                    }
-                }
-                if (bad) {
-                    if (loc.first_bad < 0 || flat < loc.first_bad)
-                        loc.first_bad = flat;
-                    loc.violations++;
-                }
-                loc.checked++;
-                if (finite_row) {
-                    double u = s + got;
-                    if (fabs(s) >= fabs(got))
-                        c += (s - u) + got;
-                    else
-                        c += (got - u) + s;
-                    s = u;
-                }
-            }
-            if (finite_row) {
-                double dev = fabs((s + c) - 1.0);
-                if (!(dev <= rowsum_a + (double)cols * rowsum_b))
-                    loc.rowsum_violations++;
-                if (dev > loc.max_rowsum_dev || isnan(dev))
-                    loc.max_rowsum_dev = isnan(dev) ? INFINITY : dev;
-            }
+            compare_row(ys, y, dtype, r, cols, row_is_finite(xs, cols), 0.0, &tol, &loc);
         }
 #pragma omp critical
-        {
-            res->checked += loc.checked;
-            res->violations += loc.violations;
-            res->nonfinite += loc.nonfinite;
-            res->rowsum_violations += loc.rowsum_violations;
-            if (loc.first_bad >= 0 && (res->first_bad < 0 || loc.first_bad < res->first_bad))
-                res->first_bad = loc.first_bad;
-            if (loc.max_rel > res->max_rel)
-                res->max_rel = loc.max_rel;
-            if (loc.max_ulp > res->max_ulp)
-                res->max_ulp = loc.max_ulp;
-            if (loc.max_rowsum_dev > res->max_rowsum_dev)
-                res->max_rowsum_dev = loc.max_rowsum_dev;
-        }
+        merge_result(res, &loc);
         free(xs);
+        free(ys);
+    }
+    return failed ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* scaled, masked softmax (attention scores)                                  */
+/* ------------------------------------------------------------------------ */
+
+/* The logits of row r:  z_j = scale * x_j + mask[r % mask_rows, j]  (mask may
+ * be absent), and with a causal mask (causal_q > 0) z_j = -inf for every key
+ * j > i + (cols - causal_q), i = r % causal_q the query index of the row (the
+ * query block is aligned to the end of the keys).  The scaled, additively
+ * masked softmax of "Softmax on DCU", section 9 (attention scores with scale
+ * and mask fused into the softmax) and the bias + mask + softmax fusion of the
+ * Pangu-Weather profile, section 6.  Binary64: scale * x is exact (24 x 24
+ * bits), the sum with the mask rounds once. */
+static void masked_logits(const void *x, const void *mask, int dtype, int64_t r, int64_t cols, double scale,
+                          int64_t mask_rows, int64_t causal_q, double *z)
+{
+    int64_t limit = cols; /* keys j < limit are visible */
+    if (causal_q > 0)
+        limit = r % causal_q + (cols - causal_q) + 1;
+    for (int64_t j = 0; j < cols; j++) {
+        double v = scale * decode_at(x, dtype, r * cols + j);
+        if (mask)
+            v += decode_at(mask, dtype, (r % mask_rows) * cols + j);
+        z[j] = j < limit ? v : -INFINITY;
+    }
+}
+
+int oracle_softmax_masked(const void *x, int dtype, int64_t rows, int64_t cols, double scale, const void *mask,
+                          int64_t mask_rows, int64_t causal_q, double *y)
+{
+    if (rows < 0 || cols < 0 || dtype < 0 || dtype > 2 || causal_q < 0 || (mask && mask_rows < 1) ||
+        (rows > 0 && cols > 0 && (!x || !y)))
+        return ORACLE_EINVAL;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *z = (rows > 0 && cols > 0) ? (double *)malloc((size_t)cols * sizeof(double)) : NULL;
+        if (rows > 0 && cols > 0 && !z) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < rows; r++) {
+            if (!z)
+                continue;
+            masked_logits(x, mask, dtype, r, cols, scale, mask_rows, causal_q, z);
+            softmax_row(z, cols, y + r * cols);
+        }
+        free(z);
+    }
+    return failed ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/* Compare a candidate with the masked definition; the tolerances of
+ * compare_row, plus zrel * max_j |z_j| relative (the rounding of the logits
+ * themselves in fp32). */
+int oracle_check_masked(const void *x, const void *y, int dtype, int64_t rows, int64_t cols, double scale,
+                        const void *mask, int64_t mask_rows, int64_t causal_q, double rel_tol, double abs_floor,
+                        int64_t max_ulp, double rowsum_a, double rowsum_b, double zrel, oracle_check_result *res)
+{
+    if (!res || rows < 0 || cols < 0 || dtype < 0 || dtype > 2 || causal_q < 0 || (mask && mask_rows < 1))
+        return ORACLE_EINVAL;
+    memset(res, 0, sizeof *res);
+    res->first_bad = -1;
+    if (rows == 0 || cols == 0)
+        return ORACLE_OK;
+    if (!x || !y)
+        return ORACLE_EINVAL;
+    const oracle_tol tol = {rel_tol, abs_floor, max_ulp, rowsum_a, rowsum_b, zrel};
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *z = (double *)malloc((size_t)cols * sizeof(double));
+        double *ys = (double *)malloc((size_t)cols * sizeof(double));
+        oracle_check_result loc;
+        memset(&loc, 0, sizeof loc);
+        loc.first_bad = -1;
+        if (!z || !ys) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; r++) {
+            if (!z || !ys)
+                continue;
+            masked_logits(x, mask, dtype, r, cols, scale, mask_rows, causal_q, z);
+            double zmax = 0.0;
+            int finite = 1;
+            for (int64_t j = 0; j < cols; j++) {
+                if (isnan(z[j]) || z[j] == INFINITY)
+                    finite = 0;
+                else if (isfinite(z[j]) && fabs(z[j]) > zmax)
+                    zmax = fabs(z[j]);
+            }
+            /* a row with no visible key is all -inf: finite inputs, NaN by the
+             * definition; treat it as non-finite for the row-sum check */
+            int any_visible = 0;
+            for (int64_t j = 0; j < cols; j++)
+                any_visible |= z[j] != -INFINITY;
+            softmax_row(z, cols, ys);
+            compare_row(ys, y, dtype, r, cols, finite && any_visible, zmax, &tol, &loc);
+        }
+#pragma omp critical
+        merge_result(res, &loc);
+        free(z);
         free(ys);
     }
     return failed ? ORACLE_EINVAL : ORACLE_OK;

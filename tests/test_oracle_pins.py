@@ -334,6 +334,60 @@ def pin_bwd_check_helper(o):
     assert r["violations"] == 1 and r["first_bad"] == 2 * 64 + j
 
 
+def pin_masked_reduces_to_plain(o):
+    rng = np.random.default_rng(30)
+    for dt, x in ((F32, rng.normal(0, 3, (6, 77)).astype(np.float32)),
+                  (F16, rng.normal(0, 3, (6, 77)).astype(np.float16)),
+                  (BF16, _bf16_bits_from_f32(rng.normal(0, 3, (6, 77))))):
+        assert np.array_equal(o.softmax_masked(x, dt, 1.0), o.softmax(x, dt))
+
+
+def pin_masked_scale_and_mask(o):
+    # scale by a power of two and an additive mask are exact in binary64, so the
+    # masked form must equal the plain definition on the transformed rows
+    rng = np.random.default_rng(31)
+    x = rng.normal(0, 10, (7, 50)).astype(np.float16)
+    mask = rng.normal(0, 4, (3, 50)).astype(np.float16)
+    got = o.softmax_masked(x, F16, 0.125, mask)
+    z = 0.125 * x.astype(np.float64) + mask.astype(np.float64)[np.arange(7) % 3]
+    assert np.allclose(got, scipy.special.softmax(z, axis=1), rtol=1e-14, atol=1e-300)
+    assert np.array_equal(got, o.softmax_f64(z))
+
+
+def pin_masked_causal_closed_form(o):
+    # zero logits: row i of a causal block sees i + 1 + (cols - q) keys, each 1/(that)
+    for q, cols in ((8, 8), (5, 12)):
+        x = np.zeros((2 * q, cols), dtype=np.float32)
+        y = o.softmax_masked(x, F32, 1.0, causal_q=q)
+        for r in range(2 * q):
+            vis = r % q + 1 + (cols - q)
+            assert np.allclose(y[r, :vis], 1.0 / vis, rtol=1e-15, atol=0)
+            assert (y[r, vis:] == 0).all()
+    # more queries than keys: the first rows see nothing -> NaN (definition of an all -inf row)
+    y = o.softmax_masked(np.zeros((4, 2), dtype=np.float32), F32, 1.0, causal_q=4)
+    assert np.isnan(y[:2]).all() and np.allclose(y[2], [1.0, 0.0]) and np.allclose(y[3], [0.5, 0.5])
+
+
+def pin_masked_check_helper(o):
+    rng = np.random.default_rng(32)
+    x = rng.normal(0, 8, (6, 40)).astype(np.float16)
+    mask = rng.normal(0, 2, (1, 40)).astype(np.float16)
+    want = o.encode(o.softmax_masked(x, F16, 0.25, mask, causal_q=3), F16)
+    kw = dict(max_ulp=1, rowsum_a=2**-10, rowsum_b=2**-24)
+    assert o.check_masked(x, want, F16, 0.25, mask, 3, **kw)["violations"] == 0
+    bad = want.copy()
+    bad[4, 1] += 3
+    r = o.check_masked(x, bad, F16, 0.25, mask, 3, **kw)
+    assert r["violations"] == 1 and r["first_bad"] == 4 * 40 + 1
+    # the logit allowance admits a relative error up to zrel * max|z|
+    bad = want.copy()
+    bad[0, 0] += 3
+    exact = o.softmax_masked(x, F16, 0.25, mask, causal_q=3)[0, 0]
+    rel = abs(o.decode(bad, F16)[0, 0] / exact - 1)
+    zmax = np.abs(0.25 * x[0].astype(np.float64) + mask[0].astype(np.float64))[:1 + 40 - 3].max()
+    assert o.check_masked(x, bad, F16, 0.25, mask, 3, zrel=1.01 * rel / zmax, **kw)["violations"] == 0
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
@@ -365,10 +419,15 @@ MUTANTS = [
     ("overflow_threshold", "if (isinf(a) || a >= ovf)", "if (isinf(a) || a > maxf)"),
     ("row_swapped", "softmax_row(x + r * cols, cols, y + r * cols);",
      "softmax_row(x + r * cols, cols, y + (rows - 1 - r) * cols);"),
-    ("check_off_by_one", "bad = dist > max_ulp;", "bad = dist > max_ulp + 1;"),
+    ("check_off_by_one", "bad = dist > t->max_ulp && ", "bad = dist > t->max_ulp + 1 && "),
     ("subnormal_quantum", "q = ldexp(1.0, min_exp - fbits); /* subnormal quantum */",
      "q = ldexp(1.0, min_exp - fbits + 1); /* subnormal quantum */"),
     ("bwd_sign", "dxr[j] = yr[j] * (dyr[j] - s);", "dxr[j] = yr[j] * (dyr[j] + s);"),
+    ("causal_off_by_one", "limit = r % causal_q + (cols - causal_q) + 1;", "limit = r % causal_q + (cols - causal_q);"),
+    ("mask_row_index", "v += decode_at(mask, dtype, (r % mask_rows) * cols + j);",
+     "v += decode_at(mask, dtype, (r % mask_rows) * cols + (cols - 1 - j));"),
+    ("scale_ignored", "double v = scale * decode_at(x, dtype, r * cols + j);",
+     "double v = decode_at(x, dtype, r * cols + j);"),
     ("bwd_missing_y", "double t = dyr[j] * yr[j];", "double t = dyr[j];"),
     ("bwd_drops_compensation", "    s += c;\n    for (int64_t j = 0; j < cols; j++)\n        dxr[j]",
      "    for (int64_t j = 0; j < cols; j++)\n        dxr[j]"),
