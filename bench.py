@@ -287,6 +287,17 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
             rc = bwd(yp, dyp, dxp, rows, cols, dt, s)
             if rc != 0:
                 raise osd.SoftmaxError(rc)
+    elif args.op == "masked":
+        masked = osd.lib().softmax_fwd_masked
+        causal_q = min(512, rows)
+        variant = "masked"
+        plan = osd.LaunchPlan()
+
+        def step(i):
+            xp, yp = ptrs[i % nbuf]
+            rc = masked(xp, yp, rows, cols, dt, 0.125, None, 0, causal_q, s)
+            if rc != 0:
+                raise osd.SoftmaxError(rc)
     else:
         def step(i):
             xp, yp = ptrs[i % nbuf]
@@ -421,9 +432,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--rows", type=int, default=None,
                     help="time only the first ROWS rows of the workload (for small profiling captures)")
-    ap.add_argument("--op", choices=("forward", "backward"), default="forward",
-                    help="backward times softmax_bwd (dx = y*(dy - sum dy*y)) on the workload's shape; "
-                         "bytes = rows*cols*(2 reads + 1 write)")
+    ap.add_argument("--op", choices=("forward", "backward", "masked"), default="forward",
+                    help="backward times softmax_bwd (dx = y*(dy - sum dy*y)) on the workload's shape, "
+                         "bytes = rows*cols*(2 reads + 1 write); masked times softmax_fwd_masked with scale 1/8 "
+                         "and a causal cut over query blocks of 512 rows (attention scores [B, H, 512, cols])")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -118,6 +118,41 @@ int softmax_fwd_variant(const void *x, void *y, int64_t rows, int64_t cols, int 
                         int variant, softmax_stream_t stream);
 
 /*
+ * softmax_fwd_masked -- scaled, masked softmax for attention scores:
+ *     z[r, j] = scale * x[r, j] + mask[r % mask_rows, j]        (mask optional)
+ *     with causal_q > 0:  z[r, j] = -inf for j > i + (cols - causal_q),
+ *                         i = r % causal_q (query blocks of causal_q rows whose
+ *                         last query sees every key)
+ *     y[r, :] = softmax(z[r, :])
+ * The scale and the masks are applied as x is loaded; the logits never go to
+ * memory ("Softmax on DCU", section 9: fuse the scale and the mask into the
+ * softmax for attention; the Pangu-Weather profile, section 6, tried a bias +
+ * mask + softmax fusion).  For attention scores [B, H, Sq, Sk]: rows = B*H*Sq,
+ * cols = Sk, scale = 1/sqrt(head dim), causal_q = Sq; a key-padding mask is
+ * [1, Sk] (mask_rows = 1), a per-query mask [Sq, Sk] (mask_rows = Sq).
+ *   mask       device pointer, [mask_rows, cols] of `dtype`, or NULL.  It may
+ *              overlap x (both are only read), not y (SOFTMAX_ERR_ALIAS).
+ *   mask_rows  >= 1 when mask is given (ignored otherwise).
+ *   causal_q   0 (no causal cut) or the query block length.  A row with no
+ *              visible key is all -inf and comes out NaN, as the definition
+ *              gives.
+ * Accuracy: as softmax_fwd against the exact softmax of z, with z formed in
+ * binary64; fp16 / bf16 additionally allow 2^-22 * max_j |z_j| relative (z is
+ * one fp32 FMA there), fp32 keeps 2e-6 (z is carried as a two-float pair).
+ * Rows up to 2048 chunks of 16 bytes (32 KiB: 16384 fp16 / bf16 or 8192 fp32
+ * keys): SOFTMAX_ERR_UNSUPPORTED_SHAPE beyond.  Alignment, streams, errors:
+ * as softmax_fwd.
+ */
+int softmax_fwd_masked(const void *x, void *y, int64_t rows, int64_t cols, int dtype, float scale,
+                       const void *mask, int64_t mask_rows, int64_t causal_q, softmax_stream_t stream);
+
+/* softmax_fwd_masked_variant -- softmax_fwd_masked with the kernel forced
+ * (ROWGROUP or BLOCK; AUTO = softmax_fwd_masked). */
+int softmax_fwd_masked_variant(const void *x, void *y, int64_t rows, int64_t cols, int dtype, float scale,
+                               const void *mask, int64_t mask_rows, int64_t causal_q, int variant,
+                               softmax_stream_t stream);
+
+/*
  * softmax_bwd -- the backward pass of softmax along the last dimension:
  *     s_r = sum_k dy[r, k] * y[r, k];   dx[r, j] = y[r, j] * (dy[r, j] - s_r)
  * the derivative of the definition above (dy_i/dx_j = y_i (delta_ij - y_j));

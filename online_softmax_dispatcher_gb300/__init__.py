@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     softmax_device_query, softmax_fwd, softmax_fwd_plan, softmax_fwd_variant,
     softmax_get_device_error, softmax_last_cuda_error, softmax_plan, softmax_query_variant,
     softmax_selftest_bounded_wait, softmax_backward, softmax_bwd, softmax_bwd_variant, softmax_fwd_ws,
-    softmax_workspace_size, softmax_fwd_noalloc,
+    softmax_workspace_size, softmax_fwd_noalloc, softmax_fwd_masked, softmax_fwd_masked_variant,
+    softmax_masked,
     softmax_strerror, softmax_variant_name,
 )

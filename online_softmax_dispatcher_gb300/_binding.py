@@ -45,7 +45,7 @@ EXPORTS = (
     "softmax_plan", "softmax_device_query", "softmax_get_device_error",
     "softmax_last_cuda_error", "softmax_strerror", "softmax_variant_name", "softmax_abi_version",
     "softmax_selftest_bounded_wait", "softmax_bwd", "softmax_bwd_variant", "softmax_fwd_ws",
-    "softmax_workspace_size", "softmax_fwd_noalloc",
+    "softmax_workspace_size", "softmax_fwd_noalloc", "softmax_fwd_masked", "softmax_fwd_masked_variant",
 )
 
 
@@ -113,6 +113,8 @@ def lib() -> ctypes.CDLL:
                 "softmax_fwd_ws": [vp, vp, i64, i64, i32, vp, ctypes.c_uint64, vp],
                 "softmax_workspace_size": [vp, vp, i64, i64, i32, ctypes.POINTER(ctypes.c_uint64)],
                 "softmax_fwd_noalloc": [vp, vp, i64, i64, i32, vp],
+                "softmax_fwd_masked": [vp, vp, i64, i64, i32, ctypes.c_float, vp, i64, i64, vp],
+                "softmax_fwd_masked_variant": [vp, vp, i64, i64, i32, ctypes.c_float, vp, i64, i64, i32, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -144,6 +146,18 @@ def softmax_fwd_plan(x: int, y: int, rows: int, cols: int, dtype: int, plan: Lau
 def softmax_fwd_ws(x: int, y: int, rows: int, cols: int, dtype: int, workspace: int, workspace_bytes: int,
                    stream: int = 0) -> int:
     return lib().softmax_fwd_ws(x, y, rows, cols, dtype, workspace or None, workspace_bytes, stream or None)
+
+
+def softmax_fwd_masked(x: int, y: int, rows: int, cols: int, dtype: int, scale: float, mask: int,
+                       mask_rows: int, causal_q: int, stream: int = 0) -> int:
+    return lib().softmax_fwd_masked(x, y, rows, cols, dtype, scale, mask or None, mask_rows, causal_q,
+                                    stream or None)
+
+
+def softmax_fwd_masked_variant(x: int, y: int, rows: int, cols: int, dtype: int, scale: float, mask: int,
+                               mask_rows: int, causal_q: int, variant: int, stream: int = 0) -> int:
+    return lib().softmax_fwd_masked_variant(x, y, rows, cols, dtype, scale, mask or None, mask_rows, causal_q,
+                                            variant, stream or None)
 
 
 def softmax_fwd_noalloc(x: int, y: int, rows: int, cols: int, dtype: int, stream: int = 0) -> int:
@@ -271,6 +285,37 @@ def softmax(x, *, out=None, variant: int | str = VARIANT_AUTO, plan: LaunchPlan 
             rc = softmax_fwd_plan(x.data_ptr(), y.data_ptr(), rows, cols, dt, plan, s)
         else:
             rc = softmax_fwd_variant(x.data_ptr(), y.data_ptr(), rows, cols, dt, variant, s)
+    if rc != OK:
+        raise SoftmaxError(rc)
+    return y
+
+
+def softmax_masked(x, *, scale: float = 1.0, mask=None, causal: bool = False, out=None,
+                   variant: int | str = VARIANT_AUTO, stream=None):
+    """softmax(scale * x + mask) over the last dimension with an optional causal
+    cut, for contiguous CUDA attention scores x of shape [..., Sq, Sk].  mask
+    (same dtype) broadcasts over the leading dimensions: [Sk], [1, Sk] or
+    [Sq, Sk]; causal=True cuts keys j > i + (Sk - Sq) for query i."""
+    import torch
+
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or not x.is_contiguous() or x.dim() == 0:
+        raise SoftmaxError(ERR_INVALID_ARG, "x must be a contiguous CUDA tensor")
+    dt = dtype_code(x.dtype)
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    mptr, mrows = 0, 0
+    if mask is not None:
+        if mask.dtype != x.dtype or not mask.is_cuda or not mask.is_contiguous() or mask.shape[-1] != cols:
+            raise SoftmaxError(ERR_INVALID_ARG, "mask must be a contiguous CUDA tensor [..., Sk] of x's dtype")
+        mptr, mrows = mask.data_ptr(), mask.numel() // cols
+    causal_q = (x.shape[-2] if x.dim() >= 2 else 1) if causal else 0
+    y = torch.empty_like(x) if out is None else out
+    s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
+    if isinstance(variant, str):
+        variant = VARIANTS[variant]
+    with torch.cuda.device(x.device):
+        rc = softmax_fwd_masked_variant(x.data_ptr(), y.data_ptr(), rows, cols, dt, float(scale), mptr, mrows,
+                                        causal_q, variant, s)
     if rc != OK:
         raise SoftmaxError(rc)
     return y

@@ -171,6 +171,46 @@ OSD_API int softmax_fwd_variant(const void *x, void *y, int64_t rows, int64_t co
     return launch(*dc, x, y, rows, cols, dtype, plan, stream);
 }
 
+OSD_API int softmax_fwd_masked_variant(const void *x, void *y, int64_t rows, int64_t cols, int dtype, float scale,
+                                      const void *mask, int64_t mask_rows, int64_t causal_q, int variant,
+                                      softmax_stream_t stream)
+{
+    int rc = validate_args(x, y, rows, cols, dtype);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (causal_q < 0 || variant < SOFTMAX_VARIANT_AUTO || variant >= SOFTMAX_VARIANT_COUNT)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (mask) {
+        const int64_t S = dtype_bytes(dtype);
+        if (mask_rows < 1 || reinterpret_cast<uintptr_t>(mask) % S || cols > INT64_MAX / S ||
+            mask_rows > INT64_MAX / (cols * S > 0 ? cols * S : 1))
+            return SOFTMAX_ERR_INVALID_ARG;
+        const uint64_t mbytes = (uint64_t)(mask_rows * cols * S), ybytes = (uint64_t)(rows * cols * S);
+        const uintptr_t ma = reinterpret_cast<uintptr_t>(mask), ya = reinterpret_cast<uintptr_t>(y);
+        if (ma < ya + ybytes && ya < ma + mbytes)
+            return SOFTMAX_ERR_ALIAS;
+    }
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    DeviceCache *dc = nullptr;
+    rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    MaskedLaunch l{x, y, rows, cols, dtype, {}, stream, scale, mask, mask_rows, causal_q};
+    rc = plan_masked(dc->info, x, y, rows, cols, dtype, variant, &l.plan);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    const int e = launch_masked(l);
+    return e == 0 ? SOFTMAX_OK : cuda_fail((cudaError_t)e);
+}
+
+OSD_API int softmax_fwd_masked(const void *x, void *y, int64_t rows, int64_t cols, int dtype, float scale,
+                               const void *mask, int64_t mask_rows, int64_t causal_q, softmax_stream_t stream)
+{
+    return softmax_fwd_masked_variant(x, y, rows, cols, dtype, scale, mask, mask_rows, causal_q,
+                                      SOFTMAX_VARIANT_AUTO, stream);
+}
+
 OSD_API int softmax_bwd_variant(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, int dtype,
                                 int variant, softmax_stream_t stream)
 {

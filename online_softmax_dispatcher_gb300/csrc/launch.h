@@ -61,6 +61,26 @@ struct BwdLaunch {
 
 int launch_bwd(const BwdLaunch &l);
 
+// Scaled, masked forward: y = softmax(scale * x + mask[r % mask_rows]) with an
+// optional causal cut; plan.variant ROWGROUP or BLOCK.
+struct MaskedLaunch {
+    const void *x;
+    void *y;
+    int64_t rows;
+    int64_t cols;
+    int dtype;
+    softmax_launch_plan plan;
+    CUstream_st *stream;
+    float scale;
+    const void *mask;
+    int64_t mask_rows;
+    int64_t causal_q;
+};
+
+int launch_masked(const MaskedLaunch &l);
+int plan_masked(const softmax_device_info &dev, const void *x, const void *y, int64_t rows, int64_t cols,
+                int dtype, int variant, softmax_launch_plan *plan);
+
 // Remember a failing cudaError_t for softmax_last_cuda_error (this thread) and
 // return SOFTMAX_ERR_CUDA.
 int record_cuda_error(int cuda_error);

@@ -325,6 +325,53 @@ uint64_t wide_workspace_bytes(const softmax_launch_plan &p)
     return p.variant == SOFTMAX_VARIANT_SPLITK_WIDE ? (uint64_t)p.grid_x * (uint64_t)p.grid_y * 16u : 0u;
 }
 
+// ---------------------------------------------------------------- masked forward
+
+// Lanes per row while the logits fit 32 registers per lane (4 chunks for every
+// dtype: fp32 keeps two floats per logit), else one CTA per row with x held
+// packed (up to 4 chunks per thread, 512 threads: 2048 chunks, 32 KiB rows).
+int plan_masked(const softmax_device_info &dev, const void *x, const void *y, int64_t rows, int64_t cols,
+                int dtype, int variant, softmax_launch_plan *plan)
+{
+    (void)dev;
+    const Geometry g = geometry(x, y, cols, dtype);
+    softmax_launch_plan p = {};
+    p.grid_y = 1;
+    p.cluster_x = 1;
+    p.aligned = g.aligned;
+    p.y_vector = g.y_vec;
+    const bool rg_fits = g.nch_max <= 32 * 4;
+    const bool blk_fits = g.nch_max <= 512 * 4;
+    int v = variant;
+    if (v == SOFTMAX_VARIANT_AUTO)
+        v = rg_fits ? SOFTMAX_VARIANT_ROWGROUP : SOFTMAX_VARIANT_BLOCK;
+    if (v == SOFTMAX_VARIANT_ROWGROUP) {
+        if (!rg_fits)
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        int64_t G = g.nch_max <= 4 ? next_pow2(g.nch_max) : next_pow2(ceil_div(g.nch_max, 4));
+        if (G > 32)
+            G = 32;
+        p.variant = v;
+        p.lanes_per_row = (int)G;
+        p.chunks_per_thread = (int)next_pow2(ceil_div(g.nch_max, G));
+        p.block_threads = kRowgroupThreads;
+        const int64_t ctas = ceil_div(rows, kRowgroupThreads / G);
+        p.grid_x = ctas < INT32_MAX ? ctas : INT32_MAX;
+    } else if (v == SOFTMAX_VARIANT_BLOCK) {
+        if (!blk_fits)
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        const int V = ceil_div(g.nch_max, 4) >= 32 ? 4 : 2;
+        p.variant = v;
+        p.chunks_per_thread = V;
+        p.block_threads = (int)(ceil_div(ceil_div(g.nch_max, V), 32) * 32);
+        p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
+    } else {
+        return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+    }
+    *plan = p;
+    return SOFTMAX_OK;
+}
+
 // ---------------------------------------------------------------- backward
 
 namespace {
