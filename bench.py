@@ -298,6 +298,22 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
             rc = masked(xp, yp, rows, cols, dt, 0.125, None, 0, causal_q, s)
             if rc != 0:
                 raise osd.SoftmaxError(rc)
+    elif args.workspace:
+        rc, need = osd.softmax_workspace_size(ptrs[0][0], ptrs[0][1], rows, cols, dt)
+        if rc != 0:
+            raise osd.SoftmaxError(rc)
+        wss = [torch.empty(max(need, 16), dtype=torch.uint8, device=dev) for _ in range(nbuf)]
+        wptrs = [(a, b, w.data_ptr()) for (a, b), w in zip(ptrs, wss)]
+        fwd_ws = osd.lib().softmax_fwd_ws
+        if need:
+            variant = "splitk_wide"
+            plan = osd.plan_for(xs[0], ys[0], "splitk_wide")
+
+        def step(i):
+            xp, yp, wp = wptrs[i % nbuf]
+            rc = fwd_ws(xp, yp, rows, cols, dt, wp, need, s)
+            if rc != 0:
+                raise osd.SoftmaxError(rc)
     else:
         def step(i):
             xp, yp = ptrs[i % nbuf]
@@ -370,6 +386,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "about": w.about, "op": args.op,
+                   "entry": "softmax_fwd_ws" if args.workspace else "softmax_fwd",
                    "variant": variant, "plan": plan.as_dict(),
                    "l2": f"rotating {nbuf} buffer sets, {nbuf * set_bytes / 2**20:.0f} MiB > 2x L2 "
                          f"({l2 / 2**20:.0f} MiB)",
@@ -384,7 +401,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         "e2e": {"value": round(set_bytes / (e2e_ms / 1e3) / 1e9 * ws, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size(), "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if variant == "splitk_wide" else 1),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -436,6 +453,9 @@ def main():
                     help="backward times softmax_bwd (dx = y*(dy - sum dy*y)) on the workload's shape, "
                          "bytes = rows*cols*(2 reads + 1 write); masked times softmax_fwd_masked with scale 1/8 "
                          "and a causal cut over query blocks of 512 rows (attention scores [B, H, 512, cols])")
+    ap.add_argument("--workspace", action="store_true",
+                    help="forward through softmax_fwd_ws with a workspace the bench allocates (lets few, very "
+                         "long rows use every SM)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -142,13 +142,16 @@ __global__ void __launch_bounds__(kRowgroupThreads) k_masked_rowgroup(const Mask
         const bool m_same = has_mask && ((reinterpret_cast<uintptr_t>(mrow) - reinterpret_cast<uintptr_t>(g.xr)) & 15) == 0;
         const int64_t limit = visible_limit(a, rr);
 
+        // chunks wholly past the causal limit are neither read nor exponentiated
         float zh[V][E], zl[V][E];
+        bool live[V];
 #pragma unroll
         for (int i = 0; i < V; i++) {
             const int64_t k = gl + i * G;
-            const uint4 xc = valid ? load_chunk<DT, ALIGNED>(g, k, a.cols) : neg_inf_chunk<DT>();
-            const uint4 mc = (valid && has_mask) ? load_mask_chunk<DT, ALIGNED>(g, mrow, m_same, k, a.cols)
-                                                 : make_uint4(0, 0, 0, 0);
+            live[i] = valid && k < g.nch && k * E - g.head < limit;
+            const uint4 xc = live[i] ? load_chunk<DT, ALIGNED>(g, k, a.cols) : neg_inf_chunk<DT>();
+            const uint4 mc = (live[i] && has_mask) ? load_mask_chunk<DT, ALIGNED>(g, mrow, m_same, k, a.cols)
+                                                   : make_uint4(0, 0, 0, 0);
             chunk_logits<DT, ALIGNED>(a, g, k, limit, xc, mc, has_mask, zh[i], zl[i]);
         }
         float m = -INFINITY;
@@ -160,12 +163,19 @@ __global__ void __launch_bounds__(kRowgroupThreads) k_masked_rowgroup(const Mask
         m = G == 32 ? warp_max_redux(m) : group_max<G>(m);
         typename M::Acc acc = M::zero();
 #pragma unroll
-        for (int i = 0; i < V; i++)
+        for (int i = 0; i < V; i++) {
+            if (live[i]) {
 #pragma unroll
-            for (int e = 0; e < E; e++) {
-                zh[i][e] = exp_logit<DT>(zh[i][e], zl[i][e], m);
-                M::add(acc, zh[i][e]);
+                for (int e = 0; e < E; e++) {
+                    zh[i][e] = exp_logit<DT>(zh[i][e], zl[i][e], m);
+                    M::add(acc, zh[i][e]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    zh[i][e] = 0.f;
             }
+        }
         acc = group_sum<DT, G>(acc);
         const float inv = 1.0f / M::value(acc);
         if (valid) {
@@ -201,14 +211,21 @@ __global__ void __launch_bounds__(512) k_masked_block(const MaskedArgs a)
         const bool m_same = has_mask && ((reinterpret_cast<uintptr_t>(mrow) - reinterpret_cast<uintptr_t>(g.xr)) & 15) == 0;
         const int64_t limit = visible_limit(a, r);
         // x stays packed in registers; the mask chunk is re-read each pass
+        // chunks wholly past the causal limit are not read (their logits are all
+        // -inf; exp gives the zeros the write pass stores)
+        const int lim32 = (int)limit;  // row-local: rows here are at most 32 KiB
+        auto live = [&](int64_t k) { return k < g.nch && (int)k * E - g.head < lim32; };
         auto logits = [&](const uint4 &xc, int64_t k, float(&zh)[E], float(&zl)[E]) {
-            const uint4 mc = has_mask ? load_mask_chunk<DT, ALIGNED>(g, mrow, m_same, k, a.cols) : make_uint4(0, 0, 0, 0);
+            const uint4 mc = (has_mask && live(k)) ? load_mask_chunk<DT, ALIGNED>(g, mrow, m_same, k, a.cols)
+                                                   : make_uint4(0, 0, 0, 0);
             chunk_logits<DT, ALIGNED>(a, g, k, limit, xc, mc, has_mask, zh, zl);
         };
         uint4 xc[V];
 #pragma unroll
-        for (int i = 0; i < V; i++)
-            xc[i] = load_chunk<DT, ALIGNED>(g, t + (int64_t)i * T, a.cols);
+        for (int i = 0; i < V; i++) {
+            const int64_t k = t + (int64_t)i * T;
+            xc[i] = live(k) ? load_chunk<DT, ALIGNED>(g, k, a.cols) : neg_inf_chunk<DT>();
+        }
         float m = -INFINITY;
 #pragma unroll
         for (int i = 0; i < V; i++) {
