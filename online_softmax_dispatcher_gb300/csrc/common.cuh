@@ -179,6 +179,7 @@ struct RowGeom {
     char *yr;         // y row start
     int head;         // elements of chunk 0 that precede the row (0 when aligned)
     int64_t nch;      // chunks covering the row
+    int64_t kf, kl;   // chunks [kf, kl) lie wholly inside the row
 };
 
 template <int DT, bool ALIGNED>
@@ -194,6 +195,8 @@ __device__ __forceinline__ RowGeom row_geom(const char *x, char *y, int64_t r, i
         g.y0 = g.yr;
         g.head = 0;
         g.nch = row_bytes >> 4;
+        g.kf = 0;
+        g.kl = g.nch;
     } else {
         const uintptr_t a = reinterpret_cast<uintptr_t>(g.xr);
         const int lead = (int)(a & 15);
@@ -201,6 +204,8 @@ __device__ __forceinline__ RowGeom row_geom(const char *x, char *y, int64_t r, i
         g.y0 = g.yr - lead;
         g.head = lead / S;
         g.nch = (lead + row_bytes + 15) >> 4;
+        g.kf = lead ? 1 : 0;
+        g.kl = ((lead + row_bytes) & 15) ? g.nch - 1 : g.nch;
     }
     return g;
 }
@@ -238,10 +243,9 @@ __device__ __forceinline__ uint4 load_chunk(const RowGeom &g, int64_t k, int64_t
     if constexpr (ALIGNED) {
         return ld_chunk(g.x0 + 16 * k);
     } else {
-        const int64_t j0 = k * E - g.head;
-        if (j0 >= 0 && j0 + E <= cols)
+        if (k >= g.kf && k < g.kl)
             return ld_chunk(g.x0 + 16 * k);
-        return ld_partial<DT>(g.xr, j0, cols);
+        return ld_partial<DT>(g.xr, k * E - g.head, cols);
     }
 }
 
@@ -257,11 +261,11 @@ __device__ __forceinline__ void store_chunk(const RowGeom &g, int64_t k, int64_t
     if constexpr (ALIGNED) {
         st_chunk(g.y0 + 16 * k, p);
     } else {
-        const int64_t j0 = k * E - g.head;
-        if (y_vec && j0 >= 0 && j0 + E <= cols) {
+        if (y_vec && k >= g.kf && k < g.kl) {
             st_chunk(g.y0 + 16 * k, p);
             return;
         }
+        const int64_t j0 = k * E - g.head;
         const uint32_t w[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
         for (int e = 0; e < E; e++) {

@@ -27,8 +27,12 @@
 
 namespace osd {
 
+// kWideStep (4) chunks in flight per thread per step keeps both kernels within
+// the 64 registers that two 512-thread CTAs per SM leave; x re-reads in
+// k_wide_write are L2 hits, every row segment having been read by k_wide_stats
+// just before.
 template <int DT, bool ALIGNED>
-__global__ void __launch_bounds__(kStreamThreads)
+__global__ void __launch_bounds__(kStreamThreads, 2)
     k_wide_stats(const char *__restrict__ x, int64_t rows, int64_t cols, int P, float4 *__restrict__ ws)
 {
     using M = Math<DT>;
@@ -43,14 +47,14 @@ __global__ void __launch_bounds__(kStreamThreads)
     const int64_t ke = kb + per < g.nch ? kb + per : g.nch;
     float4 out;
     if constexpr (DT == kF32) {
-        const float m = block_max(pass_max<DT, ALIGNED>(g, kb, ke, cols), smax);
+        const float m = block_max(pass_max<DT, ALIGNED, kWideStep>(g, kb, ke, cols), smax);
         CSum acc{0.f, 0.f};
         if (m != -INFINITY)
-            acc = pass_sum<DT, ALIGNED>(g, kb, ke, cols, m);
+            acc = pass_sum<DT, ALIGNED, kWideStep>(g, kb, ke, cols, m);
         acc = block_sum<DT>(acc, ssum);
         out = make_float4(m, acc.s, acc.c, 0.f);
     } else {
-        const MD md = block_md<DT>(pass_online<DT, ALIGNED>(g, kb, ke, cols), smd);
+        const MD md = block_md<DT>(pass_online<DT, ALIGNED, kWideStep>(g, kb, ke, cols), smd);
         out = make_float4(md.m, md.d, 0.f, 0.f);
     }
     if (threadIdx.x == 0)
@@ -93,7 +97,7 @@ __device__ __forceinline__ void merge_partials(const float4 *ws, int64_t r, int 
 }
 
 template <int DT, bool ALIGNED>
-__global__ void __launch_bounds__(kStreamThreads)
+__global__ void __launch_bounds__(kStreamThreads, 2)
     k_wide_write(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int P,
                  const float4 *__restrict__ ws, int y_vec)
 {
@@ -105,7 +109,7 @@ __global__ void __launch_bounds__(kStreamThreads)
     const int64_t ke = kb + per < g.nch ? kb + per : g.nch;
     float m, inv;
     merge_partials<DT>(ws, r, P, m, inv);
-    pass_write<DT, ALIGNED>(g, kb, ke, cols, m, inv, y_vec != 0);
+    pass_write<DT, ALIGNED, kWideStep>(g, kb, ke, cols, m, inv, y_vec != 0);
 }
 
 namespace {

@@ -16,6 +16,7 @@ constexpr int kRowgroupMaxFloats = 32;  // V * E cached per lane (registers)
 constexpr int kBlockMaxChunks = 16;     // V of the block-per-row kernel
 constexpr int kStreamThreads = 512;     // CTA size of the streaming kernel
 constexpr int kStreamUnroll = 8;        // 16-byte loads in flight per thread per step
+constexpr int kWideStep = 4;            // the same for the wide split: 64 registers at two 512-thread CTAs per SM
 constexpr int kMaxCluster = 16;         // non-portable cluster size limit
 constexpr int kSplitStages = 6;         // SPLITK: shared-memory ring depth
 constexpr int kSplitStageBytes = 32768; // SPLITK: bytes per stage (one bulk copy)

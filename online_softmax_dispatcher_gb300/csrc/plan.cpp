@@ -207,7 +207,7 @@ void plan_splitk(const Geometry &g, int64_t rows, const softmax_device_info &dev
 void plan_wide(const Geometry &g, int64_t rows, const softmax_device_info &dev, softmax_launch_plan &p)
 {
     int64_t P = ceil_div(2 * int64_t(dev.sm_count > 0 ? dev.sm_count : 1), rows > 0 ? rows : 1);
-    const int64_t by_work = g.nch_max / (int64_t(kStreamThreads) * kStreamUnroll);
+    const int64_t by_work = g.nch_max / (int64_t(kStreamThreads) * kWideStep);
     if (P > by_work)
         P = by_work;
     if (P > 1024)
@@ -215,7 +215,7 @@ void plan_wide(const Geometry &g, int64_t rows, const softmax_device_info &dev, 
     if (P < 1)
         P = 1;
     p.variant = SOFTMAX_VARIANT_SPLITK_WIDE;
-    p.chunks_per_thread = kStreamUnroll;
+    p.chunks_per_thread = kWideStep;
     p.block_threads = kStreamThreads;
     p.grid_x = P;
     p.grid_y = rows;
@@ -301,7 +301,7 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
             return SOFTMAX_ERR_INVALID_ARG;
         return SOFTMAX_OK;
     case SOFTMAX_VARIANT_SPLITK_WIDE:
-        if (V != kStreamUnroll || p.block_threads > kStreamThreads || p.cluster_x != 1)
+        if (V != kWideStep || p.block_threads > kStreamThreads || p.cluster_x != 1)
             return SOFTMAX_ERR_INVALID_ARG;
         if (p.grid_y != rows || rows > 65535 || p.grid_x > 65535)
             return SOFTMAX_ERR_INVALID_ARG;
