@@ -180,6 +180,13 @@ struct RowGeom {
     int head;         // elements of chunk 0 that precede the row (0 when aligned)
     int64_t nch;      // chunks covering the row
     int64_t kf, kl;   // chunks [kf, kl) lie wholly inside the row
+    // Interior / edge split, in 32 bits, for kernels whose rows hold fewer
+    // than 2^31 elements: the interior chunks kf .. kl - 1 lie wholly inside
+    // the row and are read and written as 16-byte vectors; the at most
+    // 2E - 2 edge elements [0, enh) and [et0, cols) are read and written one
+    // by one.  Aligned rows are all interior.
+    int n32, kf32, span32;  // nch, kf, max(kl - kf, 0)
+    int enh, et0, ne;       // edge elements: head count, tail start, total
 };
 
 template <int DT, bool ALIGNED>
@@ -207,6 +214,22 @@ __device__ __forceinline__ RowGeom row_geom(const char *x, char *y, int64_t r, i
         g.kf = lead ? 1 : 0;
         g.kl = ((lead + row_bytes) & 15) ? g.nch - 1 : g.nch;
     }
+    g.n32 = (int)g.nch;
+    g.kf32 = (int)g.kf;
+    // a row inside one chunk with both edges partial has kl < kf: no interior
+    g.span32 = g.kl > g.kf ? (int)(g.kl - g.kf) : 0;
+    if constexpr (ALIGNED) {
+        g.enh = 0;
+        g.et0 = (int)cols;
+        g.ne = 0;
+    } else {
+        constexpr int E = Fmt<DT>::kPerChunk;
+        const int c = (int)cols;
+        g.enh = g.kf32 ? (E - g.head < c ? E - g.head : c) : 0;
+        const int t0 = (int)g.kl * E - g.head;
+        g.et0 = t0 > g.enh ? t0 : g.enh;
+        g.ne = g.enh + (c - g.et0);
+    }
     return g;
 }
 
@@ -233,19 +256,29 @@ __device__ __forceinline__ uint4 ld_partial(const char *xr, int64_t j0, int64_t 
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Load chunk k of a row (k may be >= nch: then an all -inf chunk).
+template <int DT>
+__device__ __forceinline__ uint4 mask_chunk(const uint4 &c, int64_t t0, int64_t lo, int64_t hi);
+
+// Load chunk k of a row (k may be >= nch: then an all -inf chunk).  Every
+// chunk k < nch is one aligned 16-byte load, the two edge chunks of an
+// unaligned row included: such a chunk holds at least one byte of the row,
+// and an aligned 16-byte granule never crosses a page, so the granule is
+// mapped wherever that byte is.  Its slots outside the row (bytes of the
+// neighbouring rows, or just past either end of x) are replaced by -inf in
+// registers and never used.
 template <int DT, bool ALIGNED>
 __device__ __forceinline__ uint4 load_chunk(const RowGeom &g, int64_t k, int64_t cols)
 {
     constexpr int E = Fmt<DT>::kPerChunk;
     if (k >= g.nch)
         return neg_inf_chunk<DT>();
+    const uint4 c = ld_chunk(g.x0 + 16 * k);
     if constexpr (ALIGNED) {
-        return ld_chunk(g.x0 + 16 * k);
+        return c;
     } else {
         if (k >= g.kf && k < g.kl)
-            return ld_chunk(g.x0 + 16 * k);
-        return ld_partial<DT>(g.xr, k * E - g.head, cols);
+            return c;
+        return mask_chunk<DT>(c, k * E - g.head, 0, cols);
     }
 }
 
@@ -279,6 +312,77 @@ __device__ __forceinline__ void store_chunk(const RowGeom &g, int64_t k, int64_t
         }
     }
 }
+
+// ---------------------------------------------------------------- interior chunks, edge elements
+
+// Where y rows sit relative to x rows, for the kernels built on the
+// interior / edge split: kPhAligned -- every row on the 16-byte grid and whole
+// chunks long; kPhSame -- unaligned rows, y on the same 16-byte phase as x (an
+// interior chunk of x is one of y); kPhOther -- y on another phase, so
+// interior results are stored element by element.
+constexpr int kPhAligned = 0;
+constexpr int kPhSame = 1;
+constexpr int kPhOther = 2;
+
+// Interior chunk q (q >= 0) of a row; q past the interior gives -inf.
+template <int DT>
+__device__ __forceinline__ uint4 load_interior(const RowGeom &g, int q)
+{
+    return q < g.span32 ? ld_chunk(g.x0 + ((int64_t)(g.kf32 + q) << 4)) : neg_inf_chunk<DT>();
+}
+
+// Store interior chunk q (q < span32) of a row.
+template <int DT, int PH>
+__device__ __forceinline__ void store_interior(const RowGeom &g, int q, const uint4 &p)
+{
+    constexpr int E = Fmt<DT>::kPerChunk;
+    constexpr int S = Fmt<DT>::kBytes;
+    if constexpr (PH != kPhOther) {
+        st_chunk(g.y0 + ((int64_t)(g.kf32 + q) << 4), p);
+    } else {
+        const int j0 = (g.kf32 + q) * E - g.head;
+        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            if constexpr (S == 4)
+                st_u32(g.yr + 4 * (int64_t)(j0 + e), w[e]);
+            else
+                st_u16(g.yr + 2 * (int64_t)(j0 + e), (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+        }
+    }
+}
+
+// Column of edge element p (0 <= p < ne).
+__device__ __forceinline__ int edge_col(const RowGeom &g, int p) { return p < g.enh ? p : g.et0 + (p - g.enh); }
+
+// One element of a row as a float, and one float stored rounded to nearest
+// even in the dtype (the rounding pack() applies).
+template <int DT>
+__device__ __forceinline__ float ld_elem(const char *row, int j)
+{
+    if constexpr (DT == kF32) {
+        return __uint_as_float(ld_u32(row + 4 * (int64_t)j));
+    } else if constexpr (DT == kF16) {
+        return __half2float(__ushort_as_half((unsigned short)ld_u16(row + 2 * (int64_t)j)));
+    } else {
+        return __uint_as_float(ld_u16(row + 2 * (int64_t)j) << 16);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void st_elem(char *row, int j, float v)
+{
+    if constexpr (DT == kF32)
+        st_u32(row + 4 * (int64_t)j, __float_as_uint(v));
+    else if constexpr (DT == kF16)
+        st_u16(row + 2 * (int64_t)j, __half_as_ushort(__float2half_rn(v)));
+    else
+        st_u16(row + 2 * (int64_t)j, __bfloat16_as_ushort(__float2bfloat16_rn(v)));
+}
+
+// Edge elements a lane of an L-lane team holds: a row has at most 2E - 2.
+template <int DT, int L>
+__host__ __device__ constexpr int edge_slots() { return (2 * Fmt<DT>::kPerChunk - 2 + L - 1) / L; }
 
 // Make the compiler treat a cached chunk as freshly defined, so that values
 // unpacked from it before this point are not kept alive in registers to be

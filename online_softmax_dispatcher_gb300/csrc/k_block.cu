@@ -2,6 +2,10 @@
 // one HBM write per element for rows of up to 512 threads x 16 chunks x 16 B
 // = 128 KiB.
 //
+// A row off the 16-byte grid is read as its interior chunks (16-byte vectors,
+// interior chunk q to thread q mod T) plus at most 2E - 2 edge elements, one
+// per thread of the first few, outside the unrolled chunk loops.
+//
 // Prior art: the one-pass kernels of "[CUDA] safe online softmax", section 2
 // (fp16x8 register cache, 2.1; register + shared-memory cache, 2.2), written
 // for a 48 KB-per-block, 64K-register sm_120 part, and the block-per-row kernel
@@ -18,9 +22,9 @@
 
 namespace osd {
 
-template <int DT, int V, bool ALIGNED>
+template <int DT, int V, int PH>
 __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
-    k_block(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int y_vec)
+    k_block(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols)
 {
     using M = Math<DT>;
     using Acc = typename M::Acc;
@@ -28,24 +32,36 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
     // keep e = exp(x - m) in registers when it fits next to the cached chunks,
     // else recompute it
     constexpr bool kKeepE = V * E <= 32 && V <= 4;
+    constexpr bool kEdges = PH != kPhAligned;  // a CTA has >= 32 threads: one edge element each at most
     __shared__ float smax[32];
     __shared__ Acc ssum[32];
     const int T = blockDim.x;
     const int t = threadIdx.x;
 
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const RowGeom g = row_geom<DT, ALIGNED>(x, y, r, cols);
+        const RowGeom g = row_geom<DT, PH == kPhAligned>(x, y, r, cols);
         uint4 raw[V];
 #pragma unroll
         for (int i = 0; i < V; i++)
-            raw[i] = load_chunk<DT, ALIGNED>(g, t + (int64_t)i * T, cols);
+            raw[i] = load_interior<DT>(g, t + i * T);
+        int je = -1;
+        float xe = -INFINITY;
+        if (kEdges && t < g.ne) {
+            je = edge_col(g, t);
+            xe = ld_elem<DT>(g.xr, je);
+        }
+
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < V; i++)
+            m = fmaxf(m, chunk_max<DT>(raw[i]));
+        if (kEdges)
+            m = fmaxf(m, xe);
+        m = block_max(m, smax);
+        if (kEdges)
+            xe = je >= 0 ? M::exp_shift(xe, m) : 0.f;
 
         if constexpr (kKeepE) {
-            float m = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < V; i++)
-                m = fmaxf(m, chunk_max<DT>(raw[i]));
-            m = block_max(m, smax);
             float v[V][E];
             Acc acc = M::zero();
 #pragma unroll
@@ -55,25 +71,24 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
                 for (int e = 0; e < E; e++)
                     M::add(acc, v[i][e]);
             }
+            if (kEdges)
+                M::add(acc, xe);
             acc = block_sum<DT>(acc, ssum);
             const float inv = 1.0f / M::value(acc);
 #pragma unroll
             for (int i = 0; i < V; i++) {
-                const int64_t k = t + (int64_t)i * T;
-                if (k < g.nch) {
+                const int q = t + i * T;
+                if (q < g.span32) {
                     float o[E];
 #pragma unroll
                     for (int e = 0; e < E; e++)
                         o[e] = v[i][e] * inv;
-                    store_chunk<DT, ALIGNED>(g, k, cols, pack<DT>(o), y_vec != 0);
+                    store_interior<DT, PH>(g, q, pack<DT>(o));
                 }
             }
+            if (kEdges && je >= 0)
+                st_elem<DT>(g.yr, je, xe * inv);
         } else {
-            float m = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < V; i++)
-                m = fmaxf(m, chunk_max<DT>(raw[i]));
-            m = block_max(m, smax);
 #pragma unroll
             for (int i = 0; i < V; i++)
                 opaque(raw[i]);
@@ -86,6 +101,8 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
                 for (int e = 0; e < E; e++)
                     M::add(acc, f[e]);
             }
+            if (kEdges)
+                M::add(acc, xe);
             acc = block_sum<DT>(acc, ssum);
             const float inv = 1.0f / M::value(acc);
 #pragma unroll
@@ -93,34 +110,38 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
                 opaque(raw[i]);
 #pragma unroll
             for (int i = 0; i < V; i++) {
-                const int64_t k = t + (int64_t)i * T;
-                if (k < g.nch) {
+                const int q = t + i * T;
+                if (q < g.span32) {
                     float f[E];
                     chunk_exp<DT>(raw[i], m, f);
 #pragma unroll
                     for (int e = 0; e < E; e++)
                         f[e] *= inv;
-                    store_chunk<DT, ALIGNED>(g, k, cols, pack<DT>(f), y_vec != 0);
+                    store_interior<DT, PH>(g, q, pack<DT>(f));
                 }
             }
+            if (kEdges && je >= 0)
+                st_elem<DT>(g.yr, je, xe * inv);
         }
     }
 }
 
 namespace {
 
-template <int DT, int V, bool A>
+template <int DT, int V, int PH>
 int launch_one(const Launch &l)
 {
-    k_block<DT, V, A><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-        (const char *)l.x, (char *)l.y, l.rows, l.cols, l.plan.y_vector);
+    k_block<DT, V, PH><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
+        (const char *)l.x, (char *)l.y, l.rows, l.cols);
     return (int)cudaGetLastError();
 }
 
 template <int DT, int V>
 int launch_a(const Launch &l)
 {
-    return l.plan.aligned ? launch_one<DT, V, true>(l) : launch_one<DT, V, false>(l);
+    if (l.plan.aligned)
+        return launch_one<DT, V, kPhAligned>(l);
+    return l.plan.y_vector ? launch_one<DT, V, kPhSame>(l) : launch_one<DT, V, kPhOther>(l);
 }
 
 template <int DT>

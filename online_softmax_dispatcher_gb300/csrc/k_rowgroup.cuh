@@ -12,10 +12,14 @@
 // two >= cols) so that a warp holds 32 / G rows and no lane idles; long rows
 // get a whole warp.
 //
-// Per row: the group's lanes load their 16-byte chunks (chunk k of the row goes
-// to lane k mod G), take the max with a G-lane xor butterfly, compute
-// e = exp(x - m) once per element and keep it in registers, butterfly-sum e,
-// then write e * (1 / d) as 16-byte stores.  The grid normally covers every
+// Per row: the group's lanes load their 16-byte interior chunks (interior
+// chunk q goes to lane q mod G) and, for a row off the 16-byte grid, its at
+// most 2E - 2 edge elements one by one (edge element p to lane p mod G), take
+// the max with a G-lane xor butterfly, compute e = exp(x - m) once per element
+// and keep it in registers, butterfly-sum e, then write e * (1 / d): 16-byte
+// stores for interior chunks, element stores for the edges.  The edge work
+// sits outside the unrolled chunk loops, which stay as short as for aligned
+// rows.  The grid normally covers every
 // row once (many small CTAs: HBM latency is hidden by occupancy, and the tail
 // of the launch is one short CTA); a smaller grid walks the rows with a
 // stride.
@@ -26,12 +30,13 @@
 
 namespace osd {
 
-template <int DT, int G, int V, bool ALIGNED>
+template <int DT, int G, int V, int PH>
 __global__ void __launch_bounds__(kRowgroupThreads)
-    k_rowgroup(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int y_vec)
+    k_rowgroup(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols)
 {
     using M = Math<DT>;
     constexpr int E = Fmt<DT>::kPerChunk;
+    constexpr int NE = PH == kPhAligned ? 0 : edge_slots<DT, G>();
     const int groups = blockDim.x / G;  // rows per CTA per step
     const int gl = threadIdx.x & (G - 1);
     const int64_t stride = (int64_t)gridDim.x * groups;
@@ -40,17 +45,29 @@ __global__ void __launch_bounds__(kRowgroupThreads)
     for (int64_t base = (int64_t)blockIdx.x * groups; base < rows; base += stride) {
         const int64_t r = base + threadIdx.x / G;
         const bool valid = r < rows;
-        const RowGeom g = row_geom<DT, ALIGNED>(x, y, valid ? r : 0, cols);
+        const RowGeom g = row_geom<DT, PH == kPhAligned>(x, y, valid ? r : 0, cols);
 
         uint4 raw[V];
 #pragma unroll
         for (int i = 0; i < V; i++)
-            raw[i] = valid ? load_chunk<DT, ALIGNED>(g, gl + i * G, cols) : neg_inf_chunk<DT>();
+            raw[i] = valid ? load_interior<DT>(g, gl + i * G) : neg_inf_chunk<DT>();
+        // this lane's edge elements (unaligned rows): column je, value xe
+        int je[NE > 0 ? NE : 1];
+        float xe[NE > 0 ? NE : 1];
+#pragma unroll
+        for (int u = 0; u < NE; u++) {
+            const int p = gl + u * G;
+            je[u] = (valid && p < g.ne) ? edge_col(g, p) : -1;
+            xe[u] = je[u] >= 0 ? ld_elem<DT>(g.xr, je[u]) : -INFINITY;
+        }
 
         float m = -INFINITY;
 #pragma unroll
         for (int i = 0; i < V; i++)
             m = fmaxf(m, chunk_max<DT>(raw[i]));
+#pragma unroll
+        for (int u = 0; u < NE; u++)
+            m = fmaxf(m, xe[u]);
         m = G == 32 ? warp_max_redux(m) : group_max<G>(m);
 
         float v[V][E];
@@ -62,37 +79,48 @@ __global__ void __launch_bounds__(kRowgroupThreads)
             for (int e = 0; e < E; e++)
                 M::add(acc, v[i][e]);
         }
+#pragma unroll
+        for (int u = 0; u < NE; u++) {
+            xe[u] = je[u] >= 0 ? M::exp_shift(xe[u], m) : 0.f;
+            M::add(acc, xe[u]);
+        }
         acc = group_sum<DT, G>(acc);
         const float inv = 1.0f / M::value(acc);
 
         if (valid) {
 #pragma unroll
             for (int i = 0; i < V; i++) {
-                const int64_t k = gl + i * G;
-                if (k < g.nch) {
+                const int q = gl + i * G;
+                if (q < g.span32) {
                     float o[E];
 #pragma unroll
                     for (int e = 0; e < E; e++)
                         o[e] = v[i][e] * inv;
-                    store_chunk<DT, ALIGNED>(g, k, cols, pack<DT>(o), y_vec != 0);
+                    store_interior<DT, PH>(g, q, pack<DT>(o));
                 }
             }
+#pragma unroll
+            for (int u = 0; u < NE; u++)
+                if (je[u] >= 0)
+                    st_elem<DT>(g.yr, je[u], xe[u] * inv);
         }
     }
 }
 
-template <int DT, int G, int V, bool A>
+template <int DT, int G, int V, int PH>
 int rowgroup_launch_one(const Launch &l)
 {
-    k_rowgroup<DT, G, V, A><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-        (const char *)l.x, (char *)l.y, l.rows, l.cols, l.plan.y_vector);
+    k_rowgroup<DT, G, V, PH><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
+        (const char *)l.x, (char *)l.y, l.rows, l.cols);
     return (int)cudaGetLastError();
 }
 
 template <int DT, int G, int V>
 int rowgroup_launch_a(const Launch &l)
 {
-    return l.plan.aligned ? rowgroup_launch_one<DT, G, V, true>(l) : rowgroup_launch_one<DT, G, V, false>(l);
+    if (l.plan.aligned)
+        return rowgroup_launch_one<DT, G, V, kPhAligned>(l);
+    return l.plan.y_vector ? rowgroup_launch_one<DT, G, V, kPhSame>(l) : rowgroup_launch_one<DT, G, V, kPhOther>(l);
 }
 
 // V chunks per lane, V * E <= 32 floats: V in {1, 2, 4} (and 8 for fp32).

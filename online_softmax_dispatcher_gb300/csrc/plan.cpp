@@ -49,6 +49,9 @@ struct Geometry {
     bool aligned;     // every x and y row starts on the 16-byte grid and spans whole chunks
     bool y_vec;       // y rows have the same 16-byte phase as x rows
     int64_t nch_max;  // most 16-byte chunks any row spans
+    int64_t nint;     // most whole 16-byte chunks inside any row (the interior
+                      // chunks of the lanes-per-row and CTA-per-row kernels,
+                      // which take the partial edges element by element)
 };
 
 Geometry geometry(const void *x, const void *y, int64_t cols, int dtype)
@@ -62,12 +65,13 @@ Geometry geometry(const void *x, const void *y, int64_t cols, int dtype)
     g.y_vec = ((ya - xa) % 16) == 0;
     // an unaligned row starts up to 16 - S bytes into its first chunk
     g.nch_max = g.aligned ? g.row_bytes / 16 : ceil_div(g.row_bytes + 16 - g.S, 16);
+    g.nint = g.row_bytes / 16;
     return g;
 }
 
-bool rowgroup_fits(const Geometry &g) { return g.nch_max <= 32 * (kRowgroupMaxFloats / g.E); }
+bool rowgroup_fits(const Geometry &g) { return g.nint <= 32 * (kRowgroupMaxFloats / g.E); }
 
-bool block_fits(const Geometry &g) { return g.nch_max <= int64_t(block_max_threads(kBlockMaxChunks)) * kBlockMaxChunks; }
+bool block_fits(const Geometry &g) { return g.nint <= int64_t(block_max_threads(kBlockMaxChunks)) * kBlockMaxChunks; }
 
 // G lanes per row with V chunks each: aim for 32 cached floats per lane (4
 // chunks of fp16 / bf16, 8 of fp32) so that the per-row shuffles and the
@@ -77,17 +81,18 @@ bool block_fits(const Geometry &g) { return g.nch_max <= int64_t(block_max_threa
 void plan_rowgroup(const Geometry &g, int64_t rows, const softmax_device_info &dev, softmax_launch_plan &p)
 {
     int64_t G, V;
-    if (g.nch_max <= 4) {
-        G = next_pow2(g.nch_max);
+    const int64_t n = g.nint > 1 ? g.nint : 1;
+    if (n <= 4) {
+        G = next_pow2(n);
         V = 1;
     } else {
         const int64_t vt = kRowgroupMaxFloats / g.E;
-        G = next_pow2(ceil_div(g.nch_max, vt));
+        G = next_pow2(ceil_div(n, vt));
         if (G < 2)
             G = 2;
         if (G > 32)
             G = 32;
-        V = next_pow2(ceil_div(g.nch_max, G));
+        V = next_pow2(ceil_div(n, G));
     }
     p.variant = SOFTMAX_VARIANT_ROWGROUP;
     p.lanes_per_row = (int)G;
@@ -107,10 +112,10 @@ void plan_block(const Geometry &g, int64_t rows, softmax_launch_plan &p)
     // several rows -- stay resident per SM and one's loads overlap another's
     // reductions.  Measured: [8192, 5003] fp16 runs fastest at V = 8 x 96
     // threads, [32768, 32000] bf16 at V = 16 x 256 (V = 8 x 512 is slower).
-    int V = ceil_div(g.nch_max, 8) >= 64 ? 8 : 4;
-    while (V < kBlockMaxChunks && ceil_div(g.nch_max, V) > 256)
+    int V = ceil_div(g.nint, 8) >= 64 ? 8 : 4;
+    while (V < kBlockMaxChunks && ceil_div(g.nint, V) > 256)
         V *= 2;
-    int64_t threads = ceil_div(ceil_div(g.nch_max, V), 32) * 32;
+    int64_t threads = ceil_div(ceil_div(g.nint, V), 32) * 32;
     if (threads < 64)
         threads = 64;
     p.variant = SOFTMAX_VARIANT_BLOCK;
@@ -268,7 +273,7 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
         const int G = p.lanes_per_row;
         if (G < 1 || G > 32 || (G & (G - 1)) || V < 1 || V > 8 || (V & (V - 1)))
             return SOFTMAX_ERR_INVALID_ARG;
-        if (V * g.E > kRowgroupMaxFloats || int64_t(G) * V < g.nch_max || (G == 1 && V != 1))
+        if (V * g.E > kRowgroupMaxFloats || int64_t(G) * V < g.nint || (G == 1 && V != 1))
             return SOFTMAX_ERR_INVALID_ARG;
         if (p.block_threads > kRowgroupThreads || p.grid_y != 1 || p.cluster_x != 1)
             return SOFTMAX_ERR_INVALID_ARG;
@@ -277,7 +282,7 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
     case SOFTMAX_VARIANT_BLOCK:
         if (V < 1 || V > kBlockMaxChunks || (V & (V - 1)))
             return SOFTMAX_ERR_INVALID_ARG;
-        if (p.block_threads > block_max_threads(V) || int64_t(p.block_threads) * V < g.nch_max)
+        if (p.block_threads > block_max_threads(V) || int64_t(p.block_threads) * V < g.nint)
             return SOFTMAX_ERR_INVALID_ARG;
         if (p.grid_y != 1 || p.cluster_x != 1)
             return SOFTMAX_ERR_INVALID_ARG;

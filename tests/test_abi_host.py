@@ -103,12 +103,15 @@ def _nch_max(cols, elem, aligned):
 
 
 def _covers(p, rows, cols, elem, aligned):
-    """The plan's threads cover every 16-byte chunk of a row."""
+    """The plan's threads cover every 16-byte chunk of a row: for the
+    lanes-per-row and CTA-per-row kernels, every whole chunk inside a row (they
+    take the partial edge chunks element by element)."""
     n = _nch_max(cols, elem, aligned)
+    n_int = cols * elem // 16
     if p.variant == B.VARIANT_ROWGROUP:
-        return p.lanes_per_row * p.chunks_per_thread >= n and (p.lanes_per_row > 1 or p.chunks_per_thread == 1)
+        return p.lanes_per_row * p.chunks_per_thread >= n_int and (p.lanes_per_row > 1 or p.chunks_per_thread == 1)
     if p.variant == B.VARIANT_BLOCK:
-        return p.block_threads * p.chunks_per_thread >= n
+        return p.block_threads * p.chunks_per_thread >= n_int
     if p.variant == B.VARIANT_BLOCK_TMA:
         stage = p.smem_bytes // p.stages
         lead = 0 if aligned else 16 - elem
