@@ -324,11 +324,11 @@ constexpr int kPhAligned = 0;
 constexpr int kPhSame = 1;
 constexpr int kPhOther = 2;
 
-// Interior chunk q (q >= 0) of a row; q past the interior gives -inf.
+// Interior chunk q of a row; q outside [0, span32) gives -inf.
 template <int DT>
 __device__ __forceinline__ uint4 load_interior(const RowGeom &g, int q)
 {
-    return q < g.span32 ? ld_chunk(g.x0 + ((int64_t)(g.kf32 + q) << 4)) : neg_inf_chunk<DT>();
+    return (unsigned)q < (unsigned)g.span32 ? ld_chunk(g.x0 + ((int64_t)(g.kf32 + q) << 4)) : neg_inf_chunk<DT>();
 }
 
 // Store interior chunk q (q < span32) of a row.

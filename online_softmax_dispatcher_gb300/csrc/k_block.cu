@@ -40,10 +40,17 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
 
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const RowGeom g = row_geom<DT, PH == kPhAligned>(x, y, r, cols);
+        // Thread t takes interior chunks q = t + i * T - sh: the shift sh puts
+        // every 8th slot on a 128-byte line, so a warp's 32 chunks span 4
+        // lines, not 5 (taken when the CTA has sh slots to spare).
+        int sh = (int)(((reinterpret_cast<uintptr_t>(g.x0) >> 4) + g.kf32) & 7);
+        if (sh > T * V - g.span32)
+            sh = 0;
+        const int t0 = t - sh;
         uint4 raw[V];
 #pragma unroll
         for (int i = 0; i < V; i++)
-            raw[i] = load_interior<DT>(g, t + i * T);
+            raw[i] = load_interior<DT>(g, t0 + i * T);
         int je = -1;
         float xe = -INFINITY;
         if (kEdges && t < g.ne) {
@@ -77,8 +84,8 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
             const float inv = 1.0f / M::value(acc);
 #pragma unroll
             for (int i = 0; i < V; i++) {
-                const int q = t + i * T;
-                if (q < g.span32) {
+                const int q = t0 + i * T;
+                if ((unsigned)q < (unsigned)g.span32) {
                     float o[E];
 #pragma unroll
                     for (int e = 0; e < E; e++)
@@ -110,8 +117,8 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
                 opaque(raw[i]);
 #pragma unroll
             for (int i = 0; i < V; i++) {
-                const int q = t + i * T;
-                if (q < g.span32) {
+                const int q = t0 + i * T;
+                if ((unsigned)q < (unsigned)g.span32) {
                     float f[E];
                     chunk_exp<DT>(raw[i], m, f);
 #pragma unroll
