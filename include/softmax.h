@@ -31,7 +31,8 @@
  *     Pointers must be aligned to the element size (4 bytes for fp32, 2 for
  *     fp16 / bf16); 16-byte aligned rows take the vectorised fast path, any
  *     other alignment is handled by peeling partial 16-byte chunks.
- *   - x and y must not overlap (in-place is not supported).
+ *   - y may be x itself (in place: every element is read before it is
+ *     overwritten); any other overlap of x and y is refused.
  *   - work is enqueued on `stream` (NULL = the legacy default stream) and the
  *     call returns without synchronising.  Faults during execution surface at
  *     the caller's next synchronisation, as for any CUDA launch.
@@ -67,7 +68,7 @@ typedef enum {
                                            rows*cols*size overflows int64, misaligned pointer,
                                            bad variant id, null out-pointer */
     SOFTMAX_ERR_UNSUPPORTED_DTYPE = -2, /* dtype not in softmax_dtype */
-    SOFTMAX_ERR_ALIAS = -3,             /* x and y byte ranges overlap */
+    SOFTMAX_ERR_ALIAS = -3,             /* buffers overlap (other than an allowed in-place call) */
     SOFTMAX_ERR_CUDA = -4,              /* a CUDA runtime call failed; see softmax_last_cuda_error */
     SOFTMAX_ERR_UNSUPPORTED_SHAPE = -5, /* a forced variant cannot serve this shape / device */
     SOFTMAX_ERR_DEVICE_TIMEOUT = -6     /* a bounded device-side wait gave up (see
@@ -166,8 +167,9 @@ int softmax_fwd_masked_variant(const void *x, void *y, int64_t rows, int64_t col
  *     |dx - dx*| <= u(dx*) + 8 * 2^-24 * y_j * (|dy_j| + sum_k |dy_k y_k|)
  * with u = 1 ulp of the dtype at dx* for fp16 / bf16 and 2e-6 * |dx*| for
  * fp32; the second term is the fp32 cancellation budget of dy_j - s.
- * y and dy are only read (they may be the same buffer); dx must not overlap
- * either (SOFTMAX_ERR_ALIAS).  Alignment, streams, errors: as softmax_fwd.
+ * y and dy are only read (they may be the same buffer); dx may be exactly y or
+ * exactly dy (in place) and must not overlap either otherwise
+ * (SOFTMAX_ERR_ALIAS).  Alignment, streams, errors: as softmax_fwd.
  * Kernels: ROWGROUP (rows of up to 128 chunks of 16 bytes), BLOCK (up to 4096),
  * STREAM (any).
  */

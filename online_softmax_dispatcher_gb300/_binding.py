@@ -252,8 +252,9 @@ def softmax(x, *, out=None, variant: int | str = VARIANT_AUTO, plan: LaunchPlan 
             stream=None, workspace=None):
     """y = softmax(x) over the last dimension of a contiguous CUDA tensor.
 
-    `out` (same shape and dtype, contiguous, not overlapping x) receives the
-    result when given; `variant` forces a kernel; `plan` launches a
+    `out` (same shape and dtype, contiguous; x itself for an in-place call,
+    else not overlapping x) receives the result when given; `variant` forces a
+    kernel; `plan` launches a
     caller-built plan; `stream` is a torch.cuda.Stream (default: current);
     `workspace` (a CUDA tensor of at least softmax_workspace_size bytes) lets
     few, very long rows use every SM (softmax_fwd_ws).
@@ -290,6 +291,11 @@ def softmax(x, *, out=None, variant: int | str = VARIANT_AUTO, plan: LaunchPlan 
     return y
 
 
+def softmax_(x, **kw):
+    """In-place softmax over the last dimension: x is overwritten with softmax(x)."""
+    return softmax(x, out=x, **kw)
+
+
 def softmax_masked(x, *, scale: float = 1.0, mask=None, causal: bool = False, out=None,
                    variant: int | str = VARIANT_AUTO, stream=None):
     """softmax(scale * x + mask) over the last dimension with an optional causal
@@ -323,7 +329,8 @@ def softmax_masked(x, *, scale: float = 1.0, mask=None, causal: bool = False, ou
 
 def softmax_backward(y, dy, *, out=None, variant: int | str = VARIANT_AUTO, stream=None):
     """dx = y * (dy - sum(dy * y, -1)) for contiguous CUDA tensors y (a softmax
-    output) and dy (its upstream gradient)."""
+    output) and dy (its upstream gradient).  `out` may be dy or y itself (in
+    place)."""
     import torch
 
     for name, t in (("y", y), ("dy", dy)):

@@ -417,7 +417,7 @@ OSD_API const char *softmax_strerror(int status)
     case SOFTMAX_ERR_UNSUPPORTED_DTYPE:
         return "unsupported dtype";
     case SOFTMAX_ERR_ALIAS:
-        return "x and y overlap";
+        return "buffers overlap (other than exactly, in place)";
     case SOFTMAX_ERR_CUDA:
         return "CUDA runtime error (see softmax_last_cuda_error)";
     case SOFTMAX_ERR_UNSUPPORTED_SHAPE:

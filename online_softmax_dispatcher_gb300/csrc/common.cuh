@@ -180,13 +180,6 @@ struct RowGeom {
     int head;         // elements of chunk 0 that precede the row (0 when aligned)
     int64_t nch;      // chunks covering the row
     int64_t kf, kl;   // chunks [kf, kl) lie wholly inside the row
-    // Interior / edge split, in 32 bits, for kernels whose rows hold fewer
-    // than 2^31 elements: the interior chunks kf .. kl - 1 lie wholly inside
-    // the row and are read and written as 16-byte vectors; the at most
-    // 2E - 2 edge elements [0, enh) and [et0, cols) are read and written one
-    // by one.  Aligned rows are all interior.
-    int n32, kf32, span32;  // nch, kf, max(kl - kf, 0)
-    int enh, et0, ne;       // edge elements: head count, tail start, total
 };
 
 template <int DT, bool ALIGNED>
@@ -214,21 +207,57 @@ __device__ __forceinline__ RowGeom row_geom(const char *x, char *y, int64_t r, i
         g.kf = lead ? 1 : 0;
         g.kl = ((lead + row_bytes) & 15) ? g.nch - 1 : g.nch;
     }
-    g.n32 = (int)g.nch;
-    g.kf32 = (int)g.kf;
-    // a row inside one chunk with both edges partial has kl < kf: no interior
-    g.span32 = g.kl > g.kf ? (int)(g.kl - g.kf) : 0;
+    return g;
+}
+
+// A row of fewer than 2^31 bytes split into interior chunks and edge
+// elements, in 32-bit arithmetic (the lanes-per-row and CTA-per-row kernels,
+// which set this up once per row in every thread).  The interior chunks
+// kf .. kf + span - 1 (chunk k at x0 + 16 k) lie wholly inside the row and are
+// read and written as 16-byte vectors; the at most 2E - 2 edge elements
+// [0, enh) and [et0, cols) are read and written one by one.  Aligned rows are
+// all interior.
+struct ShortRow {
+    const char *x0;  // 16-byte aligned address of chunk 0 of the x row
+    char *y0;        // same for y (meaningful when y rows share x rows' phase)
+    const char *xr;  // x row start
+    char *yr;        // y row start
+    int head;        // elements of chunk 0 that precede the row
+    int kf, span;    // first interior chunk, interior chunks
+    int enh, et0, ne;  // edge elements: head count, tail start, total
+};
+
+template <int DT, bool ALIGNED>
+__device__ __forceinline__ ShortRow short_row(const char *x, char *y, int64_t r, int cols)
+{
+    constexpr int S = Fmt<DT>::kBytes;
+    constexpr int E = Fmt<DT>::kPerChunk;
+    const int rb = cols * S;
+    ShortRow g;
+    g.xr = x + r * rb;
+    g.yr = y + r * rb;
     if constexpr (ALIGNED) {
+        g.x0 = g.xr;
+        g.y0 = g.yr;
+        g.head = 0;
+        g.kf = 0;
+        g.span = rb >> 4;
         g.enh = 0;
-        g.et0 = (int)cols;
+        g.et0 = cols;
         g.ne = 0;
     } else {
-        constexpr int E = Fmt<DT>::kPerChunk;
-        const int c = (int)cols;
-        g.enh = g.kf32 ? (E - g.head < c ? E - g.head : c) : 0;
-        const int t0 = (int)g.kl * E - g.head;
+        const int lead = (int)(reinterpret_cast<uintptr_t>(g.xr) & 15);
+        g.x0 = g.xr - lead;
+        g.y0 = g.yr - lead;
+        g.head = lead / S;
+        g.kf = lead != 0;
+        const int kl = (lead + rb) >> 4;  // chunks before kl end inside the row
+        // a row inside one chunk with both edges partial has kl < kf: no interior
+        g.span = kl > g.kf ? kl - g.kf : 0;
+        g.enh = g.kf ? (E - g.head < cols ? E - g.head : cols) : 0;
+        const int t0 = kl * E - g.head;
         g.et0 = t0 > g.enh ? t0 : g.enh;
-        g.ne = g.enh + (c - g.et0);
+        g.ne = g.enh + (cols - g.et0);
     }
     return g;
 }
@@ -324,23 +353,23 @@ constexpr int kPhAligned = 0;
 constexpr int kPhSame = 1;
 constexpr int kPhOther = 2;
 
-// Interior chunk q of a row; q outside [0, span32) gives -inf.
+// Interior chunk q of a row; q outside [0, span) gives -inf.
 template <int DT>
-__device__ __forceinline__ uint4 load_interior(const RowGeom &g, int q)
+__device__ __forceinline__ uint4 load_interior(const ShortRow &g, int q)
 {
-    return (unsigned)q < (unsigned)g.span32 ? ld_chunk(g.x0 + ((int64_t)(g.kf32 + q) << 4)) : neg_inf_chunk<DT>();
+    return (unsigned)q < (unsigned)g.span ? ld_chunk(g.x0 + ((int64_t)(g.kf + q) << 4)) : neg_inf_chunk<DT>();
 }
 
-// Store interior chunk q (q < span32) of a row.
+// Store interior chunk q (0 <= q < span) of a row.
 template <int DT, int PH>
-__device__ __forceinline__ void store_interior(const RowGeom &g, int q, const uint4 &p)
+__device__ __forceinline__ void store_interior(const ShortRow &g, int q, const uint4 &p)
 {
     constexpr int E = Fmt<DT>::kPerChunk;
     constexpr int S = Fmt<DT>::kBytes;
     if constexpr (PH != kPhOther) {
-        st_chunk(g.y0 + ((int64_t)(g.kf32 + q) << 4), p);
+        st_chunk(g.y0 + ((int64_t)(g.kf + q) << 4), p);
     } else {
-        const int j0 = (g.kf32 + q) * E - g.head;
+        const int j0 = (g.kf + q) * E - g.head;
         const uint32_t w[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
         for (int e = 0; e < E; e++) {
@@ -353,7 +382,7 @@ __device__ __forceinline__ void store_interior(const RowGeom &g, int q, const ui
 }
 
 // Column of edge element p (0 <= p < ne).
-__device__ __forceinline__ int edge_col(const RowGeom &g, int p) { return p < g.enh ? p : g.et0 + (p - g.enh); }
+__device__ __forceinline__ int edge_col(const ShortRow &g, int p) { return p < g.enh ? p : g.et0 + (p - g.enh); }
 
 // One element of a row as a float, and one float stored rounded to nearest
 // even in the dtype (the rounding pack() applies).

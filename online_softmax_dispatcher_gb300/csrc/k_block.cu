@@ -39,12 +39,12 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
     const int t = threadIdx.x;
 
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const RowGeom g = row_geom<DT, PH == kPhAligned>(x, y, r, cols);
+        const ShortRow g = short_row<DT, PH == kPhAligned>(x, y, r, (int)cols);
         // Thread t takes interior chunks q = t + i * T - sh: the shift sh puts
         // every 8th slot on a 128-byte line, so a warp's 32 chunks span 4
         // lines, not 5 (taken when the CTA has sh slots to spare).
-        int sh = (int)(((reinterpret_cast<uintptr_t>(g.x0) >> 4) + g.kf32) & 7);
-        if (sh > T * V - g.span32)
+        int sh = (int)(((reinterpret_cast<uintptr_t>(g.x0) >> 4) + g.kf) & 7);
+        if (sh > T * V - g.span)
             sh = 0;
         const int t0 = t - sh;
         uint4 raw[V];
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
 #pragma unroll
             for (int i = 0; i < V; i++) {
                 const int q = t0 + i * T;
-                if ((unsigned)q < (unsigned)g.span32) {
+                if ((unsigned)q < (unsigned)g.span) {
                     float o[E];
 #pragma unroll
                     for (int e = 0; e < E; e++)
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
 #pragma unroll
             for (int i = 0; i < V; i++) {
                 const int q = t0 + i * T;
-                if ((unsigned)q < (unsigned)g.span32) {
+                if ((unsigned)q < (unsigned)g.span) {
                     float f[E];
                     chunk_exp<DT>(raw[i], m, f);
 #pragma unroll

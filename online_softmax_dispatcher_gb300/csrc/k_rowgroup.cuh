@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kRowgroupThreads)
     for (int64_t base = (int64_t)blockIdx.x * groups; base < rows; base += stride) {
         const int64_t r = base + threadIdx.x / G;
         const bool valid = r < rows;
-        const RowGeom g = row_geom<DT, PH == kPhAligned>(x, y, valid ? r : 0, cols);
+        const ShortRow g = short_row<DT, PH == kPhAligned>(x, y, valid ? r : 0, (int)cols);
 
         uint4 raw[V];
 #pragma unroll
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kRowgroupThreads)
 #pragma unroll
             for (int i = 0; i < V; i++) {
                 const int q = gl + i * G;
-                if (q < g.span32) {
+                if (q < g.span) {
                     float o[E];
 #pragma unroll
                     for (int e = 0; e < E; e++)

@@ -252,7 +252,10 @@ int validate_args(const void *x, const void *y, int64_t rows, int64_t cols, int 
         return SOFTMAX_ERR_INVALID_ARG;
     const uint64_t bytes = (uint64_t)(rows * cols * S);
     const uint64_t gap = xa <= ya ? (uint64_t)(ya - xa) : (uint64_t)(xa - ya);
-    if (gap < bytes)
+    // x == y is in place (every kernel reads each element before the thread
+    // that owns it writes it, and nothing reads it afterwards); any other
+    // overlap would let a row be read after another row's write
+    if (gap != 0 && gap < bytes)
         return SOFTMAX_ERR_ALIAS;
     return SOFTMAX_OK;
 }
@@ -407,8 +410,9 @@ int validate_bwd_args(const void *y, const void *dy, const void *dx, int64_t row
         if (reinterpret_cast<uintptr_t>(p) % S)
             return SOFTMAX_ERR_INVALID_ARG;
     const uint64_t bytes = (uint64_t)(rows * cols * S);
-    // y and dy are only read and may overlap; dx must not overlap either
-    if (overlaps(dx, y, bytes) || overlaps(dx, dy, bytes))
+    // y and dy are only read and may overlap each other; dx may be exactly y
+    // or exactly dy (in place), but overlap neither otherwise
+    if ((dx != y && overlaps(dx, y, bytes)) || (dx != dy && overlaps(dx, dy, bytes)))
         return SOFTMAX_ERR_ALIAS;
     return SOFTMAX_OK;
 }

@@ -68,7 +68,7 @@ BASE = 1 << 40  # fake, 256-byte aligned "device" addresses: validation only loo
     ((BASE + 1, BASE + 4097, 2, 3, 1), B.ERR_INVALID_ARG),       # fp16 needs 2-byte alignment
     ((BASE, BASE + 20, 2, 3, 0), B.ERR_ALIAS),                   # 24 bytes of x overlap y
     ((BASE + 20, BASE, 2, 3, 0), B.ERR_ALIAS),                   # y overlaps the start of x
-    ((BASE, BASE, 2, 3, 0), B.ERR_ALIAS),
+    ((BASE, BASE + 4, 2, 3, 0), B.ERR_ALIAS),                    # y one element past x
     ((BASE, BASE + 64, 2**40, 2**40, 0), B.ERR_INVALID_ARG),     # rows*cols*4 overflows int64
     ((0, 0, 0, 5, 0), B.OK),                                     # empty: no launch, no device
     ((0, 0, 5, 0, 2), B.OK),
@@ -79,6 +79,17 @@ def test_argument_validation(lib, args, want):
     assert B.softmax_fwd_variant(x, y, rows, cols, dt, 0, 0) == want
     rc, _ = B.softmax_plan(GB300, x, y, rows, cols, dt)
     assert rc == want
+
+
+def test_in_place_is_accepted(lib):
+    # y == x exactly is an in-place call; every variant's plan accepts it
+    for rows, cols, dt in ((2, 3, 0), (8192, 5003, 1), (32768, 32000, 2), (4, 4194304, 0)):
+        rc, p = B.softmax_plan(GB300, BASE, BASE, rows, cols, dt)
+        assert rc == B.OK
+        for v in range(1, B.VARIANT_COUNT):
+            rc, _ = B.softmax_plan(GB300, BASE, BASE, rows, cols, dt, v)
+            assert rc in (B.OK, B.ERR_UNSUPPORTED_SHAPE, B.ERR_INVALID_ARG), (rows, cols, v, rc)
+            assert rc != B.ERR_ALIAS
 
 
 def test_adjacent_buffers_are_not_aliases(lib):

@@ -125,8 +125,10 @@ def test_bwd_torch_api_and_alias():
     dy = torch.randn_like(y)
     dx = osd.softmax_backward(y, dy)
     check_bwd(y.cpu().numpy(), dy.cpu().numpy(), dx.cpu().numpy(), 0)
+    # dx may be dy itself (in place); a partial overlap is refused
+    buf = torch.randn(301 * 777, device="cuda")
     with pytest.raises(osd.SoftmaxError) as e:
-        osd.softmax_backward(y, dy, out=dy)
+        osd.softmax_backward(y, buf[: 300 * 777].view(300, 777), out=buf[777:].view(300, 777))
     assert e.value.status == -3
     # y and dy may be the same buffer (both are only read)
     dx2 = osd.softmax_backward(y, y)

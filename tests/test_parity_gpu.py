@@ -267,8 +267,10 @@ def test_side_stream_and_overlap_refusal():
         y = osd.softmax(x)
     s.synchronize()
     check(x.cpu().numpy(), y.cpu().numpy(), 0)
+    # in place is accepted; a partial overlap is refused
+    buf = torch.randn(301 * 777, device="cuda")
     with pytest.raises(osd.SoftmaxError) as e:
-        osd.softmax(x, out=x)
+        osd.softmax(buf[: 300 * 777].view(300, 777), out=buf[777:].view(300, 777))
     assert e.value.status == -3
 
 

@@ -55,5 +55,6 @@ def test_noalloc_refuses_more_partials_than_it_holds():
     y = torch.empty_like(x)
     s = torch.cuda.current_stream().cuda_stream
     assert osd.softmax_fwd_noalloc(x.data_ptr(), y.data_ptr(), 5000, 64, 0, s) == -5
-    # argument checks come first, as for every entry point
-    assert osd.softmax_fwd_noalloc(x.data_ptr(), x.data_ptr(), 5000, 64, 0, s) == -3
+    # argument checks come first, as for every entry point: y one element past
+    # x overlaps it without being an in-place call
+    assert osd.softmax_fwd_noalloc(x.data_ptr(), x.data_ptr() + 4, 5000, 64, 0, s) == -3
