@@ -103,6 +103,54 @@ __device__ __forceinline__ void st_u32(void *p, uint32_t v)
     asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// ---------------------------------------------------------------- launch
+
+// Programmatic dependent launch.  Every kernel of the library starts with
+// pdl_enter(): it lets the next kernel in the stream be scheduled once every
+// CTA of this grid has started (the next grid then fills this one's tail
+// instead of waiting for it to drain), and waits until the previous kernel in
+// the stream has completed and its writes are visible, before this kernel's
+// first global memory access.  Without a programmatic predecessor the wait
+// returns at once.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch `kernel` on `stream` with programmatic stream serialisation allowed
+// (see pdl_enter); `extra` adds one more launch attribute (a cluster shape)
+// when its id is not cudaLaunchAttributeIgnore.  Returns the launch status and
+// leaves no pending launch error behind.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      cudaLaunchAttribute extra, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (extra.id != cudaLaunchAttributeIgnore)
+        attr[cfg.numAttrs++] = extra;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e != cudaSuccess)
+        (void)cudaGetLastError();
+    return (int)e;
+}
+
+inline cudaLaunchAttribute no_attr()
+{
+    cudaLaunchAttribute a = {};
+    a.id = cudaLaunchAttributeIgnore;
+    return a;
+}
+
 // ---------------------------------------------------------------- decode / encode
 
 template <int DT>

@@ -26,6 +26,7 @@ template <int DT, int V, int PH>
 __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
     k_block(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols)
 {
+    pdl_enter();
     using M = Math<DT>;
     using Acc = typename M::Acc;
     constexpr int E = Fmt<DT>::kPerChunk;
@@ -138,9 +139,8 @@ namespace {
 template <int DT, int V, int PH>
 int launch_one(const Launch &l)
 {
-    k_block<DT, V, PH><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-        (const char *)l.x, (char *)l.y, l.rows, l.cols);
-    return (int)cudaGetLastError();
+    return launch_pdl(k_block<DT, V, PH>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+                      (cudaStream_t)l.stream, no_attr(), (const char *)l.x, (char *)l.y, l.rows, l.cols);
 }
 
 template <int DT, int V>

@@ -106,6 +106,7 @@ __device__ __forceinline__ CSum group_csum(CSum a)
 template <int DT, int G, int V, bool ALIGNED>
 __global__ void __launch_bounds__(kRowgroupThreads) k_bwd_rowgroup(const BwdArgs a)
 {
+    pdl_enter();
     const int groups = blockDim.x / G;
     const int gl = threadIdx.x & (G - 1);
     const int64_t stride = (int64_t)gridDim.x * groups;
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(kRowgroupThreads) k_bwd_rowgroup(const BwdArgs
 template <int DT, int V, bool ALIGNED>
 __global__ void __launch_bounds__(512) k_bwd_block(const BwdArgs a)
 {
+    pdl_enter();
     __shared__ CSum slots[32];
     const int T = blockDim.x, t = threadIdx.x;
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(512) k_bwd_block(const BwdArgs a)
 template <int DT, bool ALIGNED>
 __global__ void __launch_bounds__(kStreamThreads) k_bwd_stream(const BwdArgs a)
 {
+    pdl_enter();
     constexpr int U = 4;
     __shared__ CSum slots[32];
     const int64_t T = blockDim.x;
@@ -233,9 +236,8 @@ BwdArgs args_of(const BwdLaunch &l)
 template <int DT, int G, int V, bool A>
 int bwd_rowgroup_one(const BwdLaunch &l)
 {
-    k_bwd_rowgroup<DT, G, V, A><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-        args_of(l));
-    return (int)cudaGetLastError();
+    return launch_pdl(k_bwd_rowgroup<DT, G, V, A>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+                      (cudaStream_t)l.stream, no_attr(), args_of(l));
 }
 
 template <int DT, int G, int V>
@@ -283,8 +285,8 @@ int bwd_rowgroup_dt(const BwdLaunch &l)
 template <int DT, int V, bool A>
 int bwd_block_one(const BwdLaunch &l)
 {
-    k_bwd_block<DT, V, A><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(args_of(l));
-    return (int)cudaGetLastError();
+    return launch_pdl(k_bwd_block<DT, V, A>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+                      (cudaStream_t)l.stream, no_attr(), args_of(l));
 }
 
 template <int DT>
@@ -304,13 +306,10 @@ int bwd_block_dt(const BwdLaunch &l)
 template <int DT>
 int bwd_stream_dt(const BwdLaunch &l)
 {
+    const dim3 grid((unsigned)l.plan.grid_x), block(l.plan.block_threads);
     if (l.plan.aligned)
-        k_bwd_stream<DT, true><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-            args_of(l));
-    else
-        k_bwd_stream<DT, false><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-            args_of(l));
-    return (int)cudaGetLastError();
+        return launch_pdl(k_bwd_stream<DT, true>, grid, block, 0, (cudaStream_t)l.stream, no_attr(), args_of(l));
+    return launch_pdl(k_bwd_stream<DT, false>, grid, block, 0, (cudaStream_t)l.stream, no_attr(), args_of(l));
 }
 
 template <int DT>

@@ -126,6 +126,7 @@ __device__ __forceinline__ float exp_logit(float zh, float zl, float m)
 template <int DT, int G, int V, bool ALIGNED>
 __global__ void __launch_bounds__(kRowgroupThreads) k_masked_rowgroup(const MaskedArgs a)
 {
+    pdl_enter();
     using M = Math<DT>;
     constexpr int E = Fmt<DT>::kPerChunk;
     constexpr int S = Fmt<DT>::kBytes;
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(kRowgroupThreads) k_masked_rowgroup(const Mask
 template <int DT, int V, bool ALIGNED>
 __global__ void __launch_bounds__(512) k_masked_block(const MaskedArgs a)
 {
+    pdl_enter();
     using M = Math<DT>;
     using Acc = typename M::Acc;
     constexpr int E = Fmt<DT>::kPerChunk;
@@ -279,9 +281,8 @@ MaskedArgs args_of(const MaskedLaunch &l)
 template <int DT, int G, int V, bool A>
 int mrg_one(const MaskedLaunch &l)
 {
-    k_masked_rowgroup<DT, G, V, A><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-        args_of(l));
-    return (int)cudaGetLastError();
+    return launch_pdl(k_masked_rowgroup<DT, G, V, A>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+                      (cudaStream_t)l.stream, no_attr(), args_of(l));
 }
 
 template <int DT, int G, int V>
@@ -331,9 +332,8 @@ int mrg_dt(const MaskedLaunch &l)
 template <int DT, int V, bool A>
 int mblk_one(const MaskedLaunch &l)
 {
-    k_masked_block<DT, V, A><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-        args_of(l));
-    return (int)cudaGetLastError();
+    return launch_pdl(k_masked_block<DT, V, A>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+                      (cudaStream_t)l.stream, no_attr(), args_of(l));
 }
 
 template <int DT>

@@ -34,6 +34,7 @@ template <int DT, int G, int V, int PH>
 __global__ void __launch_bounds__(kRowgroupThreads)
     k_rowgroup(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols)
 {
+    pdl_enter();
     using M = Math<DT>;
     constexpr int E = Fmt<DT>::kPerChunk;
     constexpr int NE = PH == kPhAligned ? 0 : edge_slots<DT, G>();
@@ -110,9 +111,8 @@ __global__ void __launch_bounds__(kRowgroupThreads)
 template <int DT, int G, int V, int PH>
 int rowgroup_launch_one(const Launch &l)
 {
-    k_rowgroup<DT, G, V, PH><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-        (const char *)l.x, (char *)l.y, l.rows, l.cols);
-    return (int)cudaGetLastError();
+    return launch_pdl(k_rowgroup<DT, G, V, PH>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+                      (cudaStream_t)l.stream, no_attr(), (const char *)l.x, (char *)l.y, l.rows, l.cols);
 }
 
 template <int DT, int G, int V>

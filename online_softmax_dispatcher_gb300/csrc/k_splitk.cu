@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     k_splitk(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int y_vec,
              unsigned *err)
 {
+    pdl_enter();
     using M = Math<DT>;
     using Acc = typename M::Acc;
     constexpr int E = Fmt<DT>::kPerChunk;
@@ -357,25 +358,14 @@ int splitk_launch_one(const Launch &l)
     int rc = splitk_prepare<DT, A>(C);
     if (rc != 0)
         return rc;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)l.plan.grid_x, (unsigned)l.plan.grid_y, 1);
-    cfg.blockDim = dim3(kSplitThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSplitStages * kSplitStageBytes;
-    cfg.stream = (cudaStream_t)l.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, &k_splitk<DT, A>, (const char *)l.x, (char *)l.y, l.rows, l.cols,
-                                             (int)l.plan.y_vector, l.dev_err);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        return (int)e;
-    }
-    return (int)cudaGetLastError();
+    cudaLaunchAttribute cluster = {};
+    cluster.id = cudaLaunchAttributeClusterDimension;
+    cluster.val.clusterDim.x = (unsigned)C;
+    cluster.val.clusterDim.y = 1;
+    cluster.val.clusterDim.z = 1;
+    return launch_pdl(k_splitk<DT, A>, dim3((unsigned)l.plan.grid_x, (unsigned)l.plan.grid_y, 1), dim3(kSplitThreads),
+                      (size_t)(kSplitStages * kSplitStageBytes), (cudaStream_t)l.stream, cluster, (const char *)l.x,
+                      (char *)l.y, l.rows, l.cols, (int)l.plan.y_vector, l.dev_err);
 }
 
 template <int DT>

@@ -22,6 +22,7 @@ template <int DT, bool ALIGNED>
 __global__ void __launch_bounds__(kStreamThreads)
     k_stream(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int y_vec)
 {
+    pdl_enter();
     using M = Math<DT>;
     __shared__ float smax[32];
     __shared__ typename M::Acc ssum[32];
@@ -47,9 +48,9 @@ namespace {
 template <int DT, bool A>
 int launch_stream_one(const Launch &l)
 {
-    k_stream<DT, A><<<(unsigned)l.plan.grid_x, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-        (const char *)l.x, (char *)l.y, l.rows, l.cols, l.plan.y_vector);
-    return (int)cudaGetLastError();
+    return launch_pdl(k_stream<DT, A>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+                      (cudaStream_t)l.stream, no_attr(), (const char *)l.x, (char *)l.y, l.rows, l.cols,
+                      (int)l.plan.y_vector);
 }
 
 template <int DT>

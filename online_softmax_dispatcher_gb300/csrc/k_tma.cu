@@ -54,6 +54,7 @@ struct TmaParams {
 template <int DT, bool ALIGNED>
 __global__ void __launch_bounds__(kTmaThreads, 1) k_tma(const TmaParams p)
 {
+    pdl_enter();
     using M = Math<DT>;
     using Acc = typename M::Acc;
     constexpr int E = Fmt<DT>::kPerChunk;
@@ -267,8 +268,8 @@ int launch_one(const Launch &l)
     p.stage_bytes = pl.smem_bytes / pl.stages;
     p.y_vec = pl.y_vector;
     p.err = l.dev_err;
-    kern<<<(unsigned)pl.grid_x, kTmaThreads, pl.smem_bytes, (cudaStream_t)l.stream>>>(p);
-    return (int)cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)pl.grid_x), dim3(kTmaThreads), (size_t)pl.smem_bytes,
+                      (cudaStream_t)l.stream, no_attr(), p);
 }
 
 template <int DT>

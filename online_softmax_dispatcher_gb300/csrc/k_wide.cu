@@ -35,6 +35,7 @@ template <int DT, bool ALIGNED>
 __global__ void __launch_bounds__(kStreamThreads, 2)
     k_wide_stats(const char *__restrict__ x, int64_t rows, int64_t cols, int P, float4 *__restrict__ ws)
 {
+    pdl_enter();
     using M = Math<DT>;
     __shared__ float smax[32];
     __shared__ typename M::Acc ssum[32];
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     k_wide_write(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int P,
                  const float4 *__restrict__ ws, int y_vec)
 {
+    pdl_enter();
     const int64_t r = blockIdx.y;
     const int p = blockIdx.x;
     const RowGeom g = row_geom<DT, ALIGNED>(x, y, r, cols);
@@ -119,14 +121,13 @@ int wide_one(const Launch &l, float4 *ws)
 {
     const dim3 grid((unsigned)l.plan.grid_x, (unsigned)l.plan.grid_y, 1);
     const int P = (int)l.plan.grid_x;
-    k_wide_stats<DT, A><<<grid, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>((const char *)l.x, l.rows,
-                                                                                  l.cols, P, ws);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return (int)e;
-    k_wide_write<DT, A><<<grid, l.plan.block_threads, 0, (cudaStream_t)l.stream>>>(
-        (const char *)l.x, (char *)l.y, l.rows, l.cols, P, ws, l.plan.y_vector);
-    return (int)cudaGetLastError();
+    const dim3 block(l.plan.block_threads);
+    const int e = launch_pdl(k_wide_stats<DT, A>, grid, block, 0, (cudaStream_t)l.stream, no_attr(),
+                             (const char *)l.x, l.rows, l.cols, P, ws);
+    if (e != 0)
+        return e;
+    return launch_pdl(k_wide_write<DT, A>, grid, block, 0, (cudaStream_t)l.stream, no_attr(), (const char *)l.x,
+                      (char *)l.y, l.rows, l.cols, P, (const float4 *)ws, (int)l.plan.y_vector);
 }
 
 template <int DT>
