@@ -26,6 +26,11 @@ module only builds that file and marshals numpy arrays into it:
 * ``softmax_masked``        -- softmax(scale * x + mask) with an optional causal
                                mask (attention scores).
 * ``check_masked``          -- streaming comparison against the masked form.
+* ``norm_f64``              -- LayerNorm / RMSNorm along the last dimension
+                               (optional gain and bias), with the per-row mean
+                               and 1/sqrt(var + eps).
+* ``check_norm``            -- streaming comparison of a candidate norm output
+                               (and its fp32 statistics).
 
 bf16 arrays travel as ``numpy.uint16`` bit patterns (numpy has no bfloat16);
 fp16 arrays may be ``numpy.float16`` or ``numpy.uint16`` bit patterns.
@@ -40,6 +45,7 @@ import threading
 import numpy as np
 
 F32, F16, BF16 = 0, 1, 2
+LAYERNORM, RMSNORM = 0, 1
 DTYPE_NAMES = {F32: "fp32", F16: "fp16", BF16: "bf16"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -140,10 +146,13 @@ class Oracle:
                                           ctypes.c_double, ctypes.POINTER(CheckResult)]
         L.oracle_check_bwd.argtypes = [vp, vp, vp, i32, i64, i64, ctypes.c_double, i64, ctypes.c_double,
                                        ctypes.POINTER(CheckResult)]
+        L.oracle_norm_f64.argtypes = [i32, vp, i32, i64, i64, vp, vp, ctypes.c_double, vp, vp, vp]
+        L.oracle_check_norm.argtypes = [i32, vp, vp, i32, i64, i64, vp, vp, ctypes.c_double, vp, vp,
+                                        ctypes.c_double, i64, ctypes.c_double, ctypes.POINTER(CheckResult)]
         for name in ("oracle_decode", "oracle_encode", "oracle_softmax_f64", "oracle_softmax",
                      "oracle_online_softmax_f64", "oracle_check", "oracle_num_threads",
                      "oracle_softmax_bwd_f64", "oracle_check_bwd", "oracle_softmax_masked",
-                     "oracle_check_masked"):
+                     "oracle_check_masked", "oracle_norm_f64", "oracle_check_norm"):
             getattr(L, name).restype = ctypes.c_int
         self.lib = L
         self.path = path
@@ -279,6 +288,57 @@ class Oracle:
             raise ValueError("oracle_check_masked rejected its arguments")
         return res.as_dict()
 
+    def norm_f64(self, kind: int, x: np.ndarray, dtype: int, gamma: np.ndarray | None = None,
+                 beta: np.ndarray | None = None, eps: float = 1e-5):
+        """LayerNorm (kind 0) or RMSNorm (kind 1) of a dtype-typed [rows, cols]
+        array in binary64; gamma / beta: [cols] in the same dtype or None.
+        Returns (y, mean, rstd) as float64 arrays."""
+        xb = _as_bits(x, dtype)
+        rows, cols = _rows_cols(xb)
+        gb = _as_bits(gamma, dtype) if gamma is not None else None
+        bb = _as_bits(beta, dtype) if beta is not None else None
+        for v in (gb, bb):
+            if v is not None and v.size != cols:
+                raise ValueError("gamma / beta must hold cols values")
+        y = np.empty((rows, cols), dtype=np.float64)
+        mean = np.empty(rows, dtype=np.float64)
+        rstd = np.empty(rows, dtype=np.float64)
+        rc = self.lib.oracle_norm_f64(int(kind), _ptr(xb), dtype, rows, cols,
+                                      _ptr(gb) if gb is not None else None,
+                                      _ptr(bb) if bb is not None else None, float(eps), _ptr(y), _ptr(mean),
+                                      _ptr(rstd))
+        if rc != 0:
+            raise ValueError("oracle_norm_f64 rejected its arguments")
+        return y, mean, rstd
+
+    def check_norm(self, kind: int, x: np.ndarray, y: np.ndarray, dtype: int, gamma=None, beta=None,
+                   eps: float = 1e-5, mean=None, rstd=None, *, rel_tol: float = 0.0, max_ulp: int = 0,
+                   k_eps: float = 0.0) -> dict:
+        """Compare a candidate norm output (and optional fp32 mean / rstd per
+        row) with the definition; statistic violations count as
+        rowsum_violations."""
+        xb, yb = _as_bits(x, dtype), _as_bits(y, dtype)
+        if xb.shape != yb.shape:
+            raise ValueError("shape mismatch")
+        rows, cols = _rows_cols(xb)
+        gb = _as_bits(gamma, dtype) if gamma is not None else None
+        bb = _as_bits(beta, dtype) if beta is not None else None
+        mp = np.ascontiguousarray(mean, dtype=np.float32) if mean is not None else None
+        rp = np.ascontiguousarray(rstd, dtype=np.float32) if rstd is not None else None
+        for v in (mp, rp):
+            if v is not None and v.size != rows:
+                raise ValueError("mean / rstd must hold rows values")
+        res = CheckResult()
+        rc = self.lib.oracle_check_norm(int(kind), _ptr(xb), _ptr(yb), dtype, rows, cols,
+                                        _ptr(gb) if gb is not None else None,
+                                        _ptr(bb) if bb is not None else None, float(eps),
+                                        _ptr(mp) if mp is not None else None,
+                                        _ptr(rp) if rp is not None else None, float(rel_tol), int(max_ulp),
+                                        float(k_eps), ctypes.byref(res))
+        if rc != 0:
+            raise ValueError("oracle_check_norm rejected its arguments")
+        return res.as_dict()
+
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
 
@@ -338,3 +398,11 @@ def softmax_bwd_f64(y, dy):
 
 def check_bwd(y, dy, dx, dtype, **kw):
     return default().check_bwd(y, dy, dx, dtype, **kw)
+
+
+def norm_f64(kind, x, dtype, gamma=None, beta=None, eps=1e-5):
+    return default().norm_f64(kind, x, dtype, gamma, beta, eps)
+
+
+def check_norm(kind, x, y, dtype, gamma=None, beta=None, eps=1e-5, mean=None, rstd=None, **kw):
+    return default().check_norm(kind, x, y, dtype, gamma, beta, eps, mean, rstd, **kw)

@@ -49,6 +49,12 @@
  *   section 4.5 and the "[CUDA] safe online softmax" kernels use when they
  *   write half results.
  *
+ *   LayerNorm and RMSNorm along the last dimension (the operators "Softmax
+ *   on DCU", section 9, names as having the same read - reduce - normalise -
+ *   write structure; the Pangu-Weather profile, section 3, standardises fp16
+ *   rows with fp32 mean and variance): the definitions written out at
+ *   oracle_norm_f64 below.
+ *
  * Non-finite inputs follow IEEE propagation through the definition above:
  * a NaN anywhere in a row, a +inf in a row, or a row that is all -inf gives a
  * NaN row; -inf entries in an otherwise finite row give exact zeros.
@@ -741,5 +747,227 @@ int oracle_check_bwd(const void *y, const void *dy, const void *dx, int dtype, i
         free(dys);
         free(want);
     }
+    return failed ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* LayerNorm and RMSNorm along the last dimension                             */
+/* ------------------------------------------------------------------------ */
+
+/* "Softmax on DCU", section 9, names LayerNorm and RMSNorm as operators with
+ * the softmax's read - reduce - normalise - write structure; the Pangu-Weather
+ * profile, section 3, standardises fp16 rows with fp32 mean and variance (its
+ * affine parameters folded into the next layer).  Written out, per row of n
+ * values x_j, with optional per-column gain g_j and bias b_j (absent: g = 1,
+ * b = 0):
+ *   LayerNorm:  mu   = (1/n) sum_j x_j
+ *               var  = (1/n) sum_j (x_j - mu)^2      (population variance,
+ *                                                      about the mean: two passes)
+ *               rstd = 1 / sqrt(var + eps)
+ *               y_j  = (x_j - mu) * rstd * g_j + b_j
+ *   RMSNorm:    ms   = (1/n) sum_j x_j^2
+ *               rstd = 1 / sqrt(ms + eps)
+ *               y_j  = x_j * rstd * g_j                (no bias)
+ * Binary64 throughout; the sums are Neumaier-compensated. */
+
+#define ORACLE_LAYERNORM 0
+#define ORACLE_RMSNORM 1
+
+static double nsum_add(double s, double t, double *c)
+{
+    double u = s + t;
+    if (fabs(s) >= fabs(t))
+        *c += (s - u) + t;
+    else
+        *c += (t - u) + s;
+    return u;
+}
+
+/* One row: y (n values), and the statistics mu (LayerNorm; 0 for RMSNorm),
+ * rstd and a = (1/n) sum_j |x_j| (the scale of the rounding errors an fp32
+ * evaluation of the statistics makes). */
+static void norm_row(int kind, const double *x, int64_t n, const double *g, const double *b, double eps,
+                     double *y, double *mu_out, double *rstd_out, double *a_out)
+{
+    double s = 0.0, c = 0.0, sa = 0.0, ca = 0.0;
+    for (int64_t j = 0; j < n; j++) {
+        s = nsum_add(s, x[j], &c);
+        sa = nsum_add(sa, fabs(x[j]), &ca);
+    }
+    const double mu = kind == ORACLE_LAYERNORM ? (s + c) / (double)n : 0.0;
+    double q = 0.0, cq = 0.0;
+    for (int64_t j = 0; j < n; j++) {
+        double d = x[j] - mu;
+        q = nsum_add(q, d * d, &cq);
+    }
+    const double var = (q + cq) / (double)n;
+    const double rstd = 1.0 / sqrt(var + eps);
+    for (int64_t j = 0; j < n; j++) {
+        double v = (x[j] - mu) * rstd;
+        if (g)
+            v *= g[j];
+        if (b && kind == ORACLE_LAYERNORM)
+            v += b[j];
+        y[j] = v;
+    }
+    *mu_out = mu;
+    *rstd_out = rstd;
+    *a_out = (sa + ca) / (double)n;
+}
+
+static int decode_vec(const void *v, int dtype, int64_t n, double **out)
+{
+    *out = NULL;
+    if (!v)
+        return 0;
+    *out = (double *)malloc((size_t)n * sizeof(double));
+    if (!*out)
+        return -1;
+    for (int64_t j = 0; j < n; j++)
+        (*out)[j] = decode_at(v, dtype, j);
+    return 0;
+}
+
+/* y (binary64, [rows, cols]) = the norm of x (dtype); gamma, beta: [cols] in
+ * x's dtype or NULL; mean, rstd: [rows] binary64 or NULL. */
+int oracle_norm_f64(int kind, const void *x, int dtype, int64_t rows, int64_t cols, const void *gamma,
+                    const void *beta, double eps, double *y, double *mean, double *rstd)
+{
+    if ((kind != ORACLE_LAYERNORM && kind != ORACLE_RMSNORM) || rows < 0 || cols < 0 || dtype < 0 ||
+        dtype > 2 || !(eps >= 0.0) || (rows > 0 && cols > 0 && (!x || !y)))
+        return ORACLE_EINVAL;
+    if (rows == 0 || cols == 0)
+        return ORACLE_OK;
+    double *g = NULL, *b = NULL;
+    if (decode_vec(gamma, dtype, cols, &g) || decode_vec(beta, dtype, cols, &b)) {
+        free(g);
+        free(b);
+        return ORACLE_EINVAL;
+    }
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *xs = (double *)malloc((size_t)cols * sizeof(double));
+        if (!xs) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < rows; r++) {
+            if (!xs)
+                continue;
+            for (int64_t j = 0; j < cols; j++)
+                xs[j] = decode_at(x, dtype, r * cols + j);
+            double mu, rs, a;
+            norm_row(kind, xs, cols, g, b, eps, y + r * cols, &mu, &rs, &a);
+            if (mean)
+                mean[r] = mu;
+            if (rstd)
+                rstd[r] = rs;
+        }
+        free(xs);
+    }
+    free(g);
+    free(b);
+    return failed ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/* Compare a candidate y (dtype) -- and, when given, its fp32 per-row mean and
+ * rstd -- with the definition.  Element j passes when
+ *     |y_j - y*_j| <= max_ulp * ulp_dtype(y*_j) + rel_tol * |y*_j|
+ *                     + k_eps * 2^-24 * (|g_j| * (|z_j| + a * rstd) + |b_j|)
+ * with z_j = (x_j - mu) * rstd the normalised value, a = (1/n) sum |x_j| and
+ * the a * rstd term only for LayerNorm: fp32 statistics carry errors of a few
+ * 2^-24 relative to the magnitudes summed, and an error d in mu moves every
+ * output by d * rstd * g_j, which no relative bound on y*_j covers where
+ * x_j is close to mu.  The statistics pass when |mean - mu| <= k_eps * 2^-24 *
+ * a and |rstd - rstd*| <= k_eps * 2^-24 * rstd*. */
+int oracle_check_norm(int kind, const void *x, const void *y, int dtype, int64_t rows, int64_t cols,
+                      const void *gamma, const void *beta, double eps, const float *mean, const float *rstd,
+                      double rel_tol, int64_t max_ulp, double k_eps, oracle_check_result *res)
+{
+    if (!res || (kind != ORACLE_LAYERNORM && kind != ORACLE_RMSNORM) || rows < 0 || cols < 0 || dtype < 0 ||
+        dtype > 2 || !(eps >= 0.0))
+        return ORACLE_EINVAL;
+    memset(res, 0, sizeof *res);
+    res->first_bad = -1;
+    if (rows == 0 || cols == 0)
+        return ORACLE_OK;
+    if (!x || !y)
+        return ORACLE_EINVAL;
+    double *g = NULL, *b = NULL;
+    if (decode_vec(gamma, dtype, cols, &g) || decode_vec(beta, dtype, cols, &b)) {
+        free(g);
+        free(b);
+        return ORACLE_EINVAL;
+    }
+    const double u = k_eps * ldexp(1.0, -24);
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *xs = (double *)malloc((size_t)cols * sizeof(double));
+        double *want = (double *)malloc((size_t)cols * sizeof(double));
+        oracle_check_result loc;
+        memset(&loc, 0, sizeof loc);
+        loc.first_bad = -1;
+        if (!xs || !want) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; r++) {
+            if (!xs || !want)
+                continue;
+            for (int64_t j = 0; j < cols; j++)
+                xs[j] = decode_at(x, dtype, r * cols + j);
+            double mu, rs, a;
+            norm_row(kind, xs, cols, g, b, eps, want, &mu, &rs, &a);
+            const double shift = kind == ORACLE_LAYERNORM ? a * rs : 0.0;
+            for (int64_t j = 0; j < cols; j++) {
+                int64_t flat = r * cols + j;
+                double got = decode_at(y, dtype, flat);
+                double w = want[j];
+                int bad;
+                if (isnan(w) || isnan(got)) {
+                    bad = !(isnan(w) && isnan(got));
+                } else {
+                    double z = (xs[j] - mu) * rs;
+                    double gj = g ? fabs(g[j]) : 1.0;
+                    double bj = (b && kind == ORACLE_LAYERNORM) ? fabs(b[j]) : 0.0;
+                    double err = fabs(got - w);
+                    double bound = (double)max_ulp * dtype_ulp(w, dtype) + rel_tol * fabs(w) +
+                                   u * (gj * (fabs(z) + shift) + bj);
+                    bad = !(err <= bound);
+                    if (!isfinite(got))
+                        loc.nonfinite++;
+                    double ulps = err / dtype_ulp(w, dtype);
+                    if ((int64_t)ulps > loc.max_ulp)
+                        loc.max_ulp = (int64_t)ulps;
+                    if (w != 0.0 && err / fabs(w) > loc.max_rel)
+                        loc.max_rel = err / fabs(w);
+                }
+                if (bad) {
+                    if (loc.first_bad < 0 || flat < loc.first_bad)
+                        loc.first_bad = flat;
+                    loc.violations++;
+                }
+                loc.checked++;
+            }
+            /* the statistics (their violations count in rowsum_violations) */
+            int sbad = 0;
+            if (mean && kind == ORACLE_LAYERNORM && isfinite(mu))
+                sbad |= !(fabs((double)mean[r] - mu) <= u * a);
+            if (rstd && isfinite(rs))
+                sbad |= !(fabs((double)rstd[r] - rs) <= u * rs);
+            if (sbad)
+                loc.rowsum_violations++;
+        }
+#pragma omp critical
+        merge_result(res, &loc);
+        free(xs);
+        free(want);
+    }
+    free(g);
+    free(b);
     return failed ? ORACLE_EINVAL : ORACLE_OK;
 }

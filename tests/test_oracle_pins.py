@@ -388,6 +388,159 @@ def pin_masked_check_helper(o):
     assert o.check_masked(x, bad, F16, 0.25, mask, 3, zrel=1.01 * rel / zmax, **kw)["violations"] == 0
 
 
+# ----------------------------------------------------------------------------- LayerNorm / RMSNorm
+
+
+def _norm_inputs(rng, rows, cols, dt, loc=0.0, scale=1.0):
+    v = rng.normal(loc, scale, (rows, cols))
+    if dt == F32:
+        return v.astype(np.float32)
+    if dt == F16:
+        return v.astype(np.float16)
+    return _bf16_bits_from_f32(v.astype(np.float32)).reshape(rows, cols)
+
+
+def pin_norm_torch_layer_norm(o):
+    # torch's float64 layer_norm (its own implementation) on the decoded values
+    rng = np.random.default_rng(30)
+    for dt in (F32, F16, BF16):
+        for eps in (1e-5, 1e-2):
+            x = _norm_inputs(rng, 7, 33, dt, loc=3.0, scale=2.0)
+            g = _norm_inputs(rng, 1, 33, dt, loc=1.0, scale=0.5)[0]
+            b = _norm_inputs(rng, 1, 33, dt)[0]
+            y, mean, rstd = o.norm_f64(oracle.LAYERNORM, x, dt, g, b, eps)
+            xd, gd, bd = (torch.from_numpy(o.decode(v, dt)) for v in (x, g, b))
+            ref = torch.nn.functional.layer_norm(xd, (33,), gd, bd, eps).numpy()
+            assert np.abs(y - ref).max() <= 1e-12, (dt, eps)
+            var, mu = torch.var_mean(xd, dim=1, unbiased=False)
+            assert np.abs(mean - mu.numpy()).max() <= 1e-13
+            assert np.abs(rstd - 1 / np.sqrt(var.numpy() + eps)).max() <= 1e-12 * rstd.max()
+
+
+def pin_norm_torch_rms_norm(o):
+    rng = np.random.default_rng(31)
+    for dt in (F32, F16, BF16):
+        x = _norm_inputs(rng, 5, 40, dt, loc=0.5, scale=3.0)
+        g = _norm_inputs(rng, 1, 40, dt, loc=1.0, scale=0.5)[0]
+        y, _, rstd = o.norm_f64(oracle.RMSNORM, x, dt, g, None, 1e-6)
+        xd, gd = torch.from_numpy(o.decode(x, dt)), torch.from_numpy(o.decode(g, dt))
+        ref = torch.nn.functional.rms_norm(xd, (40,), gd, 1e-6).numpy()
+        assert np.abs(y - ref).max() <= 1e-12 * np.abs(ref).max(), dt
+        assert np.abs(rstd - 1 / np.sqrt((xd.numpy() ** 2).mean(1) + 1e-6)).max() <= 1e-12 * rstd.max()
+        # a bias is ignored by RMSNorm
+        y2, _, _ = o.norm_f64(oracle.RMSNORM, x, dt, g, g, 1e-6)
+        assert (y2 == y).all()
+
+
+def pin_norm_two_elements(o):
+    # x = [a, b]: mu = (a + b) / 2, var = d^2 with d = (a - b) / 2, so
+    # y = (d, -d) / sqrt(d^2 + eps)
+    rng = np.random.default_rng(32)
+    ab = rng.normal(0, 4, (64, 2)).astype(np.float32)
+    for eps in (0.0, 0.25):
+        y, _, _ = o.norm_f64(oracle.LAYERNORM, ab, F32, None, None, eps)
+        a, b = ab[:, 0].astype(np.float64), ab[:, 1].astype(np.float64)
+        d = (a - b) / 2
+        want = d / np.sqrt(d * d + eps)
+        assert np.abs(y[:, 0] - want).max() <= 1e-15 and np.abs(y[:, 1] + want).max() <= 1e-15
+
+
+def pin_norm_brute_force_tiny(o):
+    # every row of length 1..3 over a small value set against exact rational
+    # statistics (fractions), rounded once at the square root
+    from fractions import Fraction
+    vals = [-3.0, -0.5, 0.0, 0.25, 1.0, 6.0]
+    eps = Fraction(1, 64)
+    for n in (1, 2, 3):
+        rows = np.array(np.meshgrid(*([vals] * n), indexing="ij")).reshape(n, -1).T.astype(np.float32)
+        for kind in (oracle.LAYERNORM, oracle.RMSNORM):
+            y, _, _ = o.norm_f64(kind, rows, F32, None, None, float(eps))
+            for r, row in enumerate(rows):
+                fr = [Fraction(float(v)) for v in row]
+                mu = sum(fr) / n if kind == oracle.LAYERNORM else Fraction(0)
+                var = sum((v - mu) ** 2 for v in fr) / n
+                rs = 1 / math.sqrt(var + eps)
+                want = [float(v - mu) * rs for v in fr]
+                assert np.abs(y[r] - want).max() <= 1e-15 * (1 + np.abs(want).max()), (kind, row)
+
+
+def pin_norm_dyadic_invariances(o):
+    # on dyadic grids with a power-of-two row length (the mean is then exact)
+    # these hold bit for bit: LayerNorm(x + c) == LayerNorm(x), and
+    # norm(2^k x, 4^k eps) == norm(x, eps) for both kinds
+    rng = np.random.default_rng(33)
+    x = (np.round(rng.normal(0, 8, (6, 128)) * 16) / 16).astype(np.float32)
+    y0, _, _ = o.norm_f64(oracle.LAYERNORM, x, F32, None, None, 0.5)
+    y1, _, _ = o.norm_f64(oracle.LAYERNORM, (x + 32).astype(np.float32), F32, None, None, 0.5)
+    assert (y0 == y1).all()
+    for kind in (oracle.LAYERNORM, oracle.RMSNORM):
+        a, _, ra = o.norm_f64(kind, x, F32, None, None, 0.5)
+        b, _, rb = o.norm_f64(kind, (x * 8).astype(np.float32), F32, None, None, 0.5 * 64)
+        assert (a == b).all() and (ra == rb * 8).all()
+
+
+def pin_norm_moments(o):
+    # the standardised row has mean 0 and mean square var / (var + eps);
+    # RMSNorm's has mean square ms / (ms + eps) (moments by math.fsum)
+    rng = np.random.default_rng(34)
+    x = rng.normal(5, 3, (4, 1000)).astype(np.float32)
+    xd = x.astype(np.float64)
+    for kind in (oracle.LAYERNORM, oracle.RMSNORM):
+        y, mean, rstd = o.norm_f64(kind, x, F32, None, None, 1e-3)
+        for r in range(4):
+            mu = math.fsum(xd[r]) / 1000 if kind == oracle.LAYERNORM else 0.0
+            var = math.fsum((xd[r] - mu) ** 2) / 1000
+            rs = 1 / math.sqrt(var + 1e-3)
+            want_mean = 0.0 if kind == oracle.LAYERNORM else math.fsum(xd[r]) / 1000 * rs
+            assert abs(math.fsum(y[r]) / 1000 - want_mean) <= 1e-12
+            assert abs(math.fsum(y[r] ** 2) / 1000 - var / (var + 1e-3)) <= 1e-12
+            assert abs(mean[r] - mu) <= 1e-12 and abs(rstd[r] - 1 / math.sqrt(var + 1e-3)) <= 1e-12
+
+
+def pin_norm_affine_columns(o):
+    # gain and bias act per column: y(g, b)_j == z_j * g_j + b_j
+    rng = np.random.default_rng(35)
+    x = rng.normal(0, 2, (3, 17)).astype(np.float32)
+    g = np.linspace(-2, 3, 17).astype(np.float32)
+    b = np.arange(17, dtype=np.float32) * 0.25
+    z, _, _ = o.norm_f64(oracle.LAYERNORM, x, F32, None, None, 1e-5)
+    y, _, _ = o.norm_f64(oracle.LAYERNORM, x, F32, g, b, 1e-5)
+    assert (y == z * g.astype(np.float64) + b.astype(np.float64)).all()
+    zr, _, _ = o.norm_f64(oracle.RMSNORM, x, F32, None, None, 1e-5)
+    yr, _, _ = o.norm_f64(oracle.RMSNORM, x, F32, g, None, 1e-5)
+    assert (yr == zr * g.astype(np.float64)).all()
+
+
+def pin_norm_check_helper(o):
+    # the checker's budget: an element at x_j == mu (z = 0) may be off by
+    # about k 2^-24 a rstd (the fp32 error of the mean), not by twice that
+    x = np.array([[-3.0, 0.0, 3.0, -1.0, 1.0]], dtype=np.float32)
+    y, mean, rstd = o.norm_f64(oracle.LAYERNORM, x, F32, None, None, 0.0)
+    a = np.abs(x.astype(np.float64)).mean()
+    bound = 64 * 2.0**-24 * a * rstd[0]
+    for f, want in ((0.5, 0), (2.0, 1)):
+        cand = y.astype(np.float32)
+        cand[0, 1] = np.float32(f * bound)
+        r = o.check_norm(oracle.LAYERNORM, x, cand, F32, eps=0.0, k_eps=64)
+        assert r["violations"] == want and (want == 0 or r["first_bad"] == 1), (f, r)
+    # fp16 outputs: one ulp passes, two fail, at the right element
+    x16 = np.random.default_rng(36).normal(0, 1, (2, 50)).astype(np.float16)
+    want16 = o.encode(o.norm_f64(oracle.RMSNORM, x16, F16)[0], F16)
+    for d, nbad in ((1, 0), (2, 1)):
+        cand = want16.copy()
+        cand[1, 7] = cand[1, 7] + d if cand[1, 7] & 0x7FFF else cand[1, 7]
+        r = o.check_norm(oracle.RMSNORM, x16, cand.view(np.float16), F16, max_ulp=1)
+        assert r["violations"] == nbad and (nbad == 0 or r["first_bad"] == 57), (d, r)
+    # statistics: planted errors in mean and rstd are counted per row
+    _, m, s = o.norm_f64(oracle.LAYERNORM, x16, F16)
+    mf, sf = m.astype(np.float32), s.astype(np.float32)
+    assert o.check_norm(oracle.LAYERNORM, x16, o.encode(o.norm_f64(oracle.LAYERNORM, x16, F16)[0], F16).view(np.float16),
+                        F16, mean=mf, rstd=sf, max_ulp=1, k_eps=64)["rowsum_violations"] == 0
+    sf[1] *= 1.001
+    assert o.check_norm(oracle.LAYERNORM, x16, o.encode(o.norm_f64(oracle.LAYERNORM, x16, F16)[0], F16).view(np.float16),
+                        F16, mean=mf, rstd=sf, max_ulp=1, k_eps=64)["rowsum_violations"] == 1
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
@@ -429,6 +582,18 @@ MUTANTS = [
     ("scale_ignored", "double v = scale * decode_at(x, dtype, r * cols + j);",
      "double v = decode_at(x, dtype, r * cols + j);"),
     ("bwd_missing_y", "double t = dyr[j] * yr[j];", "double t = dyr[j];"),
+    ("norm_unbiased_variance", "const double var = (q + cq) / (double)n;",
+     "const double var = (q + cq) / (double)(n > 1 ? n - 1 : 1);"),
+    ("norm_eps_outside_sqrt", "const double rstd = 1.0 / sqrt(var + eps);", "const double rstd = 1.0 / (sqrt(var) + eps);"),
+    ("norm_no_sqrt", "const double rstd = 1.0 / sqrt(var + eps);", "const double rstd = 1.0 / (var + eps);"),
+    ("norm_bias_dropped", "            v += b[j];", "            v += 0.0 * b[j];"),
+    ("norm_gain_column", "            v *= g[j];", "            v *= g[n - 1 - j];"),
+    ("norm_rms_centred", "const double mu = kind == ORACLE_LAYERNORM ? (s + c) / (double)n : 0.0;",
+     "const double mu = (s + c) / (double)n;"),
+    ("norm_mean_count", "const double mu = kind == ORACLE_LAYERNORM ? (s + c) / (double)n : 0.0;",
+     "const double mu = kind == ORACLE_LAYERNORM ? (s + c) / (double)(n + 1) : 0.0;"),
+    ("norm_check_drops_mean_error", "u * (gj * (fabs(z) + shift) + bj);", "u * (gj * fabs(z) + bj);"),
+    ("norm_check_ignores_rstd", "sbad |= !(fabs((double)rstd[r] - rs) <= u * rs);", "sbad |= 0;"),
     ("bwd_drops_compensation", "    s += c;\n    for (int64_t j = 0; j < cols; j++)\n        dxr[j]",
      "    for (int64_t j = 0; j < cols; j++)\n        dxr[j]"),
 ]
