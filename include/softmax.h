@@ -237,6 +237,52 @@ int softmax_fwd_noalloc(const void *x, void *y, int64_t rows, int64_t cols, int 
                         softmax_stream_t stream);
 
 /*
+ * layernorm_fwd -- LayerNorm along the last dimension, on the softmax's
+ * read - reduce - normalise - write skeleton ("Softmax on DCU", section 9,
+ * names LayerNorm and RMSNorm as operators of that shape; the Pangu-Weather
+ * profile, section 3, standardises fp16 rows with fp32 mean and variance):
+ *     mu   = (1/n) sum_j x[r, j]                 n = cols
+ *     var  = (1/n) sum_j (x[r, j] - mu)^2        population variance
+ *     rstd = 1 / sqrt(var + eps)
+ *     y[r, j] = (x[r, j] - mu) * rstd * gamma[j] + beta[j]
+ *   x, y    as softmax_fwd (same dtype; y may be x itself, in place).
+ *   gamma   device pointer, [cols] of `dtype`, or NULL (gain 1).
+ *   beta    device pointer, [cols] of `dtype`, or NULL (bias 0).  Neither may
+ *           overlap y.
+ *   eps     >= 0 and finite, added to the variance.
+ *   mean    device pointer, [rows] fp32, or NULL: mu of each row.
+ *   rstd    device pointer, [rows] fp32, or NULL: rstd of each row.  mean and
+ *           rstd must be 4-byte aligned and overlap nothing else.
+ * The row is held in registers between its reductions (one HBM read of x, one
+ * write of y); mu and var are accumulated in fp32 (compensated for fp32
+ * input) and var is taken about mu, from the registers.  Accuracy against the
+ * exact result y*:
+ *     |y - y*| <= u(y*) + 64 * 2^-24 * (|gamma_j| * (|z_j| + a * rstd) + |beta_j|)
+ * with z_j = (x_j - mu) * rstd, a = (1/n) sum_j |x_j| and u = 1 ulp of the
+ * dtype at y* for fp16 / bf16, 0 for fp32 (the second term is the fp32
+ * rounding of the statistics); mean and rstd within 64 * 2^-24 of a and of
+ * rstd*.  Rows of up to 4096 chunks of 16 bytes (64 KiB):
+ * SOFTMAX_ERR_UNSUPPORTED_SHAPE beyond.  Streams, errors: as softmax_fwd.
+ */
+int layernorm_fwd(const void *x, void *y, int64_t rows, int64_t cols, int dtype, const void *gamma,
+                  const void *beta, float eps, float *mean, float *rstd, softmax_stream_t stream);
+
+/*
+ * rmsnorm_fwd -- RMSNorm along the last dimension:
+ *     rstd = 1 / sqrt((1/n) sum_j x[r, j]^2 + eps);   y[r, j] = x[r, j] * rstd * gamma[j]
+ * Arguments, accuracy (without the a * rstd term) and limits as
+ * layernorm_fwd, with no bias and no mean.
+ */
+int rmsnorm_fwd(const void *x, void *y, int64_t rows, int64_t cols, int dtype, const void *gamma, float eps,
+                float *rstd, softmax_stream_t stream);
+
+/* norm_fwd_variant -- layernorm_fwd (kind 0) or rmsnorm_fwd (kind 1, beta and
+ * mean ignored) with the kernel forced: SOFTMAX_VARIANT_ROWGROUP (rows of up
+ * to 128 chunks of 16 bytes) or SOFTMAX_VARIANT_BLOCK; AUTO chooses. */
+int norm_fwd_variant(int kind, const void *x, void *y, int64_t rows, int64_t cols, int dtype, const void *gamma,
+                     const void *beta, float eps, float *mean, float *rstd, int variant, softmax_stream_t stream);
+
+/*
  * softmax_query_variant -- the variant softmax_fwd would launch for these
  * arguments on the current device, written to *variant.  Validates the
  * arguments exactly as softmax_fwd does; launches nothing.

@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     softmax_get_device_error, softmax_last_cuda_error, softmax_plan, softmax_query_variant,
     softmax_selftest_bounded_wait, softmax_backward, softmax_bwd, softmax_bwd_variant, softmax_fwd_ws,
     softmax_workspace_size, softmax_fwd_noalloc, softmax_fwd_masked, softmax_fwd_masked_variant,
-    softmax_masked, softmax_,
+    softmax_masked, softmax_, layernorm_fwd, rmsnorm_fwd, norm_fwd_variant, layer_norm, rms_norm,
+    LAYERNORM, RMSNORM,
     softmax_strerror, softmax_variant_name,
 )

@@ -46,7 +46,9 @@ EXPORTS = (
     "softmax_last_cuda_error", "softmax_strerror", "softmax_variant_name", "softmax_abi_version",
     "softmax_selftest_bounded_wait", "softmax_bwd", "softmax_bwd_variant", "softmax_fwd_ws",
     "softmax_workspace_size", "softmax_fwd_noalloc", "softmax_fwd_masked", "softmax_fwd_masked_variant",
+    "layernorm_fwd", "rmsnorm_fwd", "norm_fwd_variant",
 )
+LAYERNORM, RMSNORM = 0, 1
 
 
 class SoftmaxLibraryMissing(RuntimeError):
@@ -115,6 +117,9 @@ def lib() -> ctypes.CDLL:
                 "softmax_fwd_noalloc": [vp, vp, i64, i64, i32, vp],
                 "softmax_fwd_masked": [vp, vp, i64, i64, i32, ctypes.c_float, vp, i64, i64, vp],
                 "softmax_fwd_masked_variant": [vp, vp, i64, i64, i32, ctypes.c_float, vp, i64, i64, i32, vp],
+                "layernorm_fwd": [vp, vp, i64, i64, i32, vp, vp, ctypes.c_float, vp, vp, vp],
+                "rmsnorm_fwd": [vp, vp, i64, i64, i32, vp, ctypes.c_float, vp, vp],
+                "norm_fwd_variant": [i32, vp, vp, i64, i64, i32, vp, vp, ctypes.c_float, vp, vp, i32, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -152,6 +157,23 @@ def softmax_fwd_masked(x: int, y: int, rows: int, cols: int, dtype: int, scale: 
                        mask_rows: int, causal_q: int, stream: int = 0) -> int:
     return lib().softmax_fwd_masked(x, y, rows, cols, dtype, scale, mask or None, mask_rows, causal_q,
                                     stream or None)
+
+
+def layernorm_fwd(x: int, y: int, rows: int, cols: int, dtype: int, gamma: int, beta: int, eps: float, mean: int,
+                  rstd: int, stream: int = 0) -> int:
+    return lib().layernorm_fwd(x, y, rows, cols, dtype, gamma or None, beta or None, eps, mean or None,
+                               rstd or None, stream or None)
+
+
+def rmsnorm_fwd(x: int, y: int, rows: int, cols: int, dtype: int, gamma: int, eps: float, rstd: int,
+                stream: int = 0) -> int:
+    return lib().rmsnorm_fwd(x, y, rows, cols, dtype, gamma or None, eps, rstd or None, stream or None)
+
+
+def norm_fwd_variant(kind: int, x: int, y: int, rows: int, cols: int, dtype: int, gamma: int, beta: int,
+                     eps: float, mean: int, rstd: int, variant: int, stream: int = 0) -> int:
+    return lib().norm_fwd_variant(kind, x, y, rows, cols, dtype, gamma or None, beta or None, eps, mean or None,
+                                  rstd or None, variant, stream or None)
 
 
 def softmax_fwd_masked_variant(x: int, y: int, rows: int, cols: int, dtype: int, scale: float, mask: int,
@@ -325,6 +347,49 @@ def softmax_masked(x, *, scale: float = 1.0, mask=None, causal: bool = False, ou
     if rc != OK:
         raise SoftmaxError(rc)
     return y
+
+
+def _norm(kind, x, weight, bias, eps, out, mean, rstd, variant, stream):
+    import torch
+
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or not x.is_contiguous() or x.dim() == 0:
+        raise SoftmaxError(ERR_INVALID_ARG, "x must be a contiguous CUDA tensor")
+    dt = dtype_code(x.dtype)
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    for name, v in (("weight", weight), ("bias", bias)):
+        if v is not None and (v.dtype != x.dtype or not v.is_cuda or not v.is_contiguous() or v.numel() != cols):
+            raise SoftmaxError(ERR_INVALID_ARG, f"{name} must be a contiguous CUDA tensor of {cols} x-dtype values")
+    for name, v in (("mean", mean), ("rstd", rstd)):
+        if v is not None and (v.dtype != torch.float32 or not v.is_cuda or not v.is_contiguous() or v.numel() != rows):
+            raise SoftmaxError(ERR_INVALID_ARG, f"{name} must be a contiguous CUDA float32 tensor of {rows} values")
+    y = torch.empty_like(x) if out is None else out
+    if y.shape != x.shape or y.dtype != x.dtype or not y.is_contiguous() or y.device != x.device:
+        raise SoftmaxError(ERR_INVALID_ARG, "out must match x in shape, dtype and device and be contiguous")
+    s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
+    if isinstance(variant, str):
+        variant = VARIANTS[variant]
+    ptr = (lambda t: t.data_ptr() if t is not None else 0)
+    with torch.cuda.device(x.device):
+        rc = norm_fwd_variant(kind, x.data_ptr(), y.data_ptr(), rows, cols, dt, ptr(weight), ptr(bias), float(eps),
+                              ptr(mean), ptr(rstd), variant, s)
+    if rc != OK:
+        raise SoftmaxError(rc)
+    return y
+
+
+def layer_norm(x, weight=None, bias=None, *, eps: float = 1e-5, out=None, mean=None, rstd=None,
+               variant: int | str = VARIANT_AUTO, stream=None):
+    """LayerNorm over the last dimension of a contiguous CUDA tensor (weight /
+    bias: [cols] of x's dtype or None; mean / rstd: optional float32 [rows]
+    outputs).  `out` may be x itself (in place)."""
+    return _norm(LAYERNORM, x, weight, bias, eps, out, mean, rstd, variant, stream)
+
+
+def rms_norm(x, weight=None, *, eps: float = 1e-6, out=None, rstd=None, variant: int | str = VARIANT_AUTO,
+             stream=None):
+    """RMSNorm over the last dimension of a contiguous CUDA tensor."""
+    return _norm(RMSNORM, x, weight, None, eps, out, None, rstd, variant, stream)
 
 
 def softmax_backward(y, dy, *, out=None, variant: int | str = VARIANT_AUTO, stream=None):

@@ -211,6 +211,44 @@ OSD_API int softmax_fwd_masked(const void *x, void *y, int64_t rows, int64_t col
                                       SOFTMAX_VARIANT_AUTO, stream);
 }
 
+OSD_API int norm_fwd_variant(int kind, const void *x, void *y, int64_t rows, int64_t cols, int dtype,
+                             const void *gamma, const void *beta, float eps, float *mean, float *rstd, int variant,
+                             softmax_stream_t stream)
+{
+    int rc = validate_norm_args(kind, x, y, rows, cols, dtype, gamma, beta, eps, mean, rstd);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (variant < SOFTMAX_VARIANT_AUTO || variant >= SOFTMAX_VARIANT_COUNT)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    DeviceCache *dc = nullptr;
+    rc = current_device(&dc);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    NormLaunch l{x, y, rows, cols, dtype, {}, stream, kind, 0, gamma, kind == kNormLayer ? beta : nullptr, eps,
+                 kind == kNormLayer ? mean : nullptr, rstd};
+    rc = plan_norm(dc->info, kind, x, y, rows, cols, dtype, gamma, l.beta, variant, &l.plan, &l.mode);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    const int e = launch_norm(l);
+    return e == 0 ? SOFTMAX_OK : cuda_fail((cudaError_t)e);
+}
+
+OSD_API int layernorm_fwd(const void *x, void *y, int64_t rows, int64_t cols, int dtype, const void *gamma,
+                          const void *beta, float eps, float *mean, float *rstd, softmax_stream_t stream)
+{
+    return norm_fwd_variant(kNormLayer, x, y, rows, cols, dtype, gamma, beta, eps, mean, rstd,
+                            SOFTMAX_VARIANT_AUTO, stream);
+}
+
+OSD_API int rmsnorm_fwd(const void *x, void *y, int64_t rows, int64_t cols, int dtype, const void *gamma,
+                        float eps, float *rstd, softmax_stream_t stream)
+{
+    return norm_fwd_variant(kNormRms, x, y, rows, cols, dtype, gamma, nullptr, eps, nullptr, rstd,
+                            SOFTMAX_VARIANT_AUTO, stream);
+}
+
 OSD_API int softmax_bwd_variant(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, int dtype,
                                 int variant, softmax_stream_t stream)
 {

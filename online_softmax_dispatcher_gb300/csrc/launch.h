@@ -82,6 +82,47 @@ int launch_masked(const MaskedLaunch &l);
 int plan_masked(const softmax_device_info &dev, const void *x, const void *y, int64_t rows, int64_t cols,
                 int dtype, int variant, softmax_launch_plan *plan);
 
+// LayerNorm / RMSNorm (k_norm.cuh): kind 0 / 1; `mode` says how rows, y and the
+// gain / bias vectors sit on the 16-byte grid (kNormFast: rows, y, gamma and
+// beta all on it -- vector gain / bias loads; kNormSame: y on x's phase;
+// kNormOther: y on another phase).
+constexpr int kNormLayer = 0;
+constexpr int kNormRms = 1;
+constexpr int kNormFast = 0;
+constexpr int kNormSame = 1;
+constexpr int kNormOther = 2;
+constexpr int kNormMaxV = 4;  // chunks per thread (registers)
+
+struct NormLaunch {
+    const void *x;
+    void *y;
+    int64_t rows;
+    int64_t cols;
+    int dtype;
+    softmax_launch_plan plan;
+    CUstream_st *stream;
+    int kind;
+    int mode;
+    const void *gamma;
+    const void *beta;
+    float eps;
+    float *mean;
+    float *rstd;
+};
+
+int launch_norm_f32(const NormLaunch &l);
+int launch_norm_f16(const NormLaunch &l);
+int launch_norm_bf16(const NormLaunch &l);
+inline int launch_norm(const NormLaunch &l)
+{
+    return l.dtype == SOFTMAX_F32 ? launch_norm_f32(l)
+                                  : (l.dtype == SOFTMAX_F16 ? launch_norm_f16(l) : launch_norm_bf16(l));
+}
+int validate_norm_args(int kind, const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
+                       const void *gamma, const void *beta, float eps, const float *mean, const float *rstd);
+int plan_norm(const softmax_device_info &dev, int kind, const void *x, const void *y, int64_t rows, int64_t cols,
+              int dtype, const void *gamma, const void *beta, int variant, softmax_launch_plan *plan, int *mode);
+
 // Remember a failing cudaError_t for softmax_last_cuda_error (this thread) and
 // return SOFTMAX_ERR_CUDA.
 int record_cuda_error(int cuda_error);

@@ -380,6 +380,120 @@ int plan_masked(const softmax_device_info &dev, const void *x, const void *y, in
     return SOFTMAX_OK;
 }
 
+// ---------------------------------------------------------------- LayerNorm / RMSNorm
+
+namespace {
+
+bool ranges_meet(uintptr_t a, uint64_t na, uintptr_t b, uint64_t nb) { return a < b + nb && b < a + na; }
+
+}  // namespace
+
+int validate_norm_args(int kind, const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
+                       const void *gamma, const void *beta, float eps, const float *mean, const float *rstd)
+{
+    if (kind != kNormLayer && kind != kNormRms)
+        return SOFTMAX_ERR_INVALID_ARG;
+    int rc = validate_args(x, y, rows, cols, dtype);  // dtype, sizes, alignment, x / y overlap
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (!(eps >= 0.0f) || !(eps <= 3.4e38f))
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    const int64_t S = dtype_bytes(dtype);
+    const uint64_t ybytes = (uint64_t)(rows * cols * S), vbytes = (uint64_t)(cols * S);
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
+    // gain and bias are read by every row while y is written
+    for (const void *v : {gamma, kind == kNormLayer ? beta : nullptr}) {
+        if (!v)
+            continue;
+        const uintptr_t va = reinterpret_cast<uintptr_t>(v);
+        if (va % S)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (ranges_meet(va, vbytes, ya, ybytes))
+            return SOFTMAX_ERR_ALIAS;
+    }
+    // the statistics are written: they may overlap nothing else
+    const float *stats[2] = {kind == kNormLayer ? mean : nullptr, rstd};
+    for (int i = 0; i < 2; i++) {
+        if (!stats[i])
+            continue;
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(stats[i]);
+        const uint64_t sb = (uint64_t)rows * 4u;
+        if (sa % 4 || (uint64_t)rows > UINT64_MAX / 4u)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (ranges_meet(sa, sb, xa, ybytes) || ranges_meet(sa, sb, ya, ybytes) ||
+            (gamma && ranges_meet(sa, sb, reinterpret_cast<uintptr_t>(gamma), vbytes)) ||
+            (beta && kind == kNormLayer && ranges_meet(sa, sb, reinterpret_cast<uintptr_t>(beta), vbytes)))
+            return SOFTMAX_ERR_ALIAS;
+        if (i == 1 && stats[0] && ranges_meet(sa, sb, reinterpret_cast<uintptr_t>(stats[0]), sb))
+            return SOFTMAX_ERR_ALIAS;
+    }
+    return SOFTMAX_OK;
+}
+
+// Lanes per row while a row fits 32 lanes x 4 chunks (V = 1..4, V = 3 included
+// so that rows of 24 or 48 chunks -- 192 / 384 fp16 features -- fill every
+// slot), else one CTA per row of up to 1024 threads x 4 chunks.  Sized by the
+// row's whole 16-byte chunks; partial edges go element by element.
+int plan_norm(const softmax_device_info &dev, int kind, const void *x, const void *y, int64_t rows, int64_t cols,
+              int dtype, const void *gamma, const void *beta, int variant, softmax_launch_plan *plan, int *mode)
+{
+    (void)dev;
+    const Geometry g = geometry(x, y, cols, dtype);
+    softmax_launch_plan p = {};
+    p.grid_y = 1;
+    p.cluster_x = 1;
+    p.aligned = g.aligned;
+    p.y_vector = g.y_vec;
+    bool vec_ok = g.aligned;
+    for (const void *v : {gamma, kind == kNormLayer ? beta : nullptr})
+        if (v && reinterpret_cast<uintptr_t>(v) % 16)
+            vec_ok = false;
+    *mode = vec_ok ? kNormFast : (g.y_vec ? kNormSame : kNormOther);
+    const int64_t n = g.nint > 1 ? g.nint : 1;
+    const bool rg_fits = n <= 32 * kNormMaxV;
+    const bool blk_fits = n <= 1024 * kNormMaxV;
+    int v = variant;
+    if (v == SOFTMAX_VARIANT_AUTO)
+        v = rg_fits ? SOFTMAX_VARIANT_ROWGROUP : SOFTMAX_VARIANT_BLOCK;
+    if (v == SOFTMAX_VARIANT_ROWGROUP) {
+        if (!rg_fits)
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        int64_t G, V;
+        if (n <= 4) {
+            G = next_pow2(n);
+            V = 1;
+        } else {
+            G = next_pow2(ceil_div(n, kNormMaxV));
+            if (G < 2)
+                G = 2;
+            if (G > 32)
+                G = 32;
+            V = ceil_div(n, G);
+        }
+        p.variant = v;
+        p.lanes_per_row = (int)G;
+        p.chunks_per_thread = (int)V;
+        p.block_threads = kRowgroupThreads;
+        const int64_t ctas = ceil_div(rows, kRowgroupThreads / G);
+        p.grid_x = ctas < INT32_MAX ? ctas : INT32_MAX;
+    } else if (v == SOFTMAX_VARIANT_BLOCK) {
+        if (!blk_fits)
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        const int V = ceil_div(n, 4) >= 64 ? 4 : 2;
+        int64_t threads = ceil_div(ceil_div(n, V), 32) * 32;
+        p.variant = v;
+        p.chunks_per_thread = V;
+        p.block_threads = (int)threads;
+        p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
+    } else {
+        return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+    }
+    *plan = p;
+    return SOFTMAX_OK;
+}
+
 // ---------------------------------------------------------------- backward
 
 namespace {

@@ -26,6 +26,18 @@ Workloads (rows x cols, dtype, distribution):
 * splitk_fp32_4x4194304 fp32, N(0, 1), then each entry independently with
                         probability 5% replaced by U[50, 100]; seed 5.
 * splitk_fp16_4x4194304 fp16, as above; seed 6.
+
+Normalisation workloads (NORM_WORKLOADS; LayerNorm / RMSNorm of each row):
+
+* ln_fp16_131040x192    fp16, row r drawn N(mu_r, s_r^2) with mu_r ~ U[-2, 2] and
+                        s_r ~ U[0.5, 4] per row (activations whose level and
+                        spread vary by token); seed 7.  LayerNorm without gain
+                        or bias: the [1, 131040, 192] shape of the
+                        Pangu-Weather profile, section 3.
+* ln_fp16_32760x384     fp16, as above; seed 8.  Its [1, 32760, 384] shape.
+* rms_bf16_16384x4096   bf16, as above; seed 9.  RMSNorm with a gain vector
+                        drawn N(1, 0.1^2) (seed 109): a transformer-sized
+                        hidden dimension (not a shape from the pages).
 """
 from __future__ import annotations
 
@@ -80,6 +92,34 @@ WORKLOADS = {w.name: w for w in [
 ]}
 
 
+@dataclass(frozen=True)
+class NormWorkload(Workload):
+    kind: int = 0        # 0 LayerNorm, 1 RMSNorm
+    affine: bool = False  # gain (and, for LayerNorm, bias) vectors
+    eps: float = 1e-5
+
+
+NORM_WORKLOADS = {w.name: w for w in [
+    NormWorkload("ln_fp16_131040x192", 131040, 192, "fp16", "resid", 7,
+                 "LayerNorm fp16 [131040, 192] (no gain / bias), rows N(U[-2, 2], U[0.5, 4]^2)", 0, False, 1e-5),
+    NormWorkload("ln_fp16_32760x384", 32760, 384, "fp16", "resid", 8,
+                 "LayerNorm fp16 [32760, 384] (no gain / bias), rows N(U[-2, 2], U[0.5, 4]^2)", 0, False, 1e-5),
+    NormWorkload("rms_bf16_16384x4096", 16384, 4096, "bf16", "resid", 9,
+                 "RMSNorm bf16 [16384, 4096] with gain N(1, 0.1^2), rows N(U[-2, 2], U[0.5, 4]^2)", 1, True, 1e-6),
+]}
+
+
+def norm_params(w: NormWorkload):
+    """(gain, bias) vectors of a normalisation workload in storage dtype, or
+    None where it has none."""
+    if not w.affine:
+        return None, None
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed + 100])))
+    g = _round_to(rng.normal(1.0, 0.1, w.cols), w.dtype)
+    b = _round_to(rng.normal(0.0, 0.1, w.cols), w.dtype) if w.kind == 0 else None
+    return g, b
+
+
 def rows_per_block(cols: int) -> int:
     return max(1, BLOCK_ELEMS // max(1, cols))
 
@@ -101,6 +141,10 @@ def _draw_block(dist: str, rng: np.random.Generator, nrows: int, cols: int) -> n
         peak = rng.integers(0, cols, size=nrows)
         v[np.arange(nrows), peak] = 30.0
         return v
+    if dist == "resid":
+        mu = rng.uniform(-2.0, 2.0, (nrows, 1))
+        sd = rng.uniform(0.5, 4.0, (nrows, 1))
+        return mu + sd * rng.standard_normal(n).reshape(nrows, cols)
     if dist == "splitk":
         v = rng.standard_normal(n)
         hit = rng.random(n) < 0.05
@@ -130,7 +174,7 @@ def generate(w: Workload | str, rows: int | None = None, threads: int | None = N
     """The first `rows` rows (default: all) of workload `w`, in storage dtype
     (numpy float32 / float16; bf16 as uint16 bit patterns)."""
     if isinstance(w, str):
-        w = WORKLOADS[w]
+        w = WORKLOADS[w] if w in WORKLOADS else NORM_WORKLOADS[w]
     rows = w.rows if rows is None else rows
     out = np.empty((rows, w.cols), dtype=storage_dtype(w.dtype))
     rpb = rows_per_block(w.cols)

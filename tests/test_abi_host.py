@@ -28,14 +28,15 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return set(re.findall(r"\b(softmax_\w+)\s*\(", text))
+    return set(re.findall(r"\b((?:softmax|layernorm|rmsnorm|norm)_\w+)\s*\(", text))
 
 
 def exported_symbols(path):
     import subprocess
 
     out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
-    return {line.split()[-1] for line in out.splitlines() if " T " in line and line.split()[-1].startswith("softmax_")}
+    prefixes = ("softmax_", "layernorm_", "rmsnorm_", "norm_")
+    return {line.split()[-1] for line in out.splitlines() if " T " in line and line.split()[-1].startswith(prefixes)}
 
 
 def test_exports_match_header(lib):
@@ -208,3 +209,28 @@ def test_plan_struct_layout():
     assert ctypes.sizeof(B.LaunchPlan) == 56
     assert B.LaunchPlan.grid_x.offset == 24 and B.LaunchPlan.cluster_x.offset == 40
     assert ctypes.sizeof(B.DeviceInfo) == 24
+
+
+def test_norm_argument_validation(lib):
+    # argument checks run before any device query, so they work without a GPU
+    x, y = BASE, BASE + (1 << 30)
+    g = BASE + (1 << 31)
+    m, r = BASE + (1 << 32), BASE + (1 << 32) + 4096
+    f = B.norm_fwd_variant
+    assert f(2, x, y, 8, 64, 0, 0, 0, 1e-5, 0, 0, 0, 0) == B.ERR_INVALID_ARG          # bad kind
+    assert f(0, x, y, 8, 64, 0, 0, 0, -1e-5, 0, 0, 0, 0) == B.ERR_INVALID_ARG         # eps < 0
+    assert f(0, x, y, 8, 64, 0, 0, 0, float("inf"), 0, 0, 0, 0) == B.ERR_INVALID_ARG  # eps not finite
+    assert f(0, x, y, 8, 64, 0, g + 2, 0, 1e-5, 0, 0, 0, 0) == B.ERR_INVALID_ARG      # gain misaligned
+    assert f(0, x, y, 8, 64, 1, g + 1, 0, 1e-5, 0, 0, 0, 0) == B.ERR_INVALID_ARG
+    assert f(0, x, y, 8, 64, 0, y + 64, 0, 1e-5, 0, 0, 0, 0) == B.ERR_ALIAS           # gain inside y
+    assert f(0, x, y, 8, 64, 0, 0, y, 1e-5, 0, 0, 0, 0) == B.ERR_ALIAS                # bias inside y
+    assert f(1, x, y, 8, 64, 0, 0, y, 1e-5, 0, 0, 0, 0) != B.ERR_ALIAS                # RMSNorm ignores the bias
+    assert f(0, x, y, 8, 64, 0, 0, 0, 1e-5, m + 2, 0, 0, 0) == B.ERR_INVALID_ARG      # mean misaligned
+    assert f(0, x, y, 8, 64, 0, 0, 0, 1e-5, y + 16, 0, 0, 0) == B.ERR_ALIAS           # mean inside y
+    assert f(0, x, y, 8, 64, 0, 0, 0, 1e-5, x, 0, 0, 0) == B.ERR_ALIAS                # mean inside x
+    assert f(0, x, y, 8, 64, 0, 0, 0, 1e-5, m, m + 16, 0, 0) == B.ERR_ALIAS           # mean and rstd overlap
+    assert f(0, x, y, 8, 64, 0, g, 0, 1e-5, 0, g + 8, 0, 0) == B.ERR_ALIAS            # rstd inside the gain
+    assert f(0, x, x + 4, 8, 64, 0, 0, 0, 1e-5, 0, 0, 0, 0) == B.ERR_ALIAS            # partial x / y overlap
+    assert f(0, x, y, 0, 64, 0, 0, 0, 1e-5, 0, 0, 0, 0) == B.OK                       # empty: no launch
+    assert B.layernorm_fwd(x, y, 8, 64, 7, 0, 0, 1e-5, 0, 0, 0) == B.ERR_UNSUPPORTED_DTYPE
+    assert B.rmsnorm_fwd(x, y, 8, 64, 0, g + 2, 1e-5, 0, 0) == B.ERR_INVALID_ARG
