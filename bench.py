@@ -217,25 +217,46 @@ def recorded_traffic(workload: str, variant: str, plan: dict) -> tuple[float | N
 # ----------------------------------------------------------------------------- CPU oracle timing
 
 
-def time_oracle(w, sample_rows: int, reps: int, budget_s: float) -> dict:
-    """The oracle (fp64, OpenMP over rows) on the first sample_rows rows."""
+def oracle_pass(w, op: str, rows: int):
+    """(one oracle pass of `op` over the first `rows` rows of w, bytes it
+    stands for, oracle).  Inputs are prepared outside the pass."""
+    import numpy as np
+
     import oracle
     from online_softmax_dispatcher_gb300 import workloads as W
 
-    x = W.generate(w, rows=sample_rows)
     o = oracle.default()
-    o.softmax(x[: min(2, sample_rows)], w.dtype_code)  # warm
+    x = W.generate(w, rows=rows)
+    dt = w.dtype_code
+    nbytes = w.bytes_moved(rows)
+    if op == "backward":
+        y = o.softmax(x, dt)
+        dy = np.random.default_rng(0).standard_normal(y.shape)
+        return (lambda: o.softmax_bwd_f64(y, dy)), nbytes // 2 * 3, o
+    if op == "masked":
+        return (lambda: o.softmax_masked(x, dt, 0.125, None, min(512, w.rows))), nbytes, o
+    if op == "norm":
+        g, b = W.norm_params(w)
+        return (lambda: o.norm_f64(w.kind, x, dt, g, b, w.eps)), nbytes, o
+    return (lambda: o.softmax(x, dt)), nbytes, o
+
+
+def time_oracle(w, op: str, sample_rows: int, reps: int, budget_s: float) -> dict:
+    """The oracle (fp64, OpenMP over rows) on the first sample_rows rows."""
+    one, nbytes, o = oracle_pass(w, op, sample_rows)
+    one()  # warm
     times = []
     t_all = time.perf_counter()
     for _ in range(reps):
         t = time.perf_counter()
-        o.softmax(x, w.dtype_code)
+        one()
         times.append(time.perf_counter() - t)
         if time.perf_counter() - t_all > budget_s:
             break
     per = statistics.median(times)
-    return {"value": w.bytes_moved(sample_rows) / per / 1e9, "unit": "GB/s", "cores": o.num_threads(),
-            "kind": "oracle", "sample": f"first {sample_rows} of {w.rows} rows, median of {len(times)} passes",
+    return {"value": nbytes / per / 1e9, "unit": "GB/s", "cores": o.num_threads(),
+            "kind": "oracle", "sample": f"{op} on the first {sample_rows} of {w.rows} rows, "
+                                        f"median of {len(times)} passes",
             "seconds_per_pass": per, "passes": len(times)}
 
 
@@ -246,13 +267,28 @@ def oracle_sample_rows(w, target_elems: int = 1 << 25) -> int:
 # ----------------------------------------------------------------------------- GPU arm
 
 
+def find_workload(W, args):
+    """The workload named by --workload (softmax or normalisation workloads);
+    --op norm defaults to the first normalisation workload."""
+    name = args.workload
+    if args.op == "norm":
+        if name == DEFAULT_WORKLOAD:
+            name = next(iter(W.NORM_WORKLOADS))
+        if name not in W.NORM_WORKLOADS:
+            raise SystemExit(f"--op norm needs one of {list(W.NORM_WORKLOADS)}")
+        return W.NORM_WORKLOADS[name]
+    if name not in W.WORKLOADS:
+        raise SystemExit(f"unknown workload {name}; softmax workloads: {list(W.WORKLOADS)}")
+    return W.WORKLOADS[name]
+
+
 def run_ours(args, rank: int, ws: int) -> dict | None:
     import torch
 
     import online_softmax_dispatcher_gb300 as osd
     from online_softmax_dispatcher_gb300 import workloads as W
 
-    w = W.WORKLOADS[args.workload]
+    w = find_workload(W, args)
     if args.rows is not None:
         w = dataclasses.replace(w, rows=min(args.rows, w.rows))
     dev = torch.device("cuda")
@@ -270,7 +306,38 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     rows, cols, dt = w.rows, w.cols, w.dtype_code
     ptrs = [(a.data_ptr(), b.data_ptr()) for a, b in zip(xs, ys)]
     fwd = osd.lib().softmax_fwd
-    if args.op == "backward":
+    # the same step through the public Python API, for the e2e figure:
+    # (host inputs copied in each step, api(device inputs, device output))
+    api_inputs = [x_host]
+
+    def api(dev_in, out):
+        osd.softmax(dev_in[0], out=out)
+
+    if args.op == "norm":
+        g_np, b_np = W.norm_params(w)
+        gt = W.as_torch(g_np, w.dtype).to(dev) if g_np is not None else None
+        bt = W.as_torch(b_np, w.dtype).to(dev) if b_np is not None else None
+        gp = gt.data_ptr() if gt is not None else 0
+        bp = bt.data_ptr() if bt is not None else 0
+        variant = "layernorm" if w.kind == 0 else "rmsnorm"
+        plan = osd.LaunchPlan()
+        ln, rms = osd.lib().layernorm_fwd, osd.lib().rmsnorm_fwd
+
+        def step(i):
+            xp, yp = ptrs[i % nbuf]
+            if w.kind == 0:
+                rc = ln(xp, yp, rows, cols, dt, gp or None, bp or None, w.eps, None, None, s)
+            else:
+                rc = rms(xp, yp, rows, cols, dt, gp or None, w.eps, None, s)
+            if rc != 0:
+                raise osd.SoftmaxError(rc)
+
+        def api(dev_in, out):
+            if w.kind == 0:
+                osd.layer_norm(dev_in[0], gt, bt, eps=w.eps, out=out)
+            else:
+                osd.rms_norm(dev_in[0], gt, eps=w.eps, out=out)
+    elif args.op == "backward":
         # y = softmax(x) (our forward), dy ~ N(0, 1); each step writes dx
         for a, b in zip(xs, ys):
             osd.softmax(a, out=b)
@@ -281,6 +348,10 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         bwd = osd.lib().softmax_bwd
         variant = "backward"
         plan = osd.LaunchPlan()
+        api_inputs = [ys[0].cpu().pin_memory(), dys[0].cpu().pin_memory()]
+
+        def api(dev_in, out):
+            osd.softmax_backward(dev_in[0], dev_in[1], out=out)
 
         def step(i):
             yp, dyp, dxp = ptrs3[i % nbuf]
@@ -293,6 +364,10 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         variant = "masked"
         plan = osd.LaunchPlan()
 
+        def api(dev_in, out):
+            osd.softmax_masked(dev_in[0].view(-1, causal_q, cols), scale=0.125, causal=True,
+                               out=out.view(-1, causal_q, cols))
+
         def step(i):
             xp, yp = ptrs[i % nbuf]
             rc = masked(xp, yp, rows, cols, dt, 0.125, None, 0, causal_q, s)
@@ -303,11 +378,14 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         if rc != 0:
             raise osd.SoftmaxError(rc)
         wss = [torch.empty(max(need, 16), dtype=torch.uint8, device=dev) for _ in range(nbuf)]
-        wptrs = [(a, b, w.data_ptr()) for (a, b), w in zip(ptrs, wss)]
+        wptrs = [(a, b, t.data_ptr()) for (a, b), t in zip(ptrs, wss)]
         fwd_ws = osd.lib().softmax_fwd_ws
         if need:
             variant = "splitk_wide"
             plan = osd.plan_for(xs[0], ys[0], "splitk_wide")
+
+        def api(dev_in, out):
+            osd.softmax(dev_in[0], out=out, workspace=wss[0])
 
         def step(i):
             xp, yp, wp = wptrs[i % nbuf]
@@ -356,21 +434,27 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         lat.append(a.elapsed_time(b) * 1e3)
     latency_us = statistics.median(lat)
 
-    # ---- e2e through the public API: pinned host x -> device, softmax, device -> pinned host y
+    # ---- e2e through the public API: pinned host inputs -> device, the op,
+    # device -> pinned host output, every step
     y_host = torch.empty_like(x_host).pin_memory()
+    dev_in = [t.to(dev) for t in api_inputs]
+    out_dev = torch.empty_like(xs[0])
     ke = max(3, min(args.steps, 30))
+
+    def e2e_step():
+        for d, h in zip(dev_in, api_inputs):
+            d.copy_(h, non_blocking=True)
+        api(dev_in, out_dev)
+        y_host.copy_(out_dev, non_blocking=True)
+
     for _ in range(2):
-        xs[0].copy_(x_host, non_blocking=True)
-        osd.softmax(xs[0], out=ys[0])
-        y_host.copy_(ys[0], non_blocking=True)
+        e2e_step()
     torch.cuda.synchronize()
     barrier(ws)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(ke):
-        xs[0].copy_(x_host, non_blocking=True)
-        osd.softmax(xs[0], out=ys[0])
-        y_host.copy_(ys[0], non_blocking=True)
+        e2e_step()
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b) / ke, ws)
@@ -386,7 +470,9 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "about": w.about, "op": args.op,
-                   "entry": "softmax_fwd_ws" if args.workspace else "softmax_fwd",
+                   "entry": {"norm": "layernorm_fwd" if getattr(w, "kind", 0) == 0 else "rmsnorm_fwd",
+                             "backward": "softmax_bwd", "masked": "softmax_fwd_masked"}.get(
+                                 args.op, "softmax_fwd_ws" if args.workspace else "softmax_fwd"),
                    "variant": variant, "plan": plan.as_dict(),
                    "l2": f"rotating {nbuf} buffer sets, {nbuf * set_bytes / 2**20:.0f} MiB > 2x L2 "
                          f"({l2 / 2**20:.0f} MiB)",
@@ -399,13 +485,13 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
                      "algorithmic_bytes_per_launch": set_bytes,
                      "traffic": traffic, "traffic_source": tsrc},
         "e2e": {"value": round(set_bytes / (e2e_ms / 1e3) / 1e9 * ws, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in api_inputs),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size(), "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": args.steps * (2 if variant == "splitk_wide" else 1),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = time_oracle(w, oracle_sample_rows(w), reps=5, budget_s=20.0)
+        res["cpu_baseline"] = time_oracle(w, args.op, oracle_sample_rows(w), reps=5, budget_s=20.0)
     return res if rank == 0 else None
 
 
@@ -414,25 +500,22 @@ def run_reference(args, rank: int, ws: int) -> dict | None:
         return None
     from online_softmax_dispatcher_gb300 import workloads as W
 
-    w = W.WORKLOADS[args.workload]
+    w = find_workload(W, args)
     rows = oracle_sample_rows(w, target_elems=1 << 23)
-    import oracle
-
-    x = W.generate(w, rows=rows)
-    o = oracle.default()
+    one, nbytes, o = oracle_pass(w, args.op, rows)
     for _ in range(max(0, min(args.warmup, 3))):
-        o.softmax(x, w.dtype_code)
+        one()
     t = time.perf_counter()
     for _ in range(args.steps):
-        o.softmax(x, w.dtype_code)
+        one()
     dt_s = (time.perf_counter() - t) / max(1, args.steps)
-    value = w.bytes_moved(rows) / dt_s / 1e9
-    sample = f"each step: first {rows} of {w.rows} rows of {w.name}"
+    value = nbytes / dt_s / 1e9
+    sample = f"each step: {args.op} on the first {rows} of {w.rows} rows of {w.name}"
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt_s * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "about": w.about,
+        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "about": w.about, "op": args.op,
                    "reference": "fp64 CPU oracle (OpenMP over rows) standing in for the pages' method"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
                          "sample": sample},
@@ -449,10 +532,12 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--rows", type=int, default=None,
                     help="time only the first ROWS rows of the workload (for small profiling captures)")
-    ap.add_argument("--op", choices=("forward", "backward", "masked"), default="forward",
+    ap.add_argument("--op", choices=("forward", "backward", "masked", "norm"), default="forward",
                     help="backward times softmax_bwd (dx = y*(dy - sum dy*y)) on the workload's shape, "
                          "bytes = rows*cols*(2 reads + 1 write); masked times softmax_fwd_masked with scale 1/8 "
-                         "and a causal cut over query blocks of 512 rows (attention scores [B, H, 512, cols])")
+                         "and a causal cut over query blocks of 512 rows (attention scores [B, H, 512, cols]); "
+                         "norm times layernorm_fwd / rmsnorm_fwd on a normalisation workload "
+                         "(ln_fp16_131040x192, ln_fp16_32760x384, rms_bf16_16384x4096)")
     ap.add_argument("--workspace", action="store_true",
                     help="forward through softmax_fwd_ws with a workspace the bench allocates (lets few, very "
                          "long rows use every SM)")

@@ -255,7 +255,8 @@ int softmax_fwd_noalloc(const void *x, void *y, int64_t rows, int64_t cols, int 
  *           rstd must be 4-byte aligned and overlap nothing else.
  * The row is held in registers between its reductions (one HBM read of x, one
  * write of y); mu and var are accumulated in fp32 (compensated for fp32
- * input) and var is taken about mu, from the registers.  Accuracy against the
+ * input) and var is taken about mu, from the registers; rstd is the SFU's
+ * reciprocal square root (about 2 ulp of fp32).  Accuracy against the
  * exact result y*:
  *     |y - y*| <= u(y*) + 64 * 2^-24 * (|gamma_j| * (|z_j| + a * rstd) + |beta_j|)
  * with z_j = (x_j - mu) * rstd, a = (1/n) sum_j |x_j| and u = 1 ulp of the

@@ -14,10 +14,13 @@
 // the 16-byte grid.
 //
 // Per row: mu = (1/n) sum x (LayerNorm only), then var = (1/n) sum (x - mu)^2
-// from the registers (two passes over the cached row, none over HBM), rstd =
-// 1 / sqrt(var + eps) with IEEE sqrt and division, y = (x - mu) * rstd * g + b
-// with the last two as one FMA, rounded to nearest even.  Sums are fp32,
-// compensated (TwoSum) for fp32 input.
+// from the registers (two passes over the cached row, none over HBM),
+// rstd = rsqrt(var + eps) on the SFU (about 2 ulp of fp32), and
+// y = (x * rstd - mu * rstd) * g + b as two FMAs (the rounding of mu * rstd
+// shifts every output of the row alike, by at most 2^-24 |mu| rstd), rounded
+// to nearest even.  Sums are fp32, compensated (TwoSum) for fp32 input.  The
+// lanes-per-row kernel keeps the row as floats after one unpack; the
+// CTA-per-row kernel keeps it packed and unpacks per pass.
 #pragma once
 
 #include "common.cuh"
@@ -80,11 +83,31 @@ struct CtaSum {
     }
 };
 
+// The row's chunk i as floats: from the floats kept after the first unpack
+// (KEEP) or unpacked again from the packed chunk.
+template <int DT, int V, bool KEEP>
+struct RowCache {
+    static constexpr int E = Fmt<DT>::kPerChunk;
+    uint4 raw[V];
+    float f[KEEP ? V : 1][KEEP ? E : 1];
+    __device__ __forceinline__ void get(int i, float (&out)[E]) const
+    {
+        if constexpr (KEEP) {
+#pragma unroll
+            for (int e = 0; e < E; e++)
+                out[e] = f[i][e];
+        } else {
+            unpack<DT>(raw[i], out);
+        }
+    }
+};
+
 // One row for a team of L threads (lane = this thread's index in the team).
 // NE edge elements per thread; `valid` false for a lane group past the last
 // row (it still takes part in the team's reductions).
-template <int DT, int KIND, int V, int MODE, int NE, class Red>
-__device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool valid, int lane, int L, Red red)
+template <int DT, int KIND, int V, int MODE, int NE, bool KEEP, class Red>
+__device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool valid, int lane, int L, float inv_n,
+                                         Red red)
 {
     using M = Math<DT>;
     using Acc = typename M::Acc;
@@ -92,13 +115,26 @@ __device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool vali
     constexpr int PH = MODE == kNormFast ? kPhAligned : (MODE == kNormSame ? kPhSame : kPhOther);
     const ShortRow g = short_row<DT, MODE == kNormFast>(a.x, a.y, valid ? r : 0, a.cols);
 
-    uint4 raw[V];
-    bool ok[V];
+    RowCache<DT, V, KEEP> c;
+    // interior chunk lane + i * L of this row exists
+    // which interior chunks lane + i * L exist, decided once before the loads
+    // (measured: deciding it again in each pass slows the CTA-per-row kernel
+    // by a quarter)
+    const int span = valid ? g.span : 0;
+    unsigned okm = 0;  // bit i: chunk lane + i * L exists
+#pragma unroll
+    for (int i = 0; i < V; i++)
+        okm |= (unsigned)(lane + i * L < span) << i;
+    const auto has = [okm](int i) { return ((okm >> i) & 1u) != 0; };
 #pragma unroll
     for (int i = 0; i < V; i++) {
         const int q = lane + i * L;
-        ok[i] = valid && q < g.span;
-        raw[i] = ok[i] ? ld_chunk(g.x0 + ((int64_t)(g.kf + q) << 4)) : make_uint4(0, 0, 0, 0);
+        c.raw[i] = has(i) ? ld_chunk(g.x0 + ((int64_t)(g.kf + q) << 4)) : make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (KEEP) {
+#pragma unroll
+        for (int i = 0; i < V; i++)
+            unpack<DT>(c.raw[i], c.f[i]);
     }
     int je[NE > 0 ? NE : 1];
     float xe[NE > 0 ? NE : 1];
@@ -108,7 +144,6 @@ __device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool vali
         je[u] = (valid && p < g.ne) ? edge_col(g, p) : -1;
         xe[u] = je[u] >= 0 ? ld_elem<DT>(g.xr, je[u]) : 0.f;
     }
-    const float inv_n = 1.0f / (float)a.cols;
 
     // mean (LayerNorm): slots past the row hold +0 and add nothing
     float mu = 0.f;
@@ -117,7 +152,7 @@ __device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool vali
 #pragma unroll
         for (int i = 0; i < V; i++) {
             float f[E];
-            unpack<DT>(raw[i], f);
+            c.get(i, f);
 #pragma unroll
             for (int e = 0; e < E; e++)
                 M::add(s, f[e]);
@@ -132,9 +167,9 @@ __device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool vali
     Acc q2 = M::zero();
 #pragma unroll
     for (int i = 0; i < V; i++) {
-        if (ok[i]) {
+        if (has(i)) {
             float f[E];
-            unpack<DT>(raw[i], f);
+            c.get(i, f);
 #pragma unroll
             for (int e = 0; e < E; e++) {
                 const float d = f[e] - mu;
@@ -150,7 +185,8 @@ __device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool vali
         }
     }
     const float var = M::value(red(q2)) * inv_n;
-    const float rs = 1.0f / sqrtf(var + a.eps);
+    const float rs = rsqrtf(var + a.eps);
+    const float nmr = -mu * rs;  // y = x * rs + nmr, before the gain and bias
     if (valid && lane == 0) {
         if (KIND == kNormLayer && a.mean)
             a.mean[r] = mu;
@@ -163,20 +199,24 @@ __device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool vali
         return;
 #pragma unroll
     for (int i = 0; i < V; i++) {
-        if (ok[i]) {
+        if (has(i)) {
             const int q = lane + i * L;
             float f[E], gv[E], bv[E];
-            unpack<DT>(raw[i], f);
+            c.get(i, f);
             if (a.gamma)
                 vec_chunk<DT, MODE>(a.gamma, g, q, gv);
             if (KIND == kNormLayer && a.beta)
                 vec_chunk<DT, MODE>(a.beta, g, q, bv);
 #pragma unroll
             for (int e = 0; e < E; e++) {
-                float z = (f[e] - mu) * rs;
-                const float gg = a.gamma ? gv[e] : 1.0f;
-                const float bb = (KIND == kNormLayer && a.beta) ? bv[e] : 0.0f;
-                f[e] = fmaf(z, gg, bb);
+                const float z = fmaf(f[e], rs, nmr);
+                if (a.gamma || (KIND == kNormLayer && a.beta)) {
+                    const float gg = a.gamma ? gv[e] : 1.0f;
+                    const float bb = (KIND == kNormLayer && a.beta) ? bv[e] : 0.0f;
+                    f[e] = fmaf(z, gg, bb);
+                } else {
+                    f[e] = z;
+                }
             }
             store_interior<DT, PH>(g, q, pack<DT>(f));
         }
@@ -184,7 +224,7 @@ __device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool vali
 #pragma unroll
     for (int u = 0; u < NE; u++) {
         if (je[u] >= 0) {
-            const float z = (xe[u] - mu) * rs;
+            const float z = fmaf(xe[u], rs, nmr);
             const float gg = a.gamma ? ld_elem<DT>(a.gamma, je[u]) : 1.0f;
             const float bb = (KIND == kNormLayer && a.beta) ? ld_elem<DT>(a.beta, je[u]) : 0.0f;
             st_elem<DT>(g.yr, je[u], fmaf(z, gg, bb));
@@ -201,11 +241,12 @@ __global__ void __launch_bounds__(kRowgroupThreads) k_norm_rowgroup(const NormAr
     const int groups = blockDim.x / G;
     const int gl = threadIdx.x & (G - 1);
     const int64_t stride = (int64_t)gridDim.x * groups;
+    const float inv_n = 1.0f / (float)a.cols;
     // every thread of a CTA runs the same number of iterations, so the
     // butterflies see converged warps
     for (int64_t base = (int64_t)blockIdx.x * groups; base < a.rows; base += stride) {
         const int64_t r = base + threadIdx.x / G;
-        norm_row<DT, KIND, V, MODE, NE>(a, r, r < a.rows, gl, G, GroupSum<DT, G>{});
+        norm_row<DT, KIND, V, MODE, NE, true>(a, r, r < a.rows, gl, G, inv_n, GroupSum<DT, G>{});
     }
 }
 
@@ -216,8 +257,9 @@ __global__ void __launch_bounds__(1024) k_norm_block(const NormArgs a)
     pdl_enter();
     __shared__ typename Math<DT>::Acc slots[32];
     constexpr int NE = MODE == kNormFast ? 0 : 1;  // >= 32 threads: one edge element each at most
+    const float inv_n = 1.0f / (float)a.cols;
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
-        norm_row<DT, KIND, V, MODE, NE>(a, r, true, threadIdx.x, blockDim.x, CtaSum<DT>{slots});
+        norm_row<DT, KIND, V, MODE, NE, false>(a, r, true, threadIdx.x, blockDim.x, inv_n, CtaSum<DT>{slots});
 }
 
 namespace norm_detail {
