@@ -189,7 +189,7 @@ def kernel_fingerprint(variant: str) -> str:
     """Hash of the sources the dominant kernel is built from (invalidates stale ncu traffic)."""
     csrc = os.path.join(ROOT, "online_softmax_dispatcher_gb300", "csrc")
     files = {"rowgroup": "k_rowgroup.cuh", "block": "k_block.cu", "block_tma": "k_tma.cu",
-             "stream": "k_stream.cu", "splitk": "k_splitk.cu"}
+             "stream": "k_stream.cu", "splitk": "k_splitk.cu", "layernorm": "k_norm.cuh", "rmsnorm": "k_norm.cuh"}
     h = hashlib.sha256()
     for name in (files.get(variant, ""), "common.cuh", "tma.cuh", "launch.h"):
         p = os.path.join(csrc, name)
