@@ -6,14 +6,18 @@
 //
 // * ROWGROUP: G lanes per row, V 16-byte chunks of y and of dy per lane held in
 //   registers, one HBM read of each and one HBM write of dx per element.
-// * BLOCK: one CTA per row, V <= 4 chunks of each per thread in registers.
+// * BLOCK: one CTA per row, V <= 8 chunks of each per thread in registers
+//   (rows of up to 512 threads x 8 chunks = 64 KiB), the chunk-to-thread map
+//   shifted per row so that warp accesses start on 128-byte lines.
 // * STREAM: one CTA per row of any length; a sum pass, then a pass that
 //   re-reads y and dy (from L2 when the rows fit there) and writes dx.
 //
 // s is a compensated (TwoSum) fp32 sum for every dtype: dx_j nearly cancels
 // when dy_j ~ s, and the error of s is what is left of dx_j then.  The chunk
-// grid is y's; dy and dx use vector accesses when their rows share y's 16-byte
-// phase and per-element accesses when they do not.
+// grid is y's.  ROWGROUP and BLOCK split a row into interior chunks (vector
+// accesses of all three tensors when dy and dx share y's 16-byte phase, else
+// element accesses of dy / dx) and at most 2E - 2 edge elements handled one by
+// one outside the unrolled loops; STREAM peels partial edge chunks.
 #include "common.cuh"
 #include "launch.h"
 
@@ -103,84 +107,209 @@ __device__ __forceinline__ CSum group_csum(CSum a)
 
 }  // namespace
 
-template <int DT, int G, int V, bool ALIGNED>
-__global__ void __launch_bounds__(kRowgroupThreads) k_bwd_rowgroup(const BwdArgs a)
+// Row phases for the short-row kernels: all rows of y, dy and dx on the 16-byte
+// grid (kBwdFast); dy and dx on y's phase (kBwdSame); otherwise (kBwdOther:
+// dy read and dx written element by element in the interior).
+constexpr int kBwdFast = 0;
+constexpr int kBwdSame = 1;
+constexpr int kBwdOther = 2;
+
+// Interior chunk q of the dy row (dyr = its start), on y's chunk grid.
+template <int DT, int MODE>
+__device__ __forceinline__ uint4 dy_interior(const ShortRow &g, const char *dyr, int q)
 {
-    pdl_enter();
-    const int groups = blockDim.x / G;
-    const int gl = threadIdx.x & (G - 1);
-    const int64_t stride = (int64_t)gridDim.x * groups;
-    for (int64_t base = (int64_t)blockIdx.x * groups; base < a.rows; base += stride) {
-        const int64_t r = base + threadIdx.x / G;
-        const bool valid = r < a.rows;
-        const int64_t rr = valid ? r : 0;
-        const RowGeom g = row_geom<DT, ALIGNED>(a.y, a.dx, rr, a.cols);
-        const int64_t off = rr * a.cols * Fmt<DT>::kBytes;
-        uint4 yc[V], dc[V];
+    constexpr int E = Fmt<DT>::kPerChunk;
+    constexpr int S = Fmt<DT>::kBytes;
+    if constexpr (MODE != kBwdOther) {
+        return ld_chunk(dyr - g.head * S + ((int64_t)(g.kf + q) << 4));
+    } else {
+        const int j0 = (g.kf + q) * E - g.head;
+        uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < V; i++) {
-            const int64_t k = gl + i * G;
-            yc[i] = valid ? load_chunk<DT, ALIGNED>(g, k, a.cols) : make_uint4(0, 0, 0, 0);
-            dc[i] = valid ? load_other<DT, ALIGNED>(g, a.dy + off, a.dy_vec != 0, k, a.cols) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 4; i++) {
+            if constexpr (S == 4)
+                w[i] = ld_u32(dyr + 4 * (int64_t)(j0 + i));
+            else
+                w[i] = ld_u16(dyr + 2 * (int64_t)(j0 + 2 * i)) | (ld_u16(dyr + 2 * (int64_t)(j0 + 2 * i + 1)) << 16);
         }
-        CSum acc{0.f, 0.f};
-        if (valid) {
-#pragma unroll
-            for (int i = 0; i < V; i++)
-                dot_chunk<DT, ALIGNED>(yc[i], dc[i], g, gl + i * G, a.cols, acc);
-        }
-        acc = group_csum<G>(acc);
-        const float s = acc.s + acc.c;
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            opaque(yc[i]);
-            opaque(dc[i]);
-        }
-        if (valid) {
-#pragma unroll
-            for (int i = 0; i < V; i++) {
-                const int64_t k = gl + i * G;
-                if (k < g.nch)
-                    store_other<DT, ALIGNED>(g, a.dx + off, a.dx_vec != 0, k, a.cols, grad_chunk<DT>(yc[i], dc[i], s));
-            }
-        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
-template <int DT, int V, bool ALIGNED>
-__global__ void __launch_bounds__(512) k_bwd_block(const BwdArgs a)
+// dy * y products of the two 16-bit values in each word: one mixed-precision
+// FMA per product (the product of two 16-bit values is exact in fp32, the
+// added +0 leaves it so), without unpacking either operand.
+template <int DT>
+__device__ __forceinline__ void mul_pair(uint32_t yw, uint32_t dw, float &p0, float &p1)
+{
+    if constexpr (DT == kF16) {
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+            "fma.rn.f32.f16 %0, a0, b0, 0f00000000;\n\tfma.rn.f32.f16 %1, a1, b1, 0f00000000;\n\t}"
+            : "=f"(p0), "=f"(p1)
+            : "r"(yw), "r"(dw));
+    } else {
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, a0, b0, 0f00000000;\n\tfma.rn.f32.bf16 %1, a1, b1, 0f00000000;\n\t}"
+            : "=f"(p0), "=f"(p1)
+            : "r"(yw), "r"(dw));
+    }
+}
+
+// acc += sum of dy * y over the slots of one chunk (compensated additions;
+// products of 16-bit values are exact in fp32 either way).  MIXED: one
+// mixed-precision FMA per product, else unpack both and multiply; measured,
+// the first is faster in the CTA-per-row kernel (unaligned [8192, 5003] fp16:
+// 95 % vs 80 % of HBM bandwidth), the second in the lanes-per-row kernel
+// ([65536, 512] fp16: 97 % vs 91 %).
+template <int DT, bool MIXED>
+__device__ __forceinline__ void dot_add(const uint4 &yc, const uint4 &dc, CSum &acc)
+{
+    constexpr int E = Fmt<DT>::kPerChunk;
+    if constexpr (MIXED && DT != kF32) {
+        const uint32_t yw[4] = {yc.x, yc.y, yc.z, yc.w}, dw[4] = {dc.x, dc.y, dc.z, dc.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float p0, p1;
+            mul_pair<DT>(yw[i], dw[i], p0, p1);
+            Math<kF32>::add(acc, p0);
+            Math<kF32>::add(acc, p1);
+        }
+    } else {
+        float fy[E], fd[E];
+        unpack<DT>(yc, fy);
+        unpack<DT>(dc, fd);
+#pragma unroll
+        for (int e = 0; e < E; e++)
+            Math<kF32>::add(acc, fd[e] * fy[e]);
+    }
+}
+
+// dx = y * (dy - s) for one chunk: dy - s by one mixed-precision FMA per
+// value for 16-bit data (the correctly rounded difference, dy unpacked by the
+// FMA itself; unpacking both tensors here spills registers in the CTA-per-row
+// kernel).
+template <int DT>
+__device__ __forceinline__ uint4 grad_chunk_fast(const uint4 &yc, const uint4 &dc, float s)
+{
+    constexpr int E = Fmt<DT>::kPerChunk;
+    if constexpr (DT == kF32) {
+        return grad_chunk<DT>(yc, dc, s);
+    } else {
+        float fy[E], t[E];
+        unpack<DT>(yc, fy);
+        const uint32_t dw[4] = {dc.x, dc.y, dc.z, dc.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            sub_pair<DT>(dw[i], -s, t[2 * i], t[2 * i + 1]);
+#pragma unroll
+        for (int e = 0; e < E; e++)
+            fy[e] *= t[e];
+        return pack<DT>(fy);
+    }
+}
+
+template <int G>
+struct CsumGroup {
+    __device__ __forceinline__ CSum operator()(CSum a) const { return group_csum<G>(a); }
+};
+
+struct CsumCta {
+    CSum *slots;
+    __device__ __forceinline__ CSum operator()(CSum a) const { return block_sum<kF32>(a, slots); }
+};
+
+// One row for a team of L threads (lane = this thread's index in it); SHIFT
+// (the CTA-per-row kernel) moves the chunk map so that every 8th slot starts a
+// 128-byte line, and takes the products by mixed-precision FMAs.
+template <int DT, int V, int MODE, int NE, bool SHIFT, class Red>
+__device__ __forceinline__ void bwd_row(const BwdArgs &a, int64_t r, bool valid, int lane, int L, Red red)
+{
+    constexpr int S = Fmt<DT>::kBytes;
+    constexpr int PH = MODE == kBwdFast ? kPhAligned : (MODE == kBwdSame ? kPhSame : kPhOther);
+    const int64_t rr = valid ? r : 0;
+    const ShortRow g = short_row<DT, MODE == kBwdFast>(a.y, a.dx, rr, (int)a.cols);
+    const char *dyr = a.dy + rr * a.cols * S;
+    const int span = valid ? g.span : 0;
+    int sh = 0;
+    if constexpr (SHIFT) {
+        sh = (int)(((reinterpret_cast<uintptr_t>(g.x0) >> 4) + g.kf) & 7);
+        if (sh > L * V - span)
+            sh = 0;
+    }
+    const int q0 = lane - sh;
+    unsigned okm = 0;  // bit i: interior chunk q0 + i * L exists
+#pragma unroll
+    for (int i = 0; i < V; i++)
+        okm |= (unsigned)((unsigned)(q0 + i * L) < (unsigned)span) << i;
+    uint4 yc[V], dc[V];
+#pragma unroll
+    for (int i = 0; i < V; i++) {
+        const bool ok = (okm >> i) & 1u;
+        const int q = q0 + i * L;
+        yc[i] = ok ? ld_chunk(g.x0 + ((int64_t)(g.kf + q) << 4)) : make_uint4(0, 0, 0, 0);
+        dc[i] = ok ? dy_interior<DT, MODE>(g, dyr, q) : make_uint4(0, 0, 0, 0);
+    }
+    int je[NE > 0 ? NE : 1];
+    float ye[NE > 0 ? NE : 1], de[NE > 0 ? NE : 1];
+#pragma unroll
+    for (int u = 0; u < NE; u++) {
+        const int p = lane + u * L;
+        je[u] = (valid && p < g.ne) ? edge_col(g, p) : -1;
+        ye[u] = je[u] >= 0 ? ld_elem<DT>(g.xr, je[u]) : 0.f;
+        de[u] = je[u] >= 0 ? ld_elem<DT>(dyr, je[u]) : 0.f;
+    }
+
+    // s = sum dy * y: slots past the row hold +0 on both sides and add 0
+    CSum acc{0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < V; i++)
+        dot_add<DT, SHIFT>(yc[i], dc[i], acc);
+#pragma unroll
+    for (int u = 0; u < NE; u++)
+        Math<kF32>::add(acc, de[u] * ye[u]);
+    acc = red(acc);
+    const float sum = acc.s + acc.c;
+#pragma unroll
+    for (int i = 0; i < V; i++) {
+        opaque(yc[i]);
+        opaque(dc[i]);
+    }
+    if (!valid)
+        return;
+#pragma unroll
+    for (int i = 0; i < V; i++)
+        if ((okm >> i) & 1u)
+            store_interior<DT, PH>(g, q0 + i * L, grad_chunk_fast<DT>(yc[i], dc[i], sum));
+#pragma unroll
+    for (int u = 0; u < NE; u++)
+        if (je[u] >= 0)
+            st_elem<DT>(g.yr, je[u], ye[u] * (de[u] - sum));
+}
+
+template <int DT, int G, int V, int MODE>
+__global__ void __launch_bounds__(kRowgroupThreads) k_bwd_rowgroup(const BwdArgs a)
+{
+    pdl_enter();
+    constexpr int NE = MODE == kBwdFast ? 0 : edge_slots<DT, G>();
+    const int groups = blockDim.x / G;
+    const int gl = threadIdx.x & (G - 1);
+    const int64_t stride = (int64_t)gridDim.x * groups;
+    // every thread of a CTA runs the same number of iterations, so the
+    // butterflies see converged warps
+    for (int64_t base = (int64_t)blockIdx.x * groups; base < a.rows; base += stride) {
+        const int64_t r = base + threadIdx.x / G;
+        bwd_row<DT, V, MODE, NE, false>(a, r, r < a.rows, gl, G, CsumGroup<G>{});
+    }
+}
+
+template <int DT, int V, int MODE>
+__global__ void __launch_bounds__(512, V >= 8 ? 1 : 2) k_bwd_block(const BwdArgs a)
 {
     pdl_enter();
     __shared__ CSum slots[32];
-    const int T = blockDim.x, t = threadIdx.x;
-    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
-        const RowGeom g = row_geom<DT, ALIGNED>(a.y, a.dx, r, a.cols);
-        const int64_t off = r * a.cols * Fmt<DT>::kBytes;
-        uint4 yc[V], dc[V];
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            const int64_t k = t + (int64_t)i * T;
-            yc[i] = load_chunk<DT, ALIGNED>(g, k, a.cols);
-            dc[i] = load_other<DT, ALIGNED>(g, a.dy + off, a.dy_vec != 0, k, a.cols);
-        }
-        CSum acc{0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < V; i++)
-            dot_chunk<DT, ALIGNED>(yc[i], dc[i], g, t + (int64_t)i * T, a.cols, acc);
-        acc = block_sum<kF32>(acc, slots);
-        const float s = acc.s + acc.c;
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            opaque(yc[i]);
-            opaque(dc[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            const int64_t k = t + (int64_t)i * T;
-            if (k < g.nch)
-                store_other<DT, ALIGNED>(g, a.dx + off, a.dx_vec != 0, k, a.cols, grad_chunk<DT>(yc[i], dc[i], s));
-        }
-    }
+    constexpr int NE = MODE == kBwdFast ? 0 : 1;  // >= 32 threads: one edge element each at most
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
+        bwd_row<DT, V, MODE, NE, true>(a, r, true, threadIdx.x, blockDim.x, CsumCta{slots});
 }
 
 template <int DT, bool ALIGNED>
@@ -233,17 +362,31 @@ BwdArgs args_of(const BwdLaunch &l)
     return BwdArgs{(const char *)l.y, (const char *)l.dy, (char *)l.dx, l.rows, l.cols, l.dy_vec, l.dx_vec};
 }
 
-template <int DT, int G, int V, bool A>
+int bwd_mode(const BwdLaunch &l)
+{
+    if (l.plan.aligned)
+        return kBwdFast;
+    return (l.dy_vec && l.dx_vec) ? kBwdSame : kBwdOther;
+}
+
+template <int DT, int G, int V, int MODE>
 int bwd_rowgroup_one(const BwdLaunch &l)
 {
-    return launch_pdl(k_bwd_rowgroup<DT, G, V, A>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
-                      (cudaStream_t)l.stream, no_attr(), args_of(l));
+    return launch_pdl(k_bwd_rowgroup<DT, G, V, MODE>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads),
+                      0, (cudaStream_t)l.stream, no_attr(), args_of(l));
 }
 
 template <int DT, int G, int V>
 int bwd_rowgroup_a(const BwdLaunch &l)
 {
-    return l.plan.aligned ? bwd_rowgroup_one<DT, G, V, true>(l) : bwd_rowgroup_one<DT, G, V, false>(l);
+    switch (bwd_mode(l)) {
+    case kBwdFast:
+        return bwd_rowgroup_one<DT, G, V, kBwdFast>(l);
+    case kBwdSame:
+        return bwd_rowgroup_one<DT, G, V, kBwdSame>(l);
+    default:
+        return bwd_rowgroup_one<DT, G, V, kBwdOther>(l);
+    }
 }
 
 template <int DT, int G>
@@ -282,22 +425,36 @@ int bwd_rowgroup_dt(const BwdLaunch &l)
     }
 }
 
-template <int DT, int V, bool A>
+template <int DT, int V, int MODE>
 int bwd_block_one(const BwdLaunch &l)
 {
-    return launch_pdl(k_bwd_block<DT, V, A>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+    return launch_pdl(k_bwd_block<DT, V, MODE>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
                       (cudaStream_t)l.stream, no_attr(), args_of(l));
+}
+
+template <int DT, int V>
+int bwd_block_mode(const BwdLaunch &l)
+{
+    switch (bwd_mode(l)) {
+    case kBwdFast:
+        return bwd_block_one<DT, V, kBwdFast>(l);
+    case kBwdSame:
+        return bwd_block_one<DT, V, kBwdSame>(l);
+    default:
+        return bwd_block_one<DT, V, kBwdOther>(l);
+    }
 }
 
 template <int DT>
 int bwd_block_dt(const BwdLaunch &l)
 {
-    const bool A = l.plan.aligned != 0;
     switch (l.plan.chunks_per_thread) {
     case 2:
-        return A ? bwd_block_one<DT, 2, true>(l) : bwd_block_one<DT, 2, false>(l);
+        return bwd_block_mode<DT, 2>(l);
     case 4:
-        return A ? bwd_block_one<DT, 4, true>(l) : bwd_block_one<DT, 4, false>(l);
+        return bwd_block_mode<DT, 4>(l);
+    case 8:
+        return bwd_block_mode<DT, 8>(l);
     default:
         return (int)cudaErrorInvalidValue;
     }

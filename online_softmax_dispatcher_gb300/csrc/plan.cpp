@@ -532,8 +532,8 @@ int validate_bwd_args(const void *y, const void *dy, const void *dx, int64_t row
 }
 
 // Backward dispatcher: lanes per row while y and dy fit 4 chunks per lane,
-// one CTA per row up to 2048 chunks (4 of each per thread: more spills
-// registers), then the two-pass streaming kernel.
+// one CTA per row up to 4096 chunks (64 KiB rows: 512 threads x 8 chunks of
+// each), then the two-pass streaming kernel.
 int plan_bwd(const softmax_device_info &dev, const void *y, const void *dy, const void *dx, int64_t rows,
              int64_t cols, int dtype, int variant, softmax_launch_plan *plan, int *dy_vec, int *dx_vec)
 {
@@ -549,18 +549,23 @@ int plan_bwd(const softmax_device_info &dev, const void *y, const void *dy, cons
     p.y_vector = g.y_vec;
     *dy_vec = ((da - ya) % 16) == 0;
     *dx_vec = g.y_vec;
-    const bool rg_fits = nch <= 32 * 4;
-    const bool blk_fits = nch <= 512 * 4;
+    // the lanes-per-row and CTA-per-row kernels hold a row's whole interior
+    // chunks (its partial edges go element by element); the stream kernel
+    // walks all of its chunks
+    const int64_t n = g.nint > 1 ? g.nint : 1;
+    const bool rg_fits = n <= 32 * 4;
+    const bool blk_fits = n <= 512 * 8;
+    (void)nch;
     int v = variant;
     if (v == SOFTMAX_VARIANT_AUTO)
         v = rg_fits ? SOFTMAX_VARIANT_ROWGROUP : (blk_fits ? SOFTMAX_VARIANT_BLOCK : SOFTMAX_VARIANT_STREAM);
     if (v == SOFTMAX_VARIANT_ROWGROUP) {
         if (!rg_fits)
             return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
-        int64_t G = nch <= 4 ? next_pow2(nch) : next_pow2(ceil_div(nch, 4));
+        int64_t G = n <= 4 ? next_pow2(n) : next_pow2(ceil_div(n, 4));
         if (G > 32)
             G = 32;
-        const int64_t V = next_pow2(ceil_div(nch, G));
+        const int64_t V = next_pow2(ceil_div(n, G));
         p.variant = v;
         p.lanes_per_row = (int)G;
         p.chunks_per_thread = (int)V;
@@ -570,8 +575,9 @@ int plan_bwd(const softmax_device_info &dev, const void *y, const void *dy, cons
     } else if (v == SOFTMAX_VARIANT_BLOCK) {
         if (!blk_fits)
             return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
-        const int V = ceil_div(nch, 4) >= 32 ? 4 : 2;
-        int64_t T = ceil_div(ceil_div(nch, V), 32) * 32;
+        // 8 chunks of each tensor per thread only past 512 x 4 (registers)
+        const int V = n > 512 * 4 ? 8 : (ceil_div(n, 4) >= 32 ? 4 : 2);
+        int64_t T = ceil_div(ceil_div(n, V), 32) * 32;
         p.variant = v;
         p.chunks_per_thread = V;
         p.block_threads = (int)T;
