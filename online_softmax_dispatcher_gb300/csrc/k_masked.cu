@@ -18,6 +18,11 @@
 //   registers, the mask chunk re-read through L1 and the logits recomputed in
 //   each of the three passes) up to 2048 chunks (4 per thread x 512 threads;
 //   more spills registers).
+// * A row is its interior 16-byte chunks plus at most 2E - 2 edge elements
+//   taken one by one; per interior chunk the number of visible values is
+//   computed once: chunks wholly past the causal limit are not read, only the
+//   one the limit falls in cuts values one by one.  The mask's presence and
+//   the rows' 16-byte phases are template parameters.
 #include "common.cuh"
 #include "launch.h"
 
@@ -43,9 +48,6 @@ __device__ __forceinline__ int64_t visible_limit(const MaskedArgs &a, int64_t r)
     return a.causal_q > 0 ? r % a.causal_q + (a.cols - a.causal_q) + 1 : a.cols;
 }
 
-// Chunk k (on x's chunk grid for this row) of the mask row `mrow`: vector load
-// when the mask row sits on x's 16-byte phase and the chunk is whole, else
-// element by element.
 // A mask row is typically shared by many rows, so its reads may allocate in L1.
 __device__ __forceinline__ uint4 ld_chunk_cached(const void *p)
 {
@@ -56,59 +58,20 @@ __device__ __forceinline__ uint4 ld_chunk_cached(const void *p)
     return v;
 }
 
-template <int DT, bool ALIGNED>
-__device__ __forceinline__ uint4 load_mask_chunk(const RowGeom &g, const char *mrow, bool same_phase, int64_t k,
-                                                 int64_t cols)
-{
-    constexpr int E = Fmt<DT>::kPerChunk;
-    constexpr int S = Fmt<DT>::kBytes;
-    if (k >= g.nch)
-        return make_uint4(0, 0, 0, 0);
-    const int64_t j0 = k * E - g.head;
-    if (ALIGNED || (same_phase && j0 >= 0 && j0 + E <= cols))
-        return ld_chunk_cached(mrow - g.head * S + 16 * k);
-    return ld_partial<DT>(mrow, j0, cols);
-}
+// Row phases: x, y and mask rows all on the 16-byte grid (kMFast); y on x's
+// phase (kMSame); y on another phase (kMOther).  Off the grid, a mask row on x's
+// phase is read in vectors, one on another phase element by element (decided
+// per row).
+constexpr int kMFast = 0;
+constexpr int kMSame = 1;
+constexpr int kMOther = 2;
 
-// Logits of chunk k: zh (and, for fp32, the low part zl); cut slots -> -inf.
-template <int DT, bool ALIGNED>
-__device__ __forceinline__ void chunk_logits(const MaskedArgs &a, const RowGeom &g, int64_t k, int64_t limit,
-                                             const uint4 &xc, const uint4 &mc, bool has_mask,
-                                             float (&zh)[Fmt<DT>::kPerChunk], float (&zl)[Fmt<DT>::kPerChunk])
-{
-    constexpr int E = Fmt<DT>::kPerChunk;
-    float xf[E], mf[E];
-    unpack<DT>(xc, xf);
-    if (has_mask)
-        unpack<DT>(mc, mf);
-    // row-local indices fit 32 bits: these kernels serve rows of at most 64 KiB
-    const int j0 = (int)k * E - g.head;
-    const int lim = (int)(k < g.nch ? limit : 0);
-#pragma unroll
-    for (int e = 0; e < E; e++) {
-        const float mv = has_mask ? mf[e] : 0.f;
-        if constexpr (DT == kF32) {
-            const float ph = a.scale * xf[e];
-            const float pl = fmaf(a.scale, xf[e], -ph);
-            float s, err;
-            two_sum(ph, mv, s, err);
-            zh[e] = s;
-            zl[e] = err + pl;
-        } else {
-            zh[e] = fmaf(a.scale, xf[e], mv);
-            zl[e] = 0.f;
-        }
-        const int j = j0 + e;
-        if (j < 0 || j >= lim) {
-            zh[e] = -INFINITY;
-            zl[e] = 0.f;
-        }
-    }
-}
-
-// exp(z - m) for a logit z = zh + zl (scaled as Math<DT>::exp_shift scales).
+// exp(z - m) for a logit z = zh + zl (fp32) or zh (fp16 / bf16).  16-bit:
+// one FMA z log2e + c with c = bias - m log2e, computed once per row: the
+// rounding of m log2e scales the whole row's exps by one common factor, which
+// the normalisation cancels.
 template <int DT>
-__device__ __forceinline__ float exp_logit(float zh, float zl, float m)
+__device__ __forceinline__ float exp_logit(float zh, float zl, float m, float c)
 {
     if constexpr (DT == kF32) {
         float th, tl;
@@ -117,157 +80,270 @@ __device__ __forceinline__ float exp_logit(float zh, float zl, float m)
         const float r = tl + zl;
         return (fabsf(r) < INFINITY) ? fmaf(e, r, e) : e;
     } else {
-        return Math<DT>::exp_shift(zh, m);
+        (void)m;
+        (void)zl;
+        return ex2_ftz(fmaf(zh, kLog2e, c));
     }
 }
 
-}  // namespace
-
-template <int DT, int G, int V, bool ALIGNED>
-__global__ void __launch_bounds__(kRowgroupThreads) k_masked_rowgroup(const MaskedArgs a)
+template <int DT>
+__device__ __forceinline__ float exp_offset(float m)
 {
-    pdl_enter();
+    if constexpr (DT == kF32)
+        return 0.f;
+    else
+        return Math<DT>::kExpBias - m * kLog2e;
+}
+
+// The logit of one value: zh (and the fp32 low part zl) of scale * x + mv.
+template <int DT>
+__device__ __forceinline__ void logit(float scale, float xv, float mv, float &zh, float &zl)
+{
+    if constexpr (DT == kF32) {
+        const float ph = scale * xv;
+        const float pl = fmaf(scale, xv, -ph);
+        float s, err;
+        two_sum(ph, mv, s, err);
+        zh = s;
+        zl = err + pl;
+    } else {
+        zh = fmaf(scale, xv, mv);
+        zl = 0.f;
+    }
+}
+
+// Logits of interior chunk q holding nv visible values (0 < nv <= E); slots
+// past nv are cut to -inf.
+template <int DT, int MODE, bool HAS_MASK>
+__device__ __forceinline__ void chunk_logits(const MaskedArgs &a, const ShortRow &g, const char *mrow, bool m_vec,
+                                             int q, int nv, const uint4 &xc, float (&zh)[Fmt<DT>::kPerChunk],
+                                             float (&zl)[Fmt<DT>::kPerChunk])
+{
+    constexpr int E = Fmt<DT>::kPerChunk;
+    constexpr int S = Fmt<DT>::kBytes;
+    float xf[E], mf[E];
+    unpack<DT>(xc, xf);
+    if constexpr (HAS_MASK) {
+        if (MODE == kMFast || m_vec) {
+            unpack<DT>(ld_chunk_cached(mrow - g.head * S + ((int64_t)(g.kf + q) << 4)), mf);
+        } else {
+            const int j0 = (g.kf + q) * E - g.head;
+#pragma unroll
+            for (int e = 0; e < E; e++)
+                mf[e] = ld_elem<DT>(mrow, j0 + e);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < E; e++)
+        logit<DT>(a.scale, xf[e], HAS_MASK ? mf[e] : 0.f, zh[e], zl[e]);
+    if (nv < E) {
+#pragma unroll
+        for (int e = 0; e < E; e++)
+            if (e >= nv) {
+                zh[e] = -INFINITY;
+                zl[e] = 0.f;
+            }
+    }
+}
+
+template <int G>
+struct MaxGroup {
+    __device__ __forceinline__ float operator()(float v) const { return G == 32 ? warp_max_redux(v) : group_max<G>(v); }
+};
+
+template <int DT, int G>
+struct SumGroup {
+    __device__ __forceinline__ typename Math<DT>::Acc operator()(typename Math<DT>::Acc a) const
+    {
+        return group_sum<DT, G>(a);
+    }
+};
+
+template <int DT>
+struct MaxSumCta {
+    float *smax;
+    typename Math<DT>::Acc *ssum;
+    __device__ __forceinline__ float max(float v) const { return block_max(v, smax); }
+    __device__ __forceinline__ typename Math<DT>::Acc sum(typename Math<DT>::Acc a) const
+    {
+        return block_sum<DT>(a, ssum);
+    }
+};
+
+template <int DT, int G>
+struct MaxSumGroup {
+    __device__ __forceinline__ float max(float v) const { return MaxGroup<G>{}(v); }
+    __device__ __forceinline__ typename Math<DT>::Acc sum(typename Math<DT>::Acc a) const
+    {
+        return SumGroup<DT, G>{}(a);
+    }
+};
+
+// One row for a team of L threads.  KEEP: the logits, then their exps, stay in
+// registers (lanes per row); else x stays packed and the logits are recomputed
+// in each pass (CTA per row, with the 128-byte-line chunk map).  Interior
+// chunks wholly past the causal limit are neither read nor exponentiated; only
+// the chunk the limit falls in tests its values one by one.
+template <int DT, int V, int MODE, bool HAS_MASK, int NE, bool KEEP, class Red>
+__device__ __forceinline__ void masked_row(const MaskedArgs &a, int64_t r, bool valid, int lane, int L, Red red)
+{
     using M = Math<DT>;
     constexpr int E = Fmt<DT>::kPerChunk;
     constexpr int S = Fmt<DT>::kBytes;
-    const int groups = blockDim.x / G;
-    const int gl = threadIdx.x & (G - 1);
-    const int64_t stride = (int64_t)gridDim.x * groups;
-    const bool has_mask = a.mask != nullptr;
-    for (int64_t base = (int64_t)blockIdx.x * groups; base < a.rows; base += stride) {
-        const int64_t r = base + threadIdx.x / G;
-        const bool valid = r < a.rows;
-        const int64_t rr = valid ? r : 0;
-        const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, rr, a.cols);
-        const char *mrow = has_mask ? a.mask + (rr % a.mask_rows) * a.cols * S : nullptr;
-        const bool m_same = has_mask && ((reinterpret_cast<uintptr_t>(mrow) - reinterpret_cast<uintptr_t>(g.xr)) & 15) == 0;
-        const int64_t limit = visible_limit(a, rr);
+    constexpr int PH = MODE == kMFast ? kPhAligned : (MODE == kMSame ? kPhSame : kPhOther);
+    const int64_t rr = valid ? r : 0;
+    const ShortRow g = short_row<DT, MODE == kMFast>(a.x, a.y, rr, (int)a.cols);
+    const char *mrow = HAS_MASK ? a.mask + (rr % a.mask_rows) * a.cols * S : nullptr;
+    const bool m_vec = HAS_MASK && ((reinterpret_cast<uintptr_t>(mrow) - reinterpret_cast<uintptr_t>(g.xr)) & 15) == 0;
+    // row-local indices fit 32 bits: these kernels serve rows of at most 64 KiB
+    const int lim = valid ? (int)visible_limit(a, rr) : 0;
+    const int span = valid ? g.span : 0;
+    int sh = 0;
+    if constexpr (!KEEP) {
+        sh = (int)(((reinterpret_cast<uintptr_t>(g.x0) >> 4) + g.kf) & 7);
+        if (sh > L * V - span)
+            sh = 0;
+    }
+    const int q0 = lane - sh;
+    // visible values of interior chunk i (0: absent or wholly cut)
+    int nv[V];
+    uint4 xc[V];
+#pragma unroll
+    for (int i = 0; i < V; i++) {
+        const int q = q0 + i * L;
+        const int j0 = (g.kf + q) * E - g.head;
+        const int left = lim - j0;
+        nv[i] = (unsigned)q < (unsigned)span ? (left < 0 ? 0 : (left > E ? E : left)) : 0;
+        xc[i] = nv[i] > 0 ? ld_chunk(g.x0 + ((int64_t)(g.kf + q) << 4)) : make_uint4(0, 0, 0, 0);
+    }
+    int je[NE > 0 ? NE : 1];
+    float eh[NE > 0 ? NE : 1], el[NE > 0 ? NE : 1];
+#pragma unroll
+    for (int u = 0; u < NE; u++) {
+        const int p = lane + u * L;
+        je[u] = (valid && p < g.ne) ? edge_col(g, p) : -1;
+        eh[u] = -INFINITY;
+        el[u] = 0.f;
+        if (je[u] >= 0 && je[u] < lim)
+            logit<DT>(a.scale, ld_elem<DT>(g.xr, je[u]), HAS_MASK ? ld_elem<DT>(mrow, je[u]) : 0.f, eh[u], el[u]);
+    }
 
-        // chunks wholly past the causal limit are neither read nor exponentiated
-        float zh[V][E], zl[V][E];
-        bool live[V];
+    float zh[KEEP ? V : 1][E], zl[KEEP ? V : 1][E];
+    float m = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < V; i++) {
-            const int64_t k = gl + i * G;
-            live[i] = valid && k < g.nch && k * E - g.head < limit;
-            const uint4 xc = live[i] ? load_chunk<DT, ALIGNED>(g, k, a.cols) : neg_inf_chunk<DT>();
-            const uint4 mc = (live[i] && has_mask) ? load_mask_chunk<DT, ALIGNED>(g, mrow, m_same, k, a.cols)
-                                                   : make_uint4(0, 0, 0, 0);
-            chunk_logits<DT, ALIGNED>(a, g, k, limit, xc, mc, has_mask, zh[i], zl[i]);
+    for (int i = 0; i < V; i++) {
+        if (nv[i] > 0) {
+            float h[E], l[E];
+            chunk_logits<DT, MODE, HAS_MASK>(a, g, mrow, m_vec, q0 + i * L, nv[i], xc[i], h, l);
+#pragma unroll
+            for (int e = 0; e < E; e++) {
+                m = fmaxf(m, h[e]);
+                if constexpr (KEEP) {
+                    zh[i][e] = h[e];
+                    zl[i][e] = l[e];
+                }
+            }
         }
-        float m = -INFINITY;
+    }
 #pragma unroll
-        for (int i = 0; i < V; i++)
+    for (int u = 0; u < NE; u++)
+        m = fmaxf(m, eh[u]);
+    m = red.max(m);
+    const float c = exp_offset<DT>(m);
+
+    typename M::Acc acc = M::zero();
 #pragma unroll
-            for (int e = 0; e < E; e++)
-                m = fmaxf(m, zh[i][e]);
-        m = G == 32 ? warp_max_redux(m) : group_max<G>(m);
-        typename M::Acc acc = M::zero();
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            if (live[i]) {
+    for (int i = 0; i < V; i++) {
+        if (nv[i] > 0) {
+            float h[E], l[E];
+            if constexpr (KEEP) {
 #pragma unroll
                 for (int e = 0; e < E; e++) {
-                    zh[i][e] = exp_logit<DT>(zh[i][e], zl[i][e], m);
-                    M::add(acc, zh[i][e]);
+                    h[e] = zh[i][e];
+                    l[e] = zl[i][e];
+                }
+            } else {
+                opaque(xc[i]);
+                chunk_logits<DT, MODE, HAS_MASK>(a, g, mrow, m_vec, q0 + i * L, nv[i], xc[i], h, l);
+            }
+#pragma unroll
+            for (int e = 0; e < E; e++) {
+                const float ev = exp_logit<DT>(h[e], l[e], m, c);
+                M::add(acc, ev);
+                if constexpr (KEEP)
+                    zh[i][e] = ev;
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < NE; u++) {
+        eh[u] = je[u] >= 0 ? exp_logit<DT>(eh[u], el[u], m, c) : 0.f;
+        M::add(acc, eh[u]);
+    }
+    acc = red.sum(acc);
+    const float inv = 1.0f / M::value(acc);
+    if (!valid)
+        return;
+#pragma unroll
+    for (int i = 0; i < V; i++) {
+        const int q = q0 + i * L;
+        if ((unsigned)q < (unsigned)span) {
+            float o[E];
+            if (nv[i] > 0) {
+                if constexpr (KEEP) {
+#pragma unroll
+                    for (int e = 0; e < E; e++)
+                        o[e] = zh[i][e] * inv;
+                } else {
+                    float h[E], l[E];
+                    opaque(xc[i]);
+                    chunk_logits<DT, MODE, HAS_MASK>(a, g, mrow, m_vec, q, nv[i], xc[i], h, l);
+#pragma unroll
+                    for (int e = 0; e < E; e++)
+                        o[e] = exp_logit<DT>(h[e], l[e], m, c) * inv;
                 }
             } else {
 #pragma unroll
                 for (int e = 0; e < E; e++)
-                    zh[i][e] = 0.f;
+                    o[e] = 0.f * inv;  // a cut chunk: exp(-inf) = 0 (NaN for a row with no visible key)
             }
+            store_interior<DT, PH>(g, q, pack<DT>(o));
         }
-        acc = group_sum<DT, G>(acc);
-        const float inv = 1.0f / M::value(acc);
-        if (valid) {
+    }
 #pragma unroll
-            for (int i = 0; i < V; i++) {
-                const int64_t k = gl + i * G;
-                if (k < g.nch) {
-                    float o[E];
-#pragma unroll
-                    for (int e = 0; e < E; e++)
-                        o[e] = zh[i][e] * inv;
-                    store_chunk<DT, ALIGNED>(g, k, a.cols, pack<DT>(o), a.y_vec != 0);
-                }
-            }
-        }
+    for (int u = 0; u < NE; u++)
+        if (je[u] >= 0)
+            st_elem<DT>(g.yr, je[u], eh[u] * inv);
+}
+
+}  // namespace
+
+template <int DT, int G, int V, int MODE, bool HAS_MASK>
+__global__ void __launch_bounds__(kRowgroupThreads) k_masked_rowgroup(const MaskedArgs a)
+{
+    pdl_enter();
+    constexpr int NE = MODE == kMFast ? 0 : edge_slots<DT, G>();
+    const int groups = blockDim.x / G;
+    const int gl = threadIdx.x & (G - 1);
+    const int64_t stride = (int64_t)gridDim.x * groups;
+    // every thread of a CTA runs the same number of iterations, so the
+    // butterflies see converged warps
+    for (int64_t base = (int64_t)blockIdx.x * groups; base < a.rows; base += stride) {
+        const int64_t r = base + threadIdx.x / G;
+        masked_row<DT, V, MODE, HAS_MASK, NE, true>(a, r, r < a.rows, gl, G, MaxSumGroup<DT, G>{});
     }
 }
 
-template <int DT, int V, bool ALIGNED>
+template <int DT, int V, int MODE, bool HAS_MASK>
 __global__ void __launch_bounds__(512) k_masked_block(const MaskedArgs a)
 {
     pdl_enter();
-    using M = Math<DT>;
-    using Acc = typename M::Acc;
-    constexpr int E = Fmt<DT>::kPerChunk;
-    constexpr int S = Fmt<DT>::kBytes;
     __shared__ float smax[32];
-    __shared__ Acc ssum[32];
-    const int T = blockDim.x, t = threadIdx.x;
-    const bool has_mask = a.mask != nullptr;
-    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
-        const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, r, a.cols);
-        const char *mrow = has_mask ? a.mask + (r % a.mask_rows) * a.cols * S : nullptr;
-        const bool m_same = has_mask && ((reinterpret_cast<uintptr_t>(mrow) - reinterpret_cast<uintptr_t>(g.xr)) & 15) == 0;
-        const int64_t limit = visible_limit(a, r);
-        // x stays packed in registers; the mask chunk is re-read each pass
-        // chunks wholly past the causal limit are not read (their logits are all
-        // -inf; exp gives the zeros the write pass stores)
-        const int lim32 = (int)limit;  // row-local: rows here are at most 32 KiB
-        auto live = [&](int64_t k) { return k < g.nch && (int)k * E - g.head < lim32; };
-        auto logits = [&](const uint4 &xc, int64_t k, float(&zh)[E], float(&zl)[E]) {
-            const uint4 mc = (has_mask && live(k)) ? load_mask_chunk<DT, ALIGNED>(g, mrow, m_same, k, a.cols)
-                                                   : make_uint4(0, 0, 0, 0);
-            chunk_logits<DT, ALIGNED>(a, g, k, limit, xc, mc, has_mask, zh, zl);
-        };
-        uint4 xc[V];
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            const int64_t k = t + (int64_t)i * T;
-            xc[i] = live(k) ? load_chunk<DT, ALIGNED>(g, k, a.cols) : neg_inf_chunk<DT>();
-        }
-        float m = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            float zh[E], zl[E];
-            logits(xc[i], t + (int64_t)i * T, zh, zl);
-#pragma unroll
-            for (int e = 0; e < E; e++)
-                m = fmaxf(m, zh[e]);
-        }
-        m = block_max(m, smax);
-#pragma unroll
-        for (int i = 0; i < V; i++)
-            opaque(xc[i]);
-        Acc acc = M::zero();
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            float zh[E], zl[E];
-            logits(xc[i], t + (int64_t)i * T, zh, zl);
-#pragma unroll
-            for (int e = 0; e < E; e++)
-                M::add(acc, exp_logit<DT>(zh[e], zl[e], m));
-        }
-        acc = block_sum<DT>(acc, ssum);
-        const float inv = 1.0f / M::value(acc);
-#pragma unroll
-        for (int i = 0; i < V; i++)
-            opaque(xc[i]);
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            const int64_t k = t + (int64_t)i * T;
-            if (k < g.nch) {
-                float zh[E], zl[E];
-                logits(xc[i], k, zh, zl);
-#pragma unroll
-                for (int e = 0; e < E; e++)
-                    zh[e] = exp_logit<DT>(zh[e], zl[e], m) * inv;
-                store_chunk<DT, ALIGNED>(g, k, a.cols, pack<DT>(zh), a.y_vec != 0);
-            }
-        }
-    }
+    __shared__ typename Math<DT>::Acc ssum[32];
+    constexpr int NE = MODE == kMFast ? 0 : 1;  // >= 32 threads: one edge element each at most
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
+        masked_row<DT, V, MODE, HAS_MASK, NE, false>(a, r, true, threadIdx.x, blockDim.x,
+                                                     MaxSumCta<DT>{smax, ssum});
 }
 
 namespace {
@@ -278,21 +354,41 @@ MaskedArgs args_of(const MaskedLaunch &l)
                       (const char *)l.mask, l.mask_rows, l.causal_q};
 }
 
-template <int DT, int G, int V, bool A>
+int mode_of(const MaskedLaunch &l)
+{
+    if (l.plan.aligned)
+        return kMFast;
+    return l.plan.y_vector ? kMSame : kMOther;
+}
+
+template <int DT, int G, int V, int MODE, bool HM>
 int mrg_one(const MaskedLaunch &l)
 {
-    return launch_pdl(k_masked_rowgroup<DT, G, V, A>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
-                      (cudaStream_t)l.stream, no_attr(), args_of(l));
+    return launch_pdl(k_masked_rowgroup<DT, G, V, MODE, HM>, dim3((unsigned)l.plan.grid_x),
+                      dim3(l.plan.block_threads), 0, (cudaStream_t)l.stream, no_attr(), args_of(l));
+}
+
+template <int DT, int G, int V, int MODE>
+int mrg_m(const MaskedLaunch &l)
+{
+    return l.mask ? mrg_one<DT, G, V, MODE, true>(l) : mrg_one<DT, G, V, MODE, false>(l);
 }
 
 template <int DT, int G, int V>
 int mrg_a(const MaskedLaunch &l)
 {
-    return l.plan.aligned ? mrg_one<DT, G, V, true>(l) : mrg_one<DT, G, V, false>(l);
+    switch (mode_of(l)) {
+    case kMFast:
+        return mrg_m<DT, G, V, kMFast>(l);
+    case kMSame:
+        return mrg_m<DT, G, V, kMSame>(l);
+    default:
+        return mrg_m<DT, G, V, kMOther>(l);
+    }
 }
 
 // V chunks per lane with the logits (fp32: two floats each) in at most 32
-// registers: V <= 4 for 16-bit, V <= 4 for fp32 (4 x 4 x 2).
+// registers: V <= 4.
 template <int DT, int G>
 int mrg_v(const MaskedLaunch &l)
 {
@@ -329,22 +425,40 @@ int mrg_dt(const MaskedLaunch &l)
     }
 }
 
-template <int DT, int V, bool A>
+template <int DT, int V, int MODE, bool HM>
 int mblk_one(const MaskedLaunch &l)
 {
-    return launch_pdl(k_masked_block<DT, V, A>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
-                      (cudaStream_t)l.stream, no_attr(), args_of(l));
+    return launch_pdl(k_masked_block<DT, V, MODE, HM>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads),
+                      0, (cudaStream_t)l.stream, no_attr(), args_of(l));
+}
+
+template <int DT, int V, int MODE>
+int mblk_m(const MaskedLaunch &l)
+{
+    return l.mask ? mblk_one<DT, V, MODE, true>(l) : mblk_one<DT, V, MODE, false>(l);
+}
+
+template <int DT, int V>
+int mblk_a(const MaskedLaunch &l)
+{
+    switch (mode_of(l)) {
+    case kMFast:
+        return mblk_m<DT, V, kMFast>(l);
+    case kMSame:
+        return mblk_m<DT, V, kMSame>(l);
+    default:
+        return mblk_m<DT, V, kMOther>(l);
+    }
 }
 
 template <int DT>
 int mblk_dt(const MaskedLaunch &l)
 {
-    const bool A = l.plan.aligned != 0;
     switch (l.plan.chunks_per_thread) {
     case 2:
-        return A ? mblk_one<DT, 2, true>(l) : mblk_one<DT, 2, false>(l);
+        return mblk_a<DT, 2>(l);
     case 4:
-        return A ? mblk_one<DT, 4, true>(l) : mblk_one<DT, 4, false>(l);
+        return mblk_a<DT, 4>(l);
     default:
         return (int)cudaErrorInvalidValue;
     }

@@ -348,30 +348,33 @@ int plan_masked(const softmax_device_info &dev, const void *x, const void *y, in
     p.cluster_x = 1;
     p.aligned = g.aligned;
     p.y_vector = g.y_vec;
-    const bool rg_fits = g.nch_max <= 32 * 4;
-    const bool blk_fits = g.nch_max <= 512 * 4;
+    // sized by a row's whole interior chunks (its partial edges go element by
+    // element)
+    const int64_t n = g.nint > 1 ? g.nint : 1;
+    const bool rg_fits = n <= 32 * 4;
+    const bool blk_fits = n <= 512 * 4;
     int v = variant;
     if (v == SOFTMAX_VARIANT_AUTO)
         v = rg_fits ? SOFTMAX_VARIANT_ROWGROUP : SOFTMAX_VARIANT_BLOCK;
     if (v == SOFTMAX_VARIANT_ROWGROUP) {
         if (!rg_fits)
             return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
-        int64_t G = g.nch_max <= 4 ? next_pow2(g.nch_max) : next_pow2(ceil_div(g.nch_max, 4));
+        int64_t G = n <= 4 ? next_pow2(n) : next_pow2(ceil_div(n, 4));
         if (G > 32)
             G = 32;
         p.variant = v;
         p.lanes_per_row = (int)G;
-        p.chunks_per_thread = (int)next_pow2(ceil_div(g.nch_max, G));
+        p.chunks_per_thread = (int)next_pow2(ceil_div(n, G));
         p.block_threads = kRowgroupThreads;
         const int64_t ctas = ceil_div(rows, kRowgroupThreads / G);
         p.grid_x = ctas < INT32_MAX ? ctas : INT32_MAX;
     } else if (v == SOFTMAX_VARIANT_BLOCK) {
         if (!blk_fits)
             return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
-        const int V = ceil_div(g.nch_max, 4) >= 32 ? 4 : 2;
+        const int V = ceil_div(n, 4) >= 32 ? 4 : 2;
         p.variant = v;
         p.chunks_per_thread = V;
-        p.block_threads = (int)(ceil_div(ceil_div(g.nch_max, V), 32) * 32);
+        p.block_threads = (int)(ceil_div(ceil_div(n, V), 32) * 32);
         p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
     } else {
         return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
