@@ -89,7 +89,11 @@ typedef enum {
     SOFTMAX_VARIANT_SPLITK_WIDE = 6, /* P CTAs per row over all SMs, partials merged through a
                                         global workspace in a second launch (softmax_fwd_ws
                                         only: it needs the workspace) */
-    SOFTMAX_VARIANT_COUNT = 7
+    SOFTMAX_VARIANT_SPLITK_GRID = 7, /* P CTAs per row over all SMs in one cooperative launch,
+                                        partials exchanged at a bounded per-row grid barrier
+                                        through library-owned scratch; fp16 / bf16 shares held
+                                        in shared memory (one HBM read) */
+    SOFTMAX_VARIANT_COUNT = 8
 } softmax_variant;
 
 /*
@@ -349,12 +353,15 @@ int softmax_device_query(softmax_device_info *dev);
  * softmax_get_device_error -- read and clear the library's device-side error
  * word on `stream` (the copy is ordered after work already enqueued there and
  * the call synchronises that stream).  *code receives 0 when no kernel
- * reported a problem since the last call, else a nonzero code whose low byte
- * names the wait that gave up (1 = bulk-copy arrival, 2 = buffer release).
- * Kernels that wait on an mbarrier bound the wait with %globaltimer; when it
- * runs out they record the code here, drain their own copies in flight and
- * return, so the context stays usable.  Returns SOFTMAX_ERR_DEVICE_TIMEOUT if
- * *code is nonzero, SOFTMAX_OK otherwise, SOFTMAX_ERR_CUDA if the copy failed.
+ * reported a problem since the last call, else a nonzero code: the bits of
+ * the waits that gave up (1 = bulk-copy arrival, 2 = buffer release, 3 =
+ * cluster peer statistics, 4 = a row's grid barrier in SPLITK_GRID).  Kernels
+ * that wait bound the wait with %globaltimer; when it runs out they record the
+ * code here, drain their own copies in flight and return, so the context
+ * stays usable.  A nonzero code also makes this call synchronise the device
+ * and clear SPLITK_GRID's barrier scratch.  Returns
+ * SOFTMAX_ERR_DEVICE_TIMEOUT if *code is nonzero, SOFTMAX_OK otherwise,
+ * SOFTMAX_ERR_CUDA if the copy failed.
  */
 int softmax_get_device_error(softmax_stream_t stream, unsigned int *code);
 

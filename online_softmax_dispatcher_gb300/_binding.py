@@ -32,8 +32,10 @@ VARIANT_BLOCK_TMA = 3
 VARIANT_STREAM = 4
 VARIANT_SPLITK = 5
 VARIANT_SPLITK_WIDE = 6
-VARIANT_COUNT = 7
-VARIANTS = {"auto": 0, "rowgroup": 1, "block": 2, "block_tma": 3, "stream": 4, "splitk": 5, "splitk_wide": 6}
+VARIANT_SPLITK_GRID = 7
+VARIANT_COUNT = 8
+VARIANTS = {"auto": 0, "rowgroup": 1, "block": 2, "block_tma": 3, "stream": 4, "splitk": 5, "splitk_wide": 6,
+            "splitk_grid": 7}
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libosd_softmax.so")

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(BUILD, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_SOURCES = ["abi.cu", "k_rowgroup_f32.cu", "k_rowgroup_f16.cu", "k_rowgroup_bf16.cu", "k_block.cu",
                 "k_stream.cu", "k_splitk.cu", "k_tma.cu", "k_bwd.cu", "k_wide.cu",
-                "noalloc.cu", "k_masked.cu", "k_norm_f32.cu", "k_norm_f16.cu", "k_norm_bf16.cu"]
+                "noalloc.cu", "k_masked.cu", "k_norm_f32.cu", "k_norm_f16.cu", "k_norm_bf16.cu", "k_grid.cu"]
 HOST_SOURCES = ["plan.cpp"]
 
 

@@ -112,7 +112,20 @@ int launch(const DeviceCache &dc, const void *x, void *y, int64_t rows, int64_t 
         return rc;
     Launch l{x, y, rows, cols, dtype, plan, stream, dc.error_word};
     int e;
+    if (plan.variant == SOFTMAX_VARIANT_SPLITK_GRID && grid_capturing(stream)) {
+        // the grid split's scratch slots are ordered by CUDA events, which a
+        // graph capture cannot take: capture the cluster split (or the stream
+        // kernel) instead
+        softmax_launch_plan alt;
+        if (softmax_plan(&dc.info, x, y, rows, cols, dtype, SOFTMAX_VARIANT_SPLITK, &alt) != SOFTMAX_OK &&
+            softmax_plan(&dc.info, x, y, rows, cols, dtype, SOFTMAX_VARIANT_STREAM, &alt) != SOFTMAX_OK)
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        return launch(dc, x, y, rows, cols, dtype, alt, stream);
+    }
     switch (plan.variant) {
+    case SOFTMAX_VARIANT_SPLITK_GRID:
+        e = launch_grid(l);
+        break;
     case SOFTMAX_VARIANT_SPLITK_WIDE:
         // needs the workspace only softmax_fwd_ws supplies
         if (!workspace || workspace_bytes < wide_workspace_bytes(plan))
@@ -301,15 +314,16 @@ OSD_API int softmax_fwd_plan(const void *x, void *y, int64_t rows, int64_t cols,
 
 namespace {
 
-// The plan softmax_fwd_ws launches: the dispatcher's choice, widened to
-// SPLITK_WIDE when it picked the cluster split (few, very long rows).
+// The plan softmax_fwd_ws launches: the dispatcher's choice, with the two-launch
+// SPLITK_WIDE (partials in the caller's workspace) in place of the cluster or
+// grid split (few, very long rows).
 int plan_ws(const DeviceCache &dc, const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
             softmax_launch_plan *plan)
 {
     int rc = softmax_plan(&dc.info, x, y, rows, cols, dtype, SOFTMAX_VARIANT_AUTO, plan);
     if (rc != SOFTMAX_OK)
         return rc;
-    if (plan->variant == SOFTMAX_VARIANT_SPLITK) {
+    if (plan->variant == SOFTMAX_VARIANT_SPLITK || plan->variant == SOFTMAX_VARIANT_SPLITK_GRID) {
         softmax_launch_plan wide;
         if (softmax_plan(&dc.info, x, y, rows, cols, dtype, SOFTMAX_VARIANT_SPLITK_WIDE, &wide) == SOFTMAX_OK)
             *plan = wide;
@@ -427,6 +441,12 @@ OSD_API int softmax_get_device_error(softmax_stream_t stream, unsigned int *code
     if (e != cudaSuccess)
         return cuda_fail(e);
     *code = v;
+    if (v) {
+        // a wait gave up: the grid split's barrier counts may be left mid-way
+        const int re = reset_grid_scratch();
+        if (re != 0)
+            return record_cuda_error(re);
+    }
     return v ? SOFTMAX_ERR_DEVICE_TIMEOUT : SOFTMAX_OK;
 }
 
@@ -484,6 +504,8 @@ OSD_API const char *softmax_variant_name(int variant)
         return "splitk";
     case SOFTMAX_VARIANT_SPLITK_WIDE:
         return "splitk_wide";
+    case SOFTMAX_VARIANT_SPLITK_GRID:
+        return "splitk_grid";
     default:
         return "unknown";
     }

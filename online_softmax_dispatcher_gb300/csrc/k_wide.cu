@@ -62,41 +62,6 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         ws[r * P + p] = out;
 }
 
-// Merge the P partials of row r; every warp does it, identically.
-template <int DT>
-__device__ __forceinline__ void merge_partials(const float4 *ws, int64_t r, int P, float &m, float &inv)
-{
-    const int lane = threadIdx.x & 31;
-    if constexpr (DT == kF32) {
-        float mloc = -INFINITY;
-        for (int i = lane; i < P; i += 32)
-            mloc = fmaxf(mloc, ws[r * P + i].x);
-        m = group_max<32>(mloc);
-        CSum acc{0.f, 0.f};
-        for (int i = lane; i < P; i += 32) {
-            const float4 q = ws[r * P + i];
-            if (q.x != -INFINITY) {
-                // one rescale per partial: (s + c) * exp(m_p - m), exp_shift keeps
-                // m_p - m exact
-                const float f = Math<kF32>::exp_shift(q.x, m);
-                Math<kF32>::add(acc, q.y * f);
-                Math<kF32>::add(acc, q.z * f);
-            }
-        }
-        acc = group_sum<kF32, 32>(acc);
-        inv = 1.0f / (acc.s + acc.c);
-    } else {
-        MD md{-INFINITY, 0.f};
-        for (int i = lane; i < P; i += 32) {
-            const float4 q = ws[r * P + i];
-            md = md_merge<DT>(md, MD{q.x, q.y});
-        }
-        md = warp_md<DT>(md);
-        m = md.m;
-        inv = 1.0f / md.d;
-    }
-}
-
 template <int DT, bool ALIGNED>
 __global__ void __launch_bounds__(kStreamThreads, 2)
     k_wide_write(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int P,

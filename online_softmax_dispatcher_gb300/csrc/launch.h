@@ -17,6 +17,11 @@ constexpr int kBlockMaxChunks = 16;     // V of the block-per-row kernel
 constexpr int kStreamThreads = 512;     // CTA size of the streaming kernel
 constexpr int kStreamUnroll = 8;        // 16-byte loads in flight per thread per step
 constexpr int kWideStep = 4;            // the same for the wide split: 64 registers at two 512-thread CTAs per SM
+constexpr int kGridThreads = 512;       // SPLITK_GRID: CTA size (resident and streaming forms)
+constexpr int kGridSlots = 16;          // SPLITK_GRID: scratch slots (launches in flight at once)
+constexpr int kGridMaxRows = 128;       // SPLITK_GRID: rows a slot serves
+constexpr int kGridMaxPartials = 512;   // SPLITK_GRID: rows x CTAs per row a slot serves
+constexpr int kGridStaticSmem = 1024;   // SPLITK_GRID resident form: static shared memory, upper bound
 constexpr int kMaxCluster = 16;         // non-portable cluster size limit
 constexpr int kSplitStages = 6;         // SPLITK: shared-memory ring depth
 constexpr int kSplitStageBytes = 32768; // SPLITK: bytes per stage (one bulk copy)
@@ -126,6 +131,15 @@ int plan_norm(const softmax_device_info &dev, int kind, const void *x, const voi
 // Remember a failing cudaError_t for softmax_last_cuda_error (this thread) and
 // return SOFTMAX_ERR_CUDA.
 int record_cuda_error(int cuda_error);
+
+// SPLITK_GRID: one cooperative launch over every SM (k_grid.cu); scratch in the
+// library's slot pool.  grid_capturing: the stream is being captured into a
+// graph (the slot pool's event waits cannot be captured: callers plan
+// another variant then).  reset_grid_scratch: clear the pool's barrier state
+// after a reported device time-out.
+int launch_grid(const Launch &l);
+int grid_capturing(void *stream);
+int reset_grid_scratch();
 
 // SPLITK_WIDE: two launches, partials in `workspace` (rows * grid_x float4).
 int launch_wide(const Launch &l, void *workspace);

@@ -226,6 +226,48 @@ void plan_wide(const Geometry &g, int64_t rows, const softmax_device_info &dev, 
     p.grid_y = rows;
 }
 
+// SPLITK_GRID: P CTAs per row, all resident (cooperative launch).  fp16 /
+// bf16 rows whose share fits one CTA's shared memory at one CTA per SM take
+// the resident form (the share is read from HBM once, into shared memory);
+// the rest take the streaming form at two CTAs per SM.
+bool grid_possible(int64_t rows, const softmax_device_info &dev)
+{
+    return dev.cc_major >= 9 && rows >= 1 && rows * 2 <= dev.sm_count && rows <= kGridMaxRows;
+}
+
+void plan_grid(const Geometry &g, int64_t rows, const softmax_device_info &dev, softmax_launch_plan &p)
+{
+    const int64_t budget = int64_t(dev.max_smem_optin) - kGridStaticSmem;
+    const int64_t p1 = dev.sm_count / rows;  // one CTA per SM
+    int64_t P = 0, smem = 0;
+    if (g.S == 2 && p1 >= 1 && p1 * rows <= kGridMaxPartials) {
+        const int64_t bytes = ceil_div(g.nch_max, p1) * 16;
+        if (bytes <= budget) {
+            P = p1;
+            smem = ceil_div(bytes, 128) * 128;
+            if (smem > budget)
+                smem = bytes;
+        }
+    }
+    if (P == 0) {
+        P = 2 * int64_t(dev.sm_count) / rows;
+        const int64_t by_work = g.nch_max / (int64_t(kGridThreads) * kWideStep);
+        if (P > by_work)
+            P = by_work;
+        if (P * rows > kGridMaxPartials)
+            P = kGridMaxPartials / rows;
+        if (P < 1)
+            P = 1;
+    }
+    p.variant = SOFTMAX_VARIANT_SPLITK_GRID;
+    p.chunks_per_thread = kWideStep;
+    p.block_threads = kGridThreads;
+    p.stages = smem > 0 ? 1 : 0;
+    p.smem_bytes = (int)smem;
+    p.grid_x = P;
+    p.grid_y = rows;
+}
+
 bool splitk_possible(int64_t rows, const softmax_device_info &dev)
 {
     return dev.cluster_launch && rows >= 1 && rows <= 65535 &&
@@ -314,6 +356,22 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
         if (p.grid_y != rows || rows > 65535 || p.grid_x > 65535)
             return SOFTMAX_ERR_INVALID_ARG;
         return SOFTMAX_OK;
+    case SOFTMAX_VARIANT_SPLITK_GRID: {
+        if (p.block_threads != kGridThreads || p.cluster_x != 1 || p.grid_y != rows || !grid_possible(rows, dev))
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.grid_x * p.grid_y > kGridMaxPartials || V != kWideStep)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (p.stages == 1) {
+            // resident: one CTA per SM, the share in shared memory
+            const int64_t need = ceil_div(g.nch_max, p.grid_x) * 16;
+            if (g.S != 2 || p.grid_x * p.grid_y > dev.sm_count || p.smem_bytes < need ||
+                p.smem_bytes > dev.max_smem_optin - kGridStaticSmem)
+                return SOFTMAX_ERR_INVALID_ARG;
+        } else if (p.stages != 0 || p.smem_bytes != 0 || p.grid_x * p.grid_y > 2 * int64_t(dev.sm_count)) {
+            return SOFTMAX_ERR_INVALID_ARG;
+        }
+        return SOFTMAX_OK;
+    }
     case SOFTMAX_VARIANT_SPLITK:
         if (p.block_threads != kSplitThreads || p.stages != kSplitStages ||
             p.smem_bytes != kSplitStages * kSplitStageBytes)
@@ -632,6 +690,8 @@ extern "C" __attribute__((visibility("default"))) int softmax_plan(
         const bool long_rows = g.nch_max >= int64_t(8) * (kSplitStageBytes / 16);
         if (rowgroup_fits(g))
             v = SOFTMAX_VARIANT_ROWGROUP;
+        else if (few_rows && long_rows && grid_possible(rows, *dev))
+            v = SOFTMAX_VARIANT_SPLITK_GRID;
         else if (few_rows && long_rows && splitk_possible(rows, *dev))
             v = SOFTMAX_VARIANT_SPLITK;
         else if (block_fits(g))
@@ -670,6 +730,11 @@ extern "C" __attribute__((visibility("default"))) int softmax_plan(
         if (rows > 65535)
             return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
         plan_wide(g, rows, *dev, p);
+        break;
+    case SOFTMAX_VARIANT_SPLITK_GRID:
+        if (!grid_possible(rows, *dev))
+            return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
+        plan_grid(g, rows, *dev, p);
         break;
     default:
         return SOFTMAX_ERR_UNSUPPORTED_SHAPE;

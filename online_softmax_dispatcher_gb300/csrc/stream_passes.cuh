@@ -124,4 +124,42 @@ __device__ void pass_write(const RowGeom &g, int64_t kb, int64_t ke, int64_t col
     }
 }
 
+// Merge the P partial statistics of row r (float4 slots: fp32 (m, s, c), the
+// local max and compensated sum of exp(x - m); 16-bit (m, d)); every warp does
+// it, identically, so every CTA of the row holds bit-identical (m, 1/d).  The
+// slots are read through L2 (another CTA, or the previous launch, wrote them).
+template <int DT>
+__device__ __forceinline__ void merge_partials(const float4 *ws, int64_t r, int P, float &m, float &inv)
+{
+    const int lane = threadIdx.x & 31;
+    if constexpr (DT == kF32) {
+        float mloc = -INFINITY;
+        for (int i = lane; i < P; i += 32)
+            mloc = fmaxf(mloc, __ldcg(&ws[r * P + i]).x);
+        m = group_max<32>(mloc);
+        CSum acc{0.f, 0.f};
+        for (int i = lane; i < P; i += 32) {
+            const float4 q = __ldcg(&ws[r * P + i]);
+            if (q.x != -INFINITY) {
+                // one rescale per partial: (s + c) * exp(m_p - m), exp_shift keeps
+                // m_p - m exact
+                const float f = Math<kF32>::exp_shift(q.x, m);
+                Math<kF32>::add(acc, q.y * f);
+                Math<kF32>::add(acc, q.z * f);
+            }
+        }
+        acc = group_sum<kF32, 32>(acc);
+        inv = 1.0f / (acc.s + acc.c);
+    } else {
+        MD md{-INFINITY, 0.f};
+        for (int i = lane; i < P; i += 32) {
+            const float4 q = __ldcg(&ws[r * P + i]);
+            md = md_merge<DT>(md, MD{q.x, q.y});
+        }
+        md = warp_md<DT>(md);
+        m = md.m;
+        inv = 1.0f / md.d;
+    }
+}
+
 }  // namespace osd

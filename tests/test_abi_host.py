@@ -128,7 +128,7 @@ def _covers(p, rows, cols, elem, aligned):
         stage = p.smem_bytes // p.stages
         lead = 0 if aligned else 16 - elem
         return stage * 1 >= -(-(lead + p.rows_per_tile * cols * elem) // 16) * 16
-    return p.variant in (B.VARIANT_STREAM, B.VARIANT_SPLITK, B.VARIANT_SPLITK_WIDE)
+    return p.variant in (B.VARIANT_STREAM, B.VARIANT_SPLITK, B.VARIANT_SPLITK_WIDE, B.VARIANT_SPLITK_GRID)
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
@@ -146,12 +146,19 @@ def test_dispatch_of_workloads(lib, name):
         "attn_fp16_65536x512": B.VARIANT_ROWGROUP,
         "awkward_fp16_8192x5003": B.VARIANT_BLOCK,
         "vocab_bf16_32768x32000": B.VARIANT_BLOCK,
-        "splitk_fp32_4x4194304": B.VARIANT_SPLITK,
-        "splitk_fp16_4x4194304": B.VARIANT_SPLITK,
+        "splitk_fp32_4x4194304": B.VARIANT_SPLITK_GRID,
+        "splitk_fp16_4x4194304": B.VARIANT_SPLITK_GRID,
     }[name]
     assert p.variant == expect, B.softmax_variant_name(p.variant)
-    if p.variant == B.VARIANT_SPLITK:
-        assert p.cluster_x == 16 and p.grid_x == 16 and p.grid_y == w.rows
+    if p.variant == B.VARIANT_SPLITK_GRID:
+        # every SM: fp16 shares held in shared memory at one CTA per SM
+        # (38 CTAs x 4 rows, 220 KB each), fp32 streamed at two per SM
+        assert p.grid_y == w.rows and p.block_threads == 512 and p.cluster_x == 1
+        if w.dtype == "fp16":
+            need = -(-(w.cols * 2 // 16) // 38) * 16
+            assert p.stages == 1 and p.grid_x == 38 and need <= p.smem_bytes <= 232448 - 1024
+        else:
+            assert p.stages == 0 and p.smem_bytes == 0 and p.grid_x == 76
 
 
 @pytest.mark.parametrize("dt,elem", [(0, 4), (1, 2), (2, 2)])
@@ -181,9 +188,29 @@ def test_splitk_needs_clusters(lib):
     no_clusters = B.DeviceInfo(sm_count=152, max_smem_optin=232448, cluster_launch=0,
                                l2_bytes=1 << 27, cc_major=10, cc_minor=3)
     rc, p = B.softmax_plan(no_clusters, BASE, BASE + (1 << 36), 4, 1 << 22, 0)
-    assert rc == B.OK and p.variant == B.VARIANT_STREAM
+    assert rc == B.OK and p.variant == B.VARIANT_SPLITK_GRID  # the grid split needs no cluster
     rc, _ = B.softmax_plan(no_clusters, BASE, BASE + (1 << 36), 4, 1 << 22, 0, B.VARIANT_SPLITK)
     assert rc == B.ERR_UNSUPPORTED_SHAPE
+    # a GPU without cooperative launch of this kind: the stream kernel
+    old = B.DeviceInfo(sm_count=152, max_smem_optin=232448, cluster_launch=0, l2_bytes=1 << 27,
+                       cc_major=8, cc_minor=0)
+    rc, p = B.softmax_plan(old, BASE, BASE + (1 << 36), 4, 1 << 22, 0)
+    assert rc == B.OK and p.variant == B.VARIANT_STREAM
+
+
+def test_grid_split_limits(lib):
+    # few rows only (rows * 2 <= SMs); resident form only for 16-bit shares
+    # that fit shared memory
+    rc, _ = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 77, 1 << 20, 1, B.VARIANT_SPLITK_GRID)
+    assert rc == B.ERR_UNSUPPORTED_SHAPE
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 76, 1 << 20, 1, B.VARIANT_SPLITK_GRID)
+    assert rc == B.OK and p.grid_x * p.grid_y <= 152 * 2
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 1, 1 << 24, 1, B.VARIANT_SPLITK_GRID)
+    assert rc == B.OK and p.stages == 1 and p.grid_x == 152          # 32 MiB over 152 SMs
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 1, 1 << 25, 1, B.VARIANT_SPLITK_GRID)
+    assert rc == B.OK and p.stages == 0 and p.grid_x == 304          # 64 MiB: streamed
+    rc, p = B.softmax_plan(GB300, BASE + 2, BASE + (1 << 36) + 2, 3, (1 << 21) + 7, 2, B.VARIANT_SPLITK_GRID)
+    assert rc == B.OK and p.aligned == 0 and p.stages == 1
 
 
 def test_forced_variants_reject_rows_too_long(lib):
