@@ -91,8 +91,11 @@ typedef enum {
                                         only: it needs the workspace) */
     SOFTMAX_VARIANT_SPLITK_GRID = 7, /* P CTAs per row over all SMs in one cooperative launch,
                                         partials exchanged at a bounded per-row grid barrier
-                                        through library-owned scratch; fp16 / bf16 shares held
-                                        in shared memory (one HBM read) */
+                                        through library-owned scratch.  Ring form (stages >= 1):
+                                        grid_y groups of grid_x CTAs, one CTA per SM, a group
+                                        takes every grid_y-th row in turn, each CTA's share of
+                                        a row held in one of `stages` shared-memory buffers (one
+                                        HBM read); streaming form (stages 0): grid_y = rows */
     SOFTMAX_VARIANT_COUNT = 8
 } softmax_variant;
 
@@ -312,12 +315,14 @@ typedef struct {
     int chunks_per_thread;  /* 16-byte chunks each thread caches (ROWGROUP, BLOCK), or loads in
                                flight per thread per streaming step (STREAM, SPLITK); else 0 */
     int rows_per_tile;      /* BLOCK_TMA: consecutive rows moved by one bulk copy; else 0 */
-    int stages;             /* BLOCK_TMA: shared-memory tiles in flight per CTA; else 0 */
+    int stages;             /* BLOCK_TMA: shared-memory tiles in flight per CTA; SPLITK_GRID:
+                               ring buffers per CTA (0: streaming form); else 0 */
     int block_threads;      /* threads per CTA */
     int64_t grid_x;         /* CTAs along x */
-    int64_t grid_y;         /* CTAs along y (SPLITK: rows) */
+    int64_t grid_y;         /* CTAs along y (SPLITK: rows; SPLITK_GRID: row groups) */
     int cluster_x;          /* SPLITK: CTAs per cluster (= per row); else 1 */
-    int smem_bytes;         /* dynamic shared memory per CTA (BLOCK_TMA: stages x stage bytes) */
+    int smem_bytes;         /* dynamic shared memory per CTA (BLOCK_TMA, SPLITK_GRID ring form:
+                               stages x bytes per stage) */
     int aligned;            /* 1 if every row of x and y starts 16-byte aligned and is a whole
                                number of 16-byte chunks */
     int y_vector;           /* 1 if y rows share x rows' 16-byte phase (vector stores) */

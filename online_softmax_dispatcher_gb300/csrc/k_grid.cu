@@ -9,21 +9,25 @@
 // a merge) in one kernel, with the grid synchronisation that page set aside
 // made safe here by the cooperative launch (co-residency) and a bounded wait.
 //
-// * Resident form (fp16 / bf16 rows whose share fits shared memory, one CTA
-//   per SM): the CTA's segment is copied into shared memory by bulk copies in
-//   kGridPieces pieces, the online (m, d) pass starts on each piece as it
-//   lands, and after the barrier the output is computed from shared memory:
-//   x is read from HBM once.
-// * Streaming form (fp32, or longer shares; two CTAs per SM): the passes of
-//   the two-launch split (stream_passes.cuh) around the barrier; the write pass
-//   re-reads x, from L2 when the rows fit there.
+// * Ring form (a CTA's share of a row fits a shared-memory buffer; one CTA
+//   per SM): G groups of P CTAs; a group takes every G-th row in turn, each
+//   CTA holding share p of the row.  Shares pass through a ring of Q buffers
+//   filled by bulk copies (x is read from HBM once); the statistics of one
+//   row, the output of the row before it and the loads of the rows after it
+//   overlap.  The dispatcher takes as few rows per group as the buffers allow
+//   (one, when a share of 1/G of the SMs fits), since each row costs a CTA
+//   a fixed few microseconds in turn.
+// * Streaming form (shares too long for shared memory; two CTAs per SM, P
+//   per row): the passes of the two-launch split (stream_passes.cuh) around
+//   the barrier; the write pass re-reads x, from L2 when the rows fit there.
 // * Barrier: each row has two arrival counters used by alternate launches of a
 //   slot (the launch's generation number picks one); a CTA stores its
 //   partial, adds one to the launch's counter with release semantics and
 //   waits -- for at most kWaitLimitNs of %globaltimer time -- until an acquire
-//   load of it reads P.  The first CTA of each row zeroes the other counter,
-//   ready for the slot's next launch (the previous launch that used it has
-//   finished), so a launch that gave up leaves nothing stale behind.  A wait
+//   load of it reads P.  The first CTA zeroes the other parity's counters of
+//   every row the slot serves, ready for the slot's next launch whatever its
+//   row count (the previous launch that used them has finished), so a launch
+//   that gave up leaves nothing stale behind.  A wait
 //   that gives up records kErrGridWait in the library's device error word and
 //   the CTA returns without writing.
 // * Every CTA of a row merges the P partials in the same fixed order, so all
@@ -48,14 +52,17 @@
 namespace osd {
 
 constexpr unsigned kErrGridWait = 4u;  // waiting at a row's grid barrier
-constexpr int kGridPieces = 8;         // bulk copies per resident segment, consumed as they land
+constexpr int kGridPieces = 8;         // bulk copies per share in the ring form, consumed as they land
 
 struct GridArgs {
     const char *x;
     char *y;
     int64_t rows;
     int64_t cols;
-    int P;  // CTAs per row
+    int P;    // CTAs per row
+    int Q;    // ring form: shared-memory buffers (0: streaming form)
+    int buf;  // ring form: bytes per buffer
+    int lag;  // ring form: rows a CTA's output trails its statistics (1 when Q >= 2, else 0)
     int y_vec;
     float4 *part;      // [rows * P] partial statistics
     unsigned *arrive;  // [rows][2] arrival counters, one per launch parity
@@ -91,11 +98,14 @@ __device__ __forceinline__ bool grid_row_barrier(const GridArgs &a, int64_t r, i
     return true;
 }
 
-// Zero the row's counter of the slot's next launch (first CTA of the row).
-__device__ __forceinline__ void grid_prepare_next(const GridArgs &a, int64_t r, int p)
+// Zero the slot's counters of the other parity, for every row a slot serves
+// (not only this launch's rows: the slot's next launch may have more), so
+// that the next launch starts from zero.  The first CTA does it.
+__device__ __forceinline__ void grid_prepare_next(const GridArgs &a)
 {
-    if (p == 0 && threadIdx.x == 0)
-        a.arrive[2 * r + ((a.gen + 1u) & 1u)] = 0u;
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < kGridMaxRows; i += blockDim.x)
+            a.arrive[2 * i + ((a.gen + 1u) & 1u)] = 0u;
 }
 
 // The whole chunks [fb, fe) of CTA p's share [kb, ke) of row g (a partial
@@ -157,101 +167,268 @@ __device__ __forceinline__ void md_absorb(MD &md, const uint4 (&raw)[K])
     md.d += s;
 }
 
-template <int DT, bool ALIGNED>
-__global__ void __launch_bounds__(kGridThreads, 1) k_grid_resident(const GridArgs a)
+// merge_partials spread over the CTA: thread i loads partial i (all P in one
+// round trip through L2 rather than P / 32 dependent ones per warp), then the
+// block reductions combine them in a fixed order, so every CTA of the row holds
+// bit-identical (m, 1/d).  All threads call it.
+template <int DT>
+__device__ __forceinline__ void merge_partials_cta(const float4 *ws, int64_t r, int P, float &m, float &inv,
+                                                   float *smax, typename Math<DT>::Acc *ssum, MD *smd)
 {
-    pdl_enter();
-    constexpr int E = Fmt<DT>::kPerChunk;
-    constexpr int K = 4;  // chunks per thread per step
-    extern __shared__ __align__(128) unsigned char seg[];
-    __shared__ __align__(8) uint64_t bars[kGridPieces];
-    __shared__ MD smd[32];
-    __shared__ volatile int abort_flag;
-    const int64_t r = blockIdx.y;
-    const int p = blockIdx.x;
-    const int tid = threadIdx.x, T = blockDim.x;
-    const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, r, a.cols);
-    const Share sh = share_of<DT, ALIGNED>(g, a.cols, a.P, p, tid);
-    grid_prepare_next(a, r, p);
-    const int n = (int)(sh.fe - sh.fb);  // whole chunks held in shared memory
-    const int piece = (n + kGridPieces - 1) / kGridPieces;
-    const uint32_t seg0 = smem_u32(seg);
-
-    if (tid == 0) {
-        for (int i = 0; i < kGridPieces; i++)
-            mbar_init(smem_u32(&bars[i]), 1);
-        abort_flag = 0;
-        mbar_init_fence();
-        for (int i = 0; i < kGridPieces; i++) {
-            const int c0 = i * piece, cnt = n - c0 < piece ? n - c0 : piece;
-            if (cnt <= 0)
-                break;
-            mbar_arrive_expect_tx(smem_u32(&bars[i]), (uint32_t)(16 * cnt));
-            bulk_g2s(seg0 + 16u * (uint32_t)c0, g.x0 + 16 * (sh.fb + c0), (uint32_t)(16 * cnt), smem_u32(&bars[i]));
+    const int T = blockDim.x;
+    if constexpr (DT == kF32) {
+        float4 q[2];
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const int i = threadIdx.x + j * T;
+            q[j] = i < P ? __ldcg(&ws[r * P + i]) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
         }
+        float mloc = fmaxf(q[0].x, q[1].x);
+        for (int i = threadIdx.x + 2 * T; i < P; i += T)
+            mloc = fmaxf(mloc, __ldcg(&ws[r * P + i]).x);
+        m = block_max(mloc, smax);
+        CSum acc{0.f, 0.f};
+        auto add = [&](const float4 &v) {
+            if (v.x != -INFINITY) {
+                const float f = Math<kF32>::exp_shift(v.x, m);
+                Math<kF32>::add(acc, v.y * f);
+                Math<kF32>::add(acc, v.z * f);
+            }
+        };
+        add(q[0]);
+        add(q[1]);
+        for (int i = threadIdx.x + 2 * T; i < P; i += T)
+            add(__ldcg(&ws[r * P + i]));
+        acc = block_sum<kF32>(acc, ssum);
+        inv = 1.0f / (acc.s + acc.c);
+    } else {
+        MD md{-INFINITY, 0.f};
+        for (int i = threadIdx.x; i < P; i += T) {
+            const float4 v = __ldcg(&ws[r * P + i]);
+            md = md_merge<DT>(md, MD{v.x, v.y});
+        }
+        md = block_md<DT>(md, smd);
+        m = md.m;
+        inv = 1.0f / md.d;
     }
-    __syncthreads();
+}
 
-    const uint4 edge = sh.edge_k >= 0 ? load_chunk<DT, ALIGNED>(g, sh.edge_k, a.cols) : neg_inf_chunk<DT>();
-    MD md{-INFINITY, 0.f};
-    {
-        uint4 one[1] = {edge};
-        md_absorb<DT, 1>(md, one);
-    }
+// Load CTA p's share of row r (its whole chunks, n of them) into ring buffer
+// `dst` as kGridPieces bulk copies, one mbarrier each.  One thread.
+template <int DT, bool ALIGNED>
+__device__ __forceinline__ void grid_issue(const GridArgs &a, int64_t r, int p, uint32_t dst, uint32_t bar0)
+{
+    const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, r, a.cols);
+    const Share sh = share_of<DT, ALIGNED>(g, a.cols, a.P, p, 0);
+    const int n = (int)(sh.fe - sh.fb);
+    const int piece = (n + kGridPieces - 1) / kGridPieces;
+    // the buffer's previous contents were read through the generic proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     for (int i = 0; i < kGridPieces; i++) {
         const int c0 = i * piece, cnt = n - c0 < piece ? n - c0 : piece;
         if (cnt <= 0)
             break;
-        if (!mbar_wait(smem_u32(&bars[i]), 0, &abort_flag)) {
-            if (tid == 0 && !abort_flag) {
-                atomicOr(a.err, kErrFullWait);
-                abort_flag = 1;
-            }
-            break;
-        }
-        for (int c = c0 + tid; c < c0 + cnt; c += T * K) {
-            uint4 raw[K];
-#pragma unroll
-            for (int u = 0; u < K; u++) {
-                const int cc = c + u * T;
-                raw[u] = cc < c0 + cnt ? lds_chunk(seg0 + 16u * (uint32_t)cc) : neg_inf_chunk<DT>();
-            }
-            md_absorb<DT, K>(md, raw);
-        }
+        mbar_arrive_expect_tx(bar0 + 8u * i, (uint32_t)(16 * cnt));
+        bulk_g2s(dst + 16u * (uint32_t)c0, g.x0 + 16 * (sh.fb + c0), (uint32_t)(16 * cnt), bar0 + 8u * i);
     }
-    md = block_md<DT>(md, smd);
-    if (tid == 0 && !abort_flag && !grid_row_barrier(a, r, p, make_float4(md.m, md.d, 0.f, 0.f))) {
-        atomicOr(a.err, kErrGridWait);
-        abort_flag = 1;
+}
+
+// Store this CTA's partial of row r and count it in (release); one thread.
+__device__ __forceinline__ void grid_publish(const GridArgs &a, int64_t r, int p, float4 partial)
+{
+    a.part[r * a.P + p] = partial;
+    red_add_release_gpu(&a.arrive[2 * r + (a.gen & 1u)], 1u);
+}
+
+// Wait (bounded) until every CTA that shares row r has counted its partial in.
+__device__ __forceinline__ bool grid_wait_row(const GridArgs &a, int64_t r)
+{
+    const unsigned *cnt = &a.arrive[2 * r + (a.gen & 1u)];
+    const uint64_t t0 = global_ns();
+    while (ld_acquire_gpu(cnt) < (unsigned)a.P)
+        if (global_ns() - t0 > kWaitLimitNs)
+            return false;
+    return true;
+}
+
+// Ring form: the grid is G groups (blockIdx.y) of P CTAs (blockIdx.x), one CTA
+// per SM; group gy takes rows gy, gy + G, gy + 2G, ... and CTA p of the group
+// holds share p of each of them.  The shares pass through a ring of Q
+// shared-memory buffers filled by bulk copies, so x is read from HBM once.
+// Row k of the group: wait for its pieces, fold them into this CTA's partial
+// statistics and count it in at the row's barrier without waiting; then
+// (lagging one row behind when Q >= 2) wait at the previous row's barrier,
+// merge its P partials, write it from its buffer and refill that buffer with
+// the row Q places further on.  The loads of later rows, the statistics of
+// this one and the output of the one before overlap, and a row's barrier is
+// normally complete by the time a CTA asks for it.
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(kGridThreads, 1) k_grid_ring(const GridArgs a)
+{
+    pdl_enter();
+    using M = Math<DT>;
+    constexpr int E = Fmt<DT>::kPerChunk;
+    constexpr int K = 4;  // chunks per thread per step
+    extern __shared__ __align__(128) unsigned char seg[];
+    __shared__ __align__(8) uint64_t bars[kGridMaxRing * kGridPieces];
+    __shared__ int pending[kGridMaxRing];  // group row whose copies into a buffer are unawaited, or -1
+    __shared__ float smax[32];
+    __shared__ typename M::Acc ssum[32];
+    __shared__ MD smd[32];
+    __shared__ volatile int abort_flag;
+    const int p = blockIdx.x, gy = blockIdx.y, G = gridDim.y;
+    const int tid = threadIdx.x, T = blockDim.x;
+    const int Q = a.Q;
+    const int nr = a.rows > gy ? (int)((a.rows - gy + G - 1) / G) : 0;
+    const uint32_t seg0 = smem_u32(seg), bar0 = smem_u32(bars);
+    const int lag = a.lag;
+
+    grid_prepare_next(a);
+    if (tid == 0) {
+        for (int i = 0; i < Q * kGridPieces; i++)
+            mbar_init(bar0 + 8u * i, 1);
+        abort_flag = 0;
+        mbar_init_fence();
+        for (int b = 0; b < Q; b++) {
+            pending[b] = b < nr ? b : -1;
+            if (b < nr)
+                grid_issue<DT, ALIGNED>(a, gy + (int64_t)b * G, p, seg0 + (uint32_t)b * a.buf,
+                                        bar0 + 8u * kGridPieces * b);
+        }
     }
     __syncthreads();
-    if (abort_flag) {
-        // no copy may still be landing in shared memory when the CTA leaves
-        if (tid == 0)
-            for (int i = 0; i < kGridPieces && i * piece < n; i++)
-                (void)mbar_wait(smem_u32(&bars[i]), 0, &abort_flag, false);
-        __syncthreads();
-        return;
-    }
-    __threadfence();
-    float m, inv;
-    merge_partials<DT>(a.part, r, a.P, m, inv);
 
-    if (sh.edge_k >= 0) {
-        float f[E];
-        chunk_exp<DT>(edge, m, f);
+    for (int k = 0; k < nr + lag; k++) {
+        if (k < nr) {
+            // ---- statistics of row k
+            const int64_t r = gy + (int64_t)k * G;
+            const int b = k % Q;
+            const uint32_t par = (uint32_t)(k / Q) & 1u, buf = seg0 + (uint32_t)b * a.buf;
+            const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, r, a.cols);
+            const Share sh = share_of<DT, ALIGNED>(g, a.cols, a.P, p, tid);
+            const int n = (int)(sh.fe - sh.fb);
+            const int piece = (n + kGridPieces - 1) / kGridPieces;
+            const uint4 edge = sh.edge_k >= 0 ? load_chunk<DT, ALIGNED>(g, sh.edge_k, a.cols) : neg_inf_chunk<DT>();
+            float4 partial;
+            if constexpr (DT == kF32) {
+                // fp32: the share's max, then the compensated sum of exp(x - max)
+                bool ok = true;
+                for (int i = 0; i < kGridPieces && i * piece < n && ok; i++)
+                    ok = mbar_wait(bar0 + 8u * (kGridPieces * b + i), par, &abort_flag);
+                if (!ok) {
+                    if (!abort_flag)
+                        atomicOr(a.err, kErrFullWait);
+                    abort_flag = 1;
+                }
+                float mx = chunk_max<DT>(edge);
+                if (!abort_flag)
+                    for (int c = tid; c < n; c += T)
+                        mx = fmaxf(mx, chunk_max<DT>(lds_chunk(buf + 16u * (uint32_t)c)));
+                mx = block_max(mx, smax);
+                CSum acc{0.f, 0.f};
+                if (!abort_flag && mx != -INFINITY) {
+                    float f[E];
+                    chunk_exp<DT>(edge, mx, f);
 #pragma unroll
-        for (int e = 0; e < E; e++)
-            f[e] *= inv;
-        store_chunk<DT, ALIGNED>(g, sh.edge_k, a.cols, pack<DT>(f), a.y_vec != 0);
+                    for (int e = 0; e < E; e++)
+                        M::add(acc, f[e]);
+                    for (int c = tid; c < n; c += T) {
+                        chunk_exp<DT>(lds_chunk(buf + 16u * (uint32_t)c), mx, f);
+#pragma unroll
+                        for (int e = 0; e < E; e++)
+                            M::add(acc, f[e]);
+                    }
+                }
+                acc = block_sum<DT>(acc, ssum);
+                partial = make_float4(mx, acc.s, acc.c, 0.f);
+            } else {
+                // 16-bit: one online (m, d) pass, each piece as it lands
+                MD md{-INFINITY, 0.f};
+                {
+                    uint4 one[1] = {edge};
+                    md_absorb<DT, 1>(md, one);
+                }
+                for (int i = 0; i < kGridPieces && i * piece < n; i++) {
+                    if (!mbar_wait(bar0 + 8u * (kGridPieces * b + i), par, &abort_flag)) {
+                        if (!abort_flag)
+                            atomicOr(a.err, kErrFullWait);
+                        abort_flag = 1;
+                        break;
+                    }
+                    const int c0 = i * piece, c1 = n - c0 < piece ? n : c0 + piece;
+                    for (int c = c0 + tid; c < c1; c += T * K) {
+                        uint4 raw[K];
+#pragma unroll
+                        for (int u = 0; u < K; u++) {
+                            const int cc = c + u * T;
+                            raw[u] = cc < c1 ? lds_chunk(buf + 16u * (uint32_t)cc) : neg_inf_chunk<DT>();
+                        }
+                        md_absorb<DT, K>(md, raw);
+                    }
+                }
+                md = block_md<DT>(md, smd);
+                partial = make_float4(md.m, md.d, 0.f, 0.f);
+            }
+            // (the block reduction's barriers make a time-out seen by any thread seen by all)
+            if (abort_flag)
+                break;
+            if (tid == 0) {
+                pending[b] = -1;
+                grid_publish(a, r, p, partial);
+            }
+        }
+        if (k >= lag) {
+            // ---- output of row j = k - lag
+            const int j = k - lag;
+            const int64_t r = gy + (int64_t)j * G;
+            const int b = j % Q;
+            const uint32_t buf = seg0 + (uint32_t)b * a.buf;
+            if (tid == 0 && !grid_wait_row(a, r)) {
+                atomicOr(a.err, kErrGridWait);
+                abort_flag = 1;
+            }
+            __syncthreads();
+            if (abort_flag)
+                break;
+            // (thread 0's acquire and the barrier order the partials' loads)
+            float m, inv;
+            merge_partials_cta<DT>(a.part, r, a.P, m, inv, smax, ssum, smd);
+            const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, r, a.cols);
+            const Share sh = share_of<DT, ALIGNED>(g, a.cols, a.P, p, tid);
+            const int n = (int)(sh.fe - sh.fb);
+            if (sh.edge_k >= 0) {
+                float f[E];
+                chunk_exp<DT>(load_chunk<DT, ALIGNED>(g, sh.edge_k, a.cols), m, f);
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    f[e] *= inv;
+                store_chunk<DT, ALIGNED>(g, sh.edge_k, a.cols, pack<DT>(f), a.y_vec != 0);
+            }
+            for (int c = tid; c < n; c += T) {
+                float f[E];
+                chunk_exp<DT>(lds_chunk(buf + 16u * (uint32_t)c), m, f);
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    f[e] *= inv;
+                store_chunk<DT, ALIGNED>(g, sh.fb + c, a.cols, pack<DT>(f), a.y_vec != 0);
+            }
+            __syncthreads();  // buffer b is free
+            if (tid == 0 && j + Q < nr) {
+                pending[b] = j + Q;
+                grid_issue<DT, ALIGNED>(a, gy + (int64_t)(j + Q) * G, p, buf, bar0 + 8u * kGridPieces * b);
+            }
+        }
     }
-    for (int c = tid; c < n; c += T) {
-        float f[E];
-        chunk_exp<DT>(lds_chunk(seg0 + 16u * (uint32_t)c), m, f);
-#pragma unroll
-        for (int e = 0; e < E; e++)
-            f[e] *= inv;
-        store_chunk<DT, ALIGNED>(g, sh.fb + c, a.cols, pack<DT>(f), a.y_vec != 0);
+    if (abort_flag) {
+        if (tid == 0) {
+            // no copy may still be landing in shared memory when the CTA leaves
+            for (int b = 0; b < Q; b++)
+                if (pending[b] >= 0)
+                    for (int i = 0; i < kGridPieces; i++)
+                        (void)mbar_wait(bar0 + 8u * (kGridPieces * b + i), (uint32_t)(pending[b] / Q) & 1u,
+                                        &abort_flag, false);
+        }
+        __syncthreads();
     }
 }
 
@@ -270,7 +447,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) k_grid_stream(const GridArg
     const int64_t per = (g.nch + a.P - 1) / a.P;
     const int64_t kb = per * p < g.nch ? per * p : g.nch;
     const int64_t ke = kb + per < g.nch ? kb + per : g.nch;
-    grid_prepare_next(a, r, p);
+    grid_prepare_next(a);
     float4 out;
     if constexpr (DT == kF32) {
         const float m = block_max(pass_max<DT, ALIGNED, kWideStep>(g, kb, ke, a.cols), smax);
@@ -338,7 +515,7 @@ void pool_init(GridPool &pl)
 template <int DT, bool A, bool RES>
 int grid_launch_one(const Launch &l, const GridArgs &args)
 {
-    auto kern = RES ? &k_grid_resident<DT, A> : &k_grid_stream<DT, A>;
+    auto kern = RES ? &k_grid_ring<DT, A> : &k_grid_stream<DT, A>;
     if (RES) {
         // opt in once per device to the largest segment the planner gives this
         // kernel (the device's opt-in limit less the static shared memory)
@@ -379,7 +556,7 @@ int grid_launch_one(const Launch &l, const GridArgs &args)
 template <int DT>
 int grid_dt(const Launch &l, const GridArgs &args)
 {
-    const bool res = l.plan.stages == 1;
+    const bool res = l.plan.stages >= 1;
     if (l.plan.aligned)
         return res ? grid_launch_one<DT, true, true>(l, args) : grid_launch_one<DT, true, false>(l, args);
     return res ? grid_launch_one<DT, false, true>(l, args) : grid_launch_one<DT, false, false>(l, args);
@@ -410,7 +587,7 @@ int launch_grid(const Launch &l)
     std::call_once(pl.once, pool_init, std::ref(pl));  // device d is current here
     if (pl.status != cudaSuccess)
         return (int)pl.status;
-    if (l.plan.grid_y > kGridMaxRows || l.plan.grid_x * l.plan.grid_y > kGridMaxPartials)
+    if (l.rows > kGridMaxRows || l.plan.grid_x * l.rows > kGridMaxPartials || l.plan.stages > kGridMaxRing)
         return (int)cudaErrorInvalidValue;
     const unsigned s = pl.next.fetch_add(1, std::memory_order_relaxed) % kGridSlots;
     std::lock_guard<std::mutex> lock(pl.mu[s]);
@@ -420,7 +597,11 @@ int launch_grid(const Launch &l)
     if (pl.used[s] && pl.last[s] != st && (e = cudaStreamWaitEvent(st, pl.ev[s], 0)) != cudaSuccess)
         return (int)e;
     const unsigned gen = pl.gen[s] + 1u;
-    GridArgs args{(const char *)l.x, (char *)l.y, l.rows, l.cols, (int)l.plan.grid_x, l.plan.y_vector,
+    const int Q = l.plan.stages;
+    GridArgs args{(const char *)l.x, (char *)l.y, l.rows, l.cols, (int)l.plan.grid_x, Q,
+                  Q > 0 ? l.plan.smem_bytes / Q : 0,
+                  Q > 1 ? 1 : 0,
+                  l.plan.y_vector,
                   pl.part + (size_t)s * kGridMaxPartials, pl.arrive + (size_t)s * 2 * kGridMaxRows, gen,
                   l.dev_err};
     int rc;

@@ -20,8 +20,9 @@ constexpr int kWideStep = 4;            // the same for the wide split: 64 regis
 constexpr int kGridThreads = 512;       // SPLITK_GRID: CTA size (resident and streaming forms)
 constexpr int kGridSlots = 16;          // SPLITK_GRID: scratch slots (launches in flight at once)
 constexpr int kGridMaxRows = 128;       // SPLITK_GRID: rows a slot serves
-constexpr int kGridMaxPartials = 512;   // SPLITK_GRID: rows x CTAs per row a slot serves
-constexpr int kGridStaticSmem = 1024;   // SPLITK_GRID resident form: static shared memory, upper bound
+constexpr int kGridMaxPartials = 4096;  // SPLITK_GRID: rows x CTAs per row a slot serves
+constexpr int kGridMaxRing = 8;         // SPLITK_GRID ring form: shared-memory buffers
+constexpr int kGridStaticSmem = 2048;   // SPLITK_GRID ring form: static shared memory, upper bound
 constexpr int kMaxCluster = 16;         // non-portable cluster size limit
 constexpr int kSplitStages = 6;         // SPLITK: shared-memory ring depth
 constexpr int kSplitStageBytes = 32768; // SPLITK: bytes per stage (one bulk copy)

@@ -238,32 +238,55 @@ bool grid_possible(int64_t rows, const softmax_device_info &dev)
 void plan_grid(const Geometry &g, int64_t rows, const softmax_device_info &dev, softmax_launch_plan &p)
 {
     const int64_t budget = int64_t(dev.max_smem_optin) - kGridStaticSmem;
-    const int64_t p1 = dev.sm_count / rows;  // one CTA per SM
-    int64_t P = 0, smem = 0;
-    if (g.S == 2 && p1 >= 1 && p1 * rows <= kGridMaxPartials) {
-        const int64_t bytes = ceil_div(g.nch_max, p1) * 16;
-        if (bytes <= budget) {
-            P = p1;
-            smem = ceil_div(bytes, 128) * 128;
-            if (smem > budget)
-                smem = bytes;
-        }
-    }
-    if (P == 0) {
-        P = 2 * int64_t(dev.sm_count) / rows;
-        const int64_t by_work = g.nch_max / (int64_t(kGridThreads) * kWideStep);
-        if (P > by_work)
-            P = by_work;
-        if (P * rows > kGridMaxPartials)
-            P = kGridMaxPartials / rows;
-        if (P < 1)
-            P = 1;
+    // Ring form: G groups of P = SMs / G CTAs, one CTA per SM.  Each row a CTA
+    // takes in turn costs it a fixed ~5 us (its fold at one 512-thread CTA per
+    // SM, two block reductions, the release, the merge's round trip), so the
+    // plan takes the fewest rows per group for which a CTA's share of a row
+    // fits one buffer and the partials fit a scratch slot, and for that count
+    // the fewest groups (the most CTAs on a row: the smallest shares, the
+    // deepest ring).
+    int64_t P = 0, G = 0, buf = 0;
+    for (int64_t npg = 1; npg <= rows; npg++) {
+        const int64_t gg = ceil_div(rows, npg);
+        if (npg > 1 && ceil_div(rows, gg) != npg)
+            continue;  // the same group count as a smaller npg
+        const int64_t pp = int64_t(dev.sm_count) / gg;
+        if (pp < 1 || pp * rows > kGridMaxPartials)
+            continue;
+        const int64_t bb = ceil_div(ceil_div(g.nch_max, pp) * 16, 128) * 128;
+        if (bb > budget)
+            continue;
+        P = pp;
+        G = gg;
+        buf = bb;
+        break;
     }
     p.variant = SOFTMAX_VARIANT_SPLITK_GRID;
     p.chunks_per_thread = kWideStep;
     p.block_threads = kGridThreads;
-    p.stages = smem > 0 ? 1 : 0;
-    p.smem_bytes = (int)smem;
+    if (P > 0) {
+        int64_t Q = ceil_div(rows, G);
+        if (Q > budget / buf)
+            Q = budget / buf;
+        if (Q > kGridMaxRing)
+            Q = kGridMaxRing;
+        p.stages = (int)Q;
+        p.smem_bytes = (int)(Q * buf);
+        p.grid_x = P;
+        p.grid_y = G;
+        return;
+    }
+    // Streaming form: two CTAs per SM, P per row, no shared-memory copy
+    P = 2 * int64_t(dev.sm_count) / rows;
+    const int64_t by_work = g.nch_max / (int64_t(kGridThreads) * kWideStep);
+    if (P > by_work)
+        P = by_work;
+    if (P * rows > kGridMaxPartials)
+        P = kGridMaxPartials / rows;
+    if (P < 1)
+        P = 1;
+    p.stages = 0;
+    p.smem_bytes = 0;
     p.grid_x = P;
     p.grid_y = rows;
 }
@@ -357,17 +380,22 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
             return SOFTMAX_ERR_INVALID_ARG;
         return SOFTMAX_OK;
     case SOFTMAX_VARIANT_SPLITK_GRID: {
-        if (p.block_threads != kGridThreads || p.cluster_x != 1 || p.grid_y != rows || !grid_possible(rows, dev))
+        if (p.block_threads != kGridThreads || p.cluster_x != 1 || !grid_possible(rows, dev))
             return SOFTMAX_ERR_INVALID_ARG;
-        if (p.grid_x * p.grid_y > kGridMaxPartials || V != kWideStep)
+        if (p.grid_x < 1 || p.grid_x * rows > kGridMaxPartials || V != kWideStep)
             return SOFTMAX_ERR_INVALID_ARG;
-        if (p.stages == 1) {
-            // resident: one CTA per SM, the share in shared memory
-            const int64_t need = ceil_div(g.nch_max, p.grid_x) * 16;
-            if (g.S != 2 || p.grid_x * p.grid_y > dev.sm_count || p.smem_bytes < need ||
+        if (p.stages >= 1) {
+            // ring form: G groups of P CTAs, one CTA per SM, Q buffers that each
+            // hold a CTA's share of a row
+            if (p.stages > kGridMaxRing || p.grid_y < 1 || p.grid_y > rows ||
+                p.grid_x * p.grid_y > dev.sm_count || p.smem_bytes % p.stages != 0)
+                return SOFTMAX_ERR_INVALID_ARG;
+            const int64_t buf = p.smem_bytes / p.stages;
+            if (buf % 16 != 0 || buf < ceil_div(g.nch_max, p.grid_x) * 16 ||
                 p.smem_bytes > dev.max_smem_optin - kGridStaticSmem)
                 return SOFTMAX_ERR_INVALID_ARG;
-        } else if (p.stages != 0 || p.smem_bytes != 0 || p.grid_x * p.grid_y > 2 * int64_t(dev.sm_count)) {
+        } else if (p.stages != 0 || p.smem_bytes != 0 || p.grid_y != rows ||
+                   p.grid_x * p.grid_y > 2 * int64_t(dev.sm_count)) {
             return SOFTMAX_ERR_INVALID_ARG;
         }
         return SOFTMAX_OK;

@@ -151,14 +151,14 @@ def test_dispatch_of_workloads(lib, name):
     }[name]
     assert p.variant == expect, B.softmax_variant_name(p.variant)
     if p.variant == B.VARIANT_SPLITK_GRID:
-        # every SM: fp16 shares held in shared memory at one CTA per SM
-        # (38 CTAs x 4 rows, 220 KB each), fp32 streamed at two per SM
-        assert p.grid_y == w.rows and p.block_threads == 512 and p.cluster_x == 1
-        if w.dtype == "fp16":
-            need = -(-(w.cols * 2 // 16) // 38) * 16
-            assert p.stages == 1 and p.grid_x == 38 and need <= p.smem_bytes <= 232448 - 1024
-        else:
-            assert p.stages == 0 and p.smem_bytes == 0 and p.grid_x == 76
+        # ring form, one CTA per SM: fp16, one group of 38 CTAs per row (a
+        # 220 KB share each); fp32, two groups of 76 CTAs taking two rows each
+        # (220 KB shares, one buffer)
+        G = 4 if w.dtype == "fp16" else 2
+        P = 152 // G
+        assert p.grid_x == P and p.grid_y == G and p.block_threads == 512 and p.cluster_x == 1
+        buf = -(-(-(-(w.cols * w.elem_bytes // 16) // P) * 16) // 128) * 128
+        assert p.stages == 1 and p.smem_bytes == buf <= 232448 - 2048
 
 
 @pytest.mark.parametrize("dt,elem", [(0, 4), (1, 2), (2, 2)])
@@ -199,18 +199,27 @@ def test_splitk_needs_clusters(lib):
 
 
 def test_grid_split_limits(lib):
-    # few rows only (rows * 2 <= SMs); resident form only for 16-bit shares
-    # that fit shared memory
+    # few rows only (rows * 2 <= SMs); the ring form while a CTA's share of a
+    # row fits a buffer and rows x CTAs per row fit a scratch slot (4096)
     rc, _ = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 77, 1 << 20, 1, B.VARIANT_SPLITK_GRID)
     assert rc == B.ERR_UNSUPPORTED_SHAPE
     rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 76, 1 << 20, 1, B.VARIANT_SPLITK_GRID)
-    assert rc == B.OK and p.grid_x * p.grid_y <= 152 * 2
+    # 76 rows of 2 MiB: shares fit a buffer from 10 CTAs a row on, so 6 rows per
+    # group at least, and with 6, 13 groups of 11 CTAs
+    assert rc == B.OK and (p.grid_x, p.grid_y) == (11, 13) and p.stages == 1
+    assert p.smem_bytes == -(-(-(-(1 << 17) // 11) * 16) // 128) * 128
     rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 1, 1 << 24, 1, B.VARIANT_SPLITK_GRID)
-    assert rc == B.OK and p.stages == 1 and p.grid_x == 152          # 32 MiB over 152 SMs
+    assert rc == B.OK and p.stages == 1 and p.grid_x == 152 and p.grid_y == 1   # 32 MiB over 152 SMs
     rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 1, 1 << 25, 1, B.VARIANT_SPLITK_GRID)
-    assert rc == B.OK and p.stages == 0 and p.grid_x == 304          # 64 MiB: streamed
+    assert rc == B.OK and p.stages == 0 and p.grid_x == 304 and p.grid_y == 1   # 64 MiB: streamed
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 2, 1 << 24, 1, B.VARIANT_SPLITK_GRID)
+    assert rc == B.OK and p.stages == 1 and (p.grid_x, p.grid_y) == (152, 1)     # two rows, one buffer
     rc, p = B.softmax_plan(GB300, BASE + 2, BASE + (1 << 36) + 2, 3, (1 << 21) + 7, 2, B.VARIANT_SPLITK_GRID)
-    assert rc == B.OK and p.aligned == 0 and p.stages == 1
+    assert rc == B.OK and p.aligned == 0 and p.stages == 1 and (p.grid_x, p.grid_y) == (50, 3)
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 16, 1 << 20, 1, B.VARIANT_SPLITK_GRID)
+    # 16 rows of 2 MiB: 8 groups of 19 CTAs, two rows each through a ring of two buffers
+    assert rc == B.OK and (p.grid_x, p.grid_y, p.stages) == (19, 8, 2)
+
 
 
 def test_forced_variants_reject_rows_too_long(lib):

@@ -126,3 +126,71 @@ def test_grid_under_graph_capture_falls_back():
     torch.cuda.synchronize()
     check(torch_to_np(x, 1), torch_to_np(y, 1), 1)
     _no_device_error()
+
+
+def _grid_plan(rows, cols, dt, x_off=0, y_off=0):
+    rc, dev = osd.softmax_device_query()
+    assert rc == 0
+    e = {0: 4, 1: 2, 2: 2}[dt]
+    base = 1 << 40
+    rc, p = osd.softmax_plan(dev, base + x_off * e, base + (1 << 38) + y_off * e, rows, cols, dt, GRID)
+    assert rc == 0
+    return dev, p
+
+
+@pytest.mark.parametrize("dt", [0, 1, 2])
+def test_grid_ring_groups_and_depths(dt):
+    # hand-made ring plans: every CTA on every row (G = 1) with a ring of 1 to
+    # 4 buffers, two groups, one group per row; and plans the checks refuse
+    rng = np.random.default_rng(310 + dt)
+    rows, cols = 4, (1 << 20) + 3
+    x = rng.normal(0, 3, (rows, cols))
+    x[:, ::89] += 55.0
+    x = _quant(x, dt)
+    dev, p = _grid_plan(rows, cols, dt, 1, 1)
+    assert p.stages >= 1
+    S = dev.sm_count
+    budget = dev.max_smem_optin - 2048
+
+    def buf_for(P):
+        nch = (cols * {0: 4, 1: 2, 2: 2}[dt]) // 16 + 2
+        return -(-(-(-nch // P) * 16) // 128) * 128
+
+    good = []
+    for G, Q in ((1, 1), (1, 2), (1, 4), (2, 1), (2, 2), (4, 1)):
+        P = S // G
+        if Q * buf_for(P) <= budget:
+            good.append(dict(grid_x=P, grid_y=G, stages=Q, smem_bytes=Q * buf_for(P)))
+    assert len(good) >= 4
+    for ch in good:
+        q = osd.LaunchPlan(**{**p.as_dict(), **ch})
+        rc, y = run(x, dt, plan=q, x_off=1, y_off=1)
+        assert rc == 0, ch
+        check(x, y, dt)
+    bad = [dict(grid_y=rows + 1), dict(grid_x=S + 1, grid_y=1), dict(stages=9, smem_bytes=9 * 128),
+           dict(smem_bytes=(p.smem_bytes // p.stages // 32 * 16) * p.stages), dict(smem_bytes=p.smem_bytes + 8)]
+    for ch in bad:
+        q = osd.LaunchPlan(**{**p.as_dict(), **ch})
+        rc, _ = run(x, dt, plan=q, x_off=1, y_off=1)
+        assert rc == osd.ERR_INVALID_ARG, ch
+    _no_device_error()
+
+
+def test_grid_slot_reuse_with_changing_row_counts():
+    # blocks of 16 launches (one per scratch slot) with 7, then 3, then 7 rows:
+    # every slot's third launch finds counters its second launch had no rows for
+    torch.manual_seed(5)
+    xa = torch.randn(7, 1 << 20, device="cuda", dtype=torch.float16) * 5
+    xb = torch.randn(3, 1 << 20, device="cuda", dtype=torch.float16) * 5
+    assert osd.plan_for(xa, torch.empty_like(xa)).variant == GRID
+    assert osd.plan_for(xb, torch.empty_like(xb)).variant == GRID
+    outs = []
+    for i in range(64):
+        outs.append(osd.softmax(xb if (i // 16) % 2 else xa))
+    torch.cuda.synchronize()
+    check(torch_to_np(xa, 1), torch_to_np(outs[0], 1), 1)
+    check(torch_to_np(xb, 1), torch_to_np(outs[16], 1), 1)
+    for i, o in enumerate(outs):
+        ref = outs[16] if (i // 16) % 2 else outs[0]
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16)), i
+    _no_device_error()
