@@ -302,14 +302,38 @@ __global__ void __launch_bounds__(kRowgroupThreads) k_bwd_rowgroup(const BwdArgs
     }
 }
 
+// L2 prefetch (one bulk request) of the 16-byte granules holding bytes
+// [p, p + n) of a row: every granule holds a byte of the row, so all are
+// mapped.
+__device__ __forceinline__ void prefetch_row_l2(const char *p, int64_t n)
+{
+    const uintptr_t b = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(15);
+    const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + (uintptr_t)n + 15u) & ~uintptr_t(15);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b), "r"((uint32_t)(e - b)) : "memory");
+}
+
+// V = 8 (rows past 512 x 4 chunks, 128 registers a thread): one 512-thread CTA
+// per SM, whose loads stop while it reduces and writes; the grid is one CTA
+// per SM looping over rows, and each row starts by asking L2 for y and dy of
+// the CTA's next row, so HBM keeps streaming through those gaps and the next
+// row's loads hit L2.
 template <int DT, int V, int MODE>
 __global__ void __launch_bounds__(512, V >= 8 ? 1 : 2) k_bwd_block(const BwdArgs a)
 {
     pdl_enter();
     __shared__ CSum slots[32];
     constexpr int NE = MODE == kBwdFast ? 0 : 1;  // >= 32 threads: one edge element each at most
-    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
+    const int64_t row_bytes = a.cols * Fmt<DT>::kBytes;
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        if constexpr (V >= 8) {
+            const int64_t nx = r + gridDim.x;
+            if (threadIdx.x == 0 && nx < a.rows) {
+                prefetch_row_l2(a.y + nx * row_bytes, row_bytes);
+                prefetch_row_l2(a.dy + nx * row_bytes, row_bytes);
+            }
+        }
         bwd_row<DT, V, MODE, NE, true>(a, r, true, threadIdx.x, blockDim.x, CsumCta{slots});
+    }
 }
 
 template <int DT, bool ALIGNED>

@@ -626,7 +626,6 @@ int validate_bwd_args(const void *y, const void *dy, const void *dx, int64_t row
 int plan_bwd(const softmax_device_info &dev, const void *y, const void *dy, const void *dx, int64_t rows,
              int64_t cols, int dtype, int variant, softmax_launch_plan *plan, int *dy_vec, int *dx_vec)
 {
-    (void)dev;
     const Geometry g = geometry(y, dx, cols, dtype);
     const uintptr_t ya = reinterpret_cast<uintptr_t>(y), da = reinterpret_cast<uintptr_t>(dy);
     const bool aligned = g.aligned && da % 16 == 0;
@@ -671,6 +670,8 @@ int plan_bwd(const softmax_device_info &dev, const void *y, const void *dy, cons
         p.chunks_per_thread = V;
         p.block_threads = (int)T;
         p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
+        if (V == 8 && p.grid_x > dev.sm_count)
+            p.grid_x = dev.sm_count;  // one CTA per SM, looping (and prefetching) over rows
     } else if (v == SOFTMAX_VARIANT_STREAM) {
         p.variant = v;
         p.chunks_per_thread = 4;

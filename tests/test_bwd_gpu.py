@@ -74,8 +74,9 @@ def bwd_variants():
 
 @pytest.mark.parametrize("dt", [0, 1, 2])
 def test_bwd_shapes_and_variants(dt):
-    for cols in list(range(1, 34)) + [63, 64, 65, 255, 256, 512, 513, 1000, 2047, 2048, 2049, 5003, 16384,
-                                      32000, 40001]:
+    # (2049 .. 4096 chunks: the cluster-pair kernel for BLOCK)
+    for cols in list(range(1, 34)) + [63, 64, 65, 255, 256, 512, 513, 1000, 2047, 2048, 2049, 5003, 8193, 16384,
+                                      20000, 24577, 32000, 40001]:
         for rows in (1, 7):
             y, dy = make_case(rows, cols, dt, seed=cols * 10 + rows)
             for v in bwd_variants():
