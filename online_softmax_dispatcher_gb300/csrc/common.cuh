@@ -491,6 +491,16 @@ __device__ __forceinline__ uint4 mask_chunk(const uint4 &c, int64_t t0, int64_t 
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// L2 prefetch (one bulk request) of the 16-byte granules holding bytes
+// [p, p + n) of a row (n < 4 GiB): every granule holds a byte of the row, so
+// all are mapped.
+__device__ __forceinline__ void prefetch_row_l2(const char *p, int64_t n)
+{
+    const uintptr_t b = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(15);
+    const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + (uintptr_t)n + 15u) & ~uintptr_t(15);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b), "r"((uint32_t)(e - b)) : "memory");
+}
+
 // ---------------------------------------------------------------- exp and sums
 
 // 2^v on the SFU, subnormal results flushed to zero (one instruction).

@@ -302,16 +302,6 @@ __global__ void __launch_bounds__(kRowgroupThreads) k_bwd_rowgroup(const BwdArgs
     }
 }
 
-// L2 prefetch (one bulk request) of the 16-byte granules holding bytes
-// [p, p + n) of a row: every granule holds a byte of the row, so all are
-// mapped.
-__device__ __forceinline__ void prefetch_row_l2(const char *p, int64_t n)
-{
-    const uintptr_t b = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(15);
-    const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + (uintptr_t)n + 15u) & ~uintptr_t(15);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b), "r"((uint32_t)(e - b)) : "memory");
-}
-
 // V = 8 (rows past 512 x 4 chunks, 128 registers a thread): one 512-thread CTA
 // per SM, whose loads stop while it reduces and writes; the grid is one CTA
 // per SM looping over rows, and each row starts by asking L2 for y and dy of
