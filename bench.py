@@ -188,10 +188,13 @@ def gpu_id_for_nvsmi() -> str | None:
 def kernel_fingerprint(variant: str) -> str:
     """Hash of the sources the dominant kernel is built from (invalidates stale ncu traffic)."""
     csrc = os.path.join(ROOT, "online_softmax_dispatcher_gb300", "csrc")
-    files = {"rowgroup": "k_rowgroup.cuh", "block": "k_block.cu", "block_tma": "k_tma.cu",
-             "stream": "k_stream.cu", "splitk": "k_splitk.cu", "layernorm": "k_norm.cuh", "rmsnorm": "k_norm.cuh"}
+    files = {"rowgroup": ("k_rowgroup.cuh",), "block": ("k_block.cu",), "block_tma": ("k_tma.cu",),
+             "stream": ("k_stream.cu", "stream_passes.cuh"), "splitk": ("k_splitk.cu",),
+             "splitk_grid": ("k_grid.cu", "stream_passes.cuh"), "splitk_wide": ("k_wide.cu", "stream_passes.cuh"),
+             "layernorm": ("k_norm.cuh",), "rmsnorm": ("k_norm.cuh",), "backward": ("k_bwd.cu",),
+             "masked": ("k_masked.cu",)}
     h = hashlib.sha256()
-    for name in (files.get(variant, ""), "common.cuh", "tma.cuh", "launch.h"):
+    for name in files.get(variant, ()) + ("common.cuh", "tma.cuh", "launch.h"):
         p = os.path.join(csrc, name)
         if name and os.path.exists(p):
             h.update(open(p, "rb").read())
@@ -200,7 +203,9 @@ def kernel_fingerprint(variant: str) -> str:
 
 def recorded_traffic(workload: str, variant: str, plan: dict) -> tuple[float | None, str]:
     """dram bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel source with the same launch plan."""
+    current kernel source with the same launch plan.  `workload` is the record's
+    key: the workload's name for its default forward softmax, name:op for the
+    other operations (name:ws for the forward with a workspace)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -320,7 +325,10 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         gp = gt.data_ptr() if gt is not None else 0
         bp = bt.data_ptr() if bt is not None else 0
         variant = "layernorm" if w.kind == 0 else "rmsnorm"
-        plan = osd.LaunchPlan()
+        rc, plan = osd.norm_plan(osd.softmax_device_query()[1], w.kind, ptrs[0][0], ptrs[0][1], rows, cols, dt,
+                                 gp, bp)
+        if rc != 0:
+            raise osd.SoftmaxError(rc)
         ln, rms = osd.lib().layernorm_fwd, osd.lib().rmsnorm_fwd
 
         def step(i):
@@ -347,7 +355,9 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         set_bytes = set_bytes // 2 * 3
         bwd = osd.lib().softmax_bwd
         variant = "backward"
-        plan = osd.LaunchPlan()
+        rc, plan = osd.softmax_bwd_plan(osd.softmax_device_query()[1], *ptrs3[0], rows, cols, dt)
+        if rc != 0:
+            raise osd.SoftmaxError(rc)
         api_inputs = [ys[0].cpu().pin_memory(), dys[0].cpu().pin_memory()]
 
         def api(dev_in, out, i=0):
@@ -362,7 +372,9 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         masked = osd.lib().softmax_fwd_masked
         causal_q = min(512, rows)
         variant = "masked"
-        plan = osd.LaunchPlan()
+        rc, plan = osd.softmax_masked_plan(osd.softmax_device_query()[1], ptrs[0][0], ptrs[0][1], rows, cols, dt)
+        if rc != 0:
+            raise osd.SoftmaxError(rc)
 
         def api(dev_in, out, i=0):
             osd.softmax_masked(dev_in[0].view(-1, causal_q, cols), scale=0.125, causal=True,
@@ -475,7 +487,8 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     peaks = load_peaks()
     per_launch_ms = ms / args.steps
     achieved = set_bytes / (per_launch_ms / 1e3) / 1e9
-    traffic, tsrc = recorded_traffic(w.name, variant, plan.as_dict())
+    rec_key = f"{w.name}:ws" if args.workspace else (w.name if args.op == "forward" else f"{w.name}:{args.op}")
+    traffic, tsrc = recorded_traffic(rec_key, variant, plan.as_dict())
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,

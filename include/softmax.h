@@ -351,6 +351,24 @@ int softmax_fwd_plan(const void *x, void *y, int64_t rows, int64_t cols, int dty
 int softmax_plan(const softmax_device_info *dev, const void *x, const void *y, int64_t rows,
                  int64_t cols, int dtype, int variant, softmax_launch_plan *plan);
 
+/*
+ * softmax_bwd_plan / softmax_masked_plan / norm_plan -- the dispatchers of
+ * softmax_bwd_variant, softmax_fwd_masked_variant and norm_fwd_variant as pure
+ * host functions, like softmax_plan: the plan those calls would launch for
+ * these arguments on a device described by *dev (the mask, scale, causal cut,
+ * eps and the mean / rstd outputs do not change the plan and are not taken).
+ * Arguments are validated as the launching calls validate them; pointers are
+ * only inspected for their addresses.  rows == 0 or cols == 0 gives OK and a
+ * zeroed plan.  Makes no CUDA call.
+ */
+int softmax_bwd_plan(const softmax_device_info *dev, const void *y, const void *dy, const void *dx,
+                     int64_t rows, int64_t cols, int dtype, int variant, softmax_launch_plan *plan);
+int softmax_masked_plan(const softmax_device_info *dev, const void *x, const void *y, int64_t rows,
+                        int64_t cols, int dtype, int variant, softmax_launch_plan *plan);
+int norm_plan(const softmax_device_info *dev, int kind, const void *x, const void *y, int64_t rows,
+              int64_t cols, int dtype, const void *gamma, const void *beta, int variant,
+              softmax_launch_plan *plan);
+
 /* softmax_device_query -- fill *dev for the current CUDA device (cached). */
 int softmax_device_query(softmax_device_info *dev);
 

@@ -18,6 +18,6 @@ from ._binding import (  # noqa: F401
     softmax_workspace_size, softmax_fwd_noalloc, softmax_fwd_masked, softmax_fwd_masked_variant,
     softmax_masked, softmax_, layernorm_fwd, rmsnorm_fwd, norm_fwd_variant, layer_norm, rms_norm,
     LAYERNORM, RMSNORM, ERR_INVALID_ARG, ERR_UNSUPPORTED_DTYPE, ERR_ALIAS, ERR_CUDA, ERR_UNSUPPORTED_SHAPE,
-    ERR_DEVICE_TIMEOUT,
+    ERR_DEVICE_TIMEOUT, softmax_bwd_plan, softmax_masked_plan, norm_plan,
     softmax_strerror, softmax_variant_name,
 )

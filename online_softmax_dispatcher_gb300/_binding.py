@@ -48,7 +48,7 @@ EXPORTS = (
     "softmax_last_cuda_error", "softmax_strerror", "softmax_variant_name", "softmax_abi_version",
     "softmax_selftest_bounded_wait", "softmax_bwd", "softmax_bwd_variant", "softmax_fwd_ws",
     "softmax_workspace_size", "softmax_fwd_noalloc", "softmax_fwd_masked", "softmax_fwd_masked_variant",
-    "layernorm_fwd", "rmsnorm_fwd", "norm_fwd_variant",
+    "layernorm_fwd", "rmsnorm_fwd", "norm_fwd_variant", "softmax_bwd_plan", "softmax_masked_plan", "norm_plan",
 )
 LAYERNORM, RMSNORM = 0, 1
 
@@ -122,6 +122,12 @@ def lib() -> ctypes.CDLL:
                 "layernorm_fwd": [vp, vp, i64, i64, i32, vp, vp, ctypes.c_float, vp, vp, vp],
                 "rmsnorm_fwd": [vp, vp, i64, i64, i32, vp, ctypes.c_float, vp, vp],
                 "norm_fwd_variant": [i32, vp, vp, i64, i64, i32, vp, vp, ctypes.c_float, vp, vp, i32, vp],
+                "softmax_bwd_plan": [ctypes.POINTER(DeviceInfo), vp, vp, vp, i64, i64, i32, i32,
+                                     ctypes.POINTER(LaunchPlan)],
+                "softmax_masked_plan": [ctypes.POINTER(DeviceInfo), vp, vp, i64, i64, i32, i32,
+                                        ctypes.POINTER(LaunchPlan)],
+                "norm_plan": [ctypes.POINTER(DeviceInfo), i32, vp, vp, i64, i64, i32, vp, vp, i32,
+                              ctypes.POINTER(LaunchPlan)],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -213,6 +219,28 @@ def softmax_plan(dev: DeviceInfo, x: int, y: int, rows: int, cols: int, dtype: i
                  variant: int = VARIANT_AUTO) -> tuple[int, LaunchPlan]:
     p = LaunchPlan()
     rc = lib().softmax_plan(ctypes.byref(dev), x, y, rows, cols, dtype, variant, ctypes.byref(p))
+    return rc, p
+
+
+def softmax_bwd_plan(dev: DeviceInfo, y: int, dy: int, dx: int, rows: int, cols: int, dtype: int,
+                     variant: int = VARIANT_AUTO) -> tuple[int, LaunchPlan]:
+    p = LaunchPlan()
+    rc = lib().softmax_bwd_plan(ctypes.byref(dev), y, dy, dx, rows, cols, dtype, variant, ctypes.byref(p))
+    return rc, p
+
+
+def softmax_masked_plan(dev: DeviceInfo, x: int, y: int, rows: int, cols: int, dtype: int,
+                        variant: int = VARIANT_AUTO) -> tuple[int, LaunchPlan]:
+    p = LaunchPlan()
+    rc = lib().softmax_masked_plan(ctypes.byref(dev), x, y, rows, cols, dtype, variant, ctypes.byref(p))
+    return rc, p
+
+
+def norm_plan(dev: DeviceInfo, kind: int, x: int, y: int, rows: int, cols: int, dtype: int, gamma: int = 0,
+              beta: int = 0, variant: int = VARIANT_AUTO) -> tuple[int, LaunchPlan]:
+    p = LaunchPlan()
+    rc = lib().norm_plan(ctypes.byref(dev), kind, x, y, rows, cols, dtype, gamma or None, beta or None, variant,
+                         ctypes.byref(p))
     return rc, p
 
 

@@ -771,3 +771,59 @@ extern "C" __attribute__((visibility("default"))) int softmax_plan(
     *plan = p;
     return SOFTMAX_OK;
 }
+
+// The dispatchers of the other operations as pure host functions (no CUDA
+// call): the plan softmax_bwd_variant / softmax_fwd_masked_variant /
+// norm_fwd_variant would launch on a device described by *dev.
+extern "C" __attribute__((visibility("default"))) int softmax_bwd_plan(
+    const softmax_device_info *dev, const void *y, const void *dy, const void *dx, int64_t rows, int64_t cols,
+    int dtype, int variant, softmax_launch_plan *plan)
+{
+    if (!dev || !plan)
+        return SOFTMAX_ERR_INVALID_ARG;
+    int rc = validate_bwd_args(y, dy, dx, rows, cols, dtype);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (variant < SOFTMAX_VARIANT_AUTO || variant >= SOFTMAX_VARIANT_COUNT)
+        return SOFTMAX_ERR_INVALID_ARG;
+    *plan = softmax_launch_plan{};
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    int dy_vec = 0, dx_vec = 0;
+    return plan_bwd(*dev, y, dy, dx, rows, cols, dtype, variant, plan, &dy_vec, &dx_vec);
+}
+
+extern "C" __attribute__((visibility("default"))) int softmax_masked_plan(
+    const softmax_device_info *dev, const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
+    int variant, softmax_launch_plan *plan)
+{
+    if (!dev || !plan)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int rc = validate_args(x, y, rows, cols, dtype);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (variant < SOFTMAX_VARIANT_AUTO || variant >= SOFTMAX_VARIANT_COUNT)
+        return SOFTMAX_ERR_INVALID_ARG;
+    *plan = softmax_launch_plan{};
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    return plan_masked(*dev, x, y, rows, cols, dtype, variant, plan);
+}
+
+extern "C" __attribute__((visibility("default"))) int norm_plan(
+    const softmax_device_info *dev, int kind, const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
+    const void *gamma, const void *beta, int variant, softmax_launch_plan *plan)
+{
+    if (!dev || !plan)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int rc = validate_norm_args(kind, x, y, rows, cols, dtype, gamma, beta, 1e-5f, nullptr, nullptr);
+    if (rc != SOFTMAX_OK)
+        return rc;
+    if (variant < SOFTMAX_VARIANT_AUTO || variant >= SOFTMAX_VARIANT_COUNT)
+        return SOFTMAX_ERR_INVALID_ARG;
+    *plan = softmax_launch_plan{};
+    if (rows == 0 || cols == 0)
+        return SOFTMAX_OK;
+    int mode = 0;
+    return plan_norm(*dev, kind, x, y, rows, cols, dtype, gamma, beta, variant, plan, &mode);
+}

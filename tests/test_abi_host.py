@@ -10,6 +10,7 @@ import pytest
 
 from online_softmax_dispatcher_gb300 import _binding as B
 from online_softmax_dispatcher_gb300 import build as build_mod
+from online_softmax_dispatcher_gb300 import workloads as W
 from online_softmax_dispatcher_gb300.workloads import WORKLOADS
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "softmax.h")
@@ -270,3 +271,40 @@ def test_norm_argument_validation(lib):
     assert f(0, x, y, 0, 64, 0, 0, 0, 1e-5, 0, 0, 0, 0) == B.OK                       # empty: no launch
     assert B.layernorm_fwd(x, y, 8, 64, 7, 0, 0, 1e-5, 0, 0, 0) == B.ERR_UNSUPPORTED_DTYPE
     assert B.rmsnorm_fwd(x, y, 8, 64, 0, g + 2, 1e-5, 0, 0) == B.ERR_INVALID_ARG
+
+
+def test_other_operations_dispatch(lib):
+    # the backward, masked and normalisation dispatchers as host functions
+    y, dy, dx = BASE, BASE + (1 << 36), BASE + (2 << 36)
+    expect_bwd = {"attn_fp16_65536x512": (B.VARIANT_ROWGROUP, None), "awkward_fp16_8192x5003": (B.VARIANT_BLOCK, 4),
+                  "vocab_bf16_32768x32000": (B.VARIANT_BLOCK, 8)}
+    for name, (v, V) in expect_bwd.items():
+        w = W.WORKLOADS[name]
+        rc, p = B.softmax_bwd_plan(GB300, y, dy, dx, w.rows, w.cols, w.dtype_code)
+        assert rc == B.OK and p.variant == v, name
+        if V is not None:
+            assert p.chunks_per_thread == V
+            assert p.block_threads * V >= -(-w.cols * w.elem_bytes // 16)
+        if V == 8:
+            # one 512-thread CTA per SM: the grid is one CTA per SM, looping over rows
+            assert p.grid_x == 152 and p.block_threads == 512
+    rc, p = B.softmax_masked_plan(GB300, BASE, BASE + (1 << 36), 65536, 512, 1)
+    assert rc == B.OK and p.variant == B.VARIANT_ROWGROUP
+    for name, (v, G, V) in {"ln_fp16_131040x192": (B.VARIANT_ROWGROUP, 8, 3),
+                            "ln_fp16_32760x384": (B.VARIANT_ROWGROUP, 16, 3),
+                            "rms_bf16_16384x4096": (B.VARIANT_BLOCK, 0, 4)}.items():
+        w = W.NORM_WORKLOADS[name]
+        rc, p = B.norm_plan(GB300, w.kind, BASE, BASE + (1 << 36), w.rows, w.cols, w.dtype_code)
+        assert rc == B.OK and p.variant == v and p.chunks_per_thread == V, (name, p.as_dict())
+        if G:
+            assert p.lanes_per_row == G
+    # arguments are checked as the launching calls check them
+    assert lib.softmax_bwd_plan(None, y, dy, dx, 2, 3, 0, 0, None) == B.ERR_INVALID_ARG
+    rc, _ = B.softmax_bwd_plan(GB300, y, dy, dx, 2, 3, 7)
+    assert rc == B.ERR_UNSUPPORTED_DTYPE
+    rc, _ = B.softmax_masked_plan(GB300, BASE, BASE + 4, 2, 3, 0)
+    assert rc == B.ERR_ALIAS
+    rc, _ = B.norm_plan(GB300, 5, BASE, BASE + (1 << 36), 2, 3, 0)
+    assert rc == B.ERR_INVALID_ARG
+    rc, p = B.norm_plan(GB300, 0, BASE, BASE + (1 << 36), 0, 3, 0)
+    assert rc == B.OK and p.grid_x == 0
