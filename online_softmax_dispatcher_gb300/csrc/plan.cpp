@@ -110,11 +110,18 @@ void plan_block(const Geometry &g, int64_t rows, softmax_launch_plan &p)
     // loads in flight per thread, fewer reduction rounds per element), else 4;
     // raised to 16 when the CTA would pass 256 threads, so that several CTAs --
     // several rows -- stay resident per SM and one's loads overlap another's
-    // reductions.  Measured: [8192, 5003] fp16 runs fastest at V = 8 x 96
-    // threads, [32768, 32000] bf16 at V = 16 x 256 (V = 8 x 512 is slower).
+    // reductions.  Back to 4 when 8 leaves more than a tenth of the CTA's
+    // chunk slots idle and 4 leaves fewer (16-bit rows then also keep
+    // exp(x - m) instead of computing it twice).  Measured: [8192, 5003] fp16
+    // (625 interior chunks) at V = 4 x 160 threads 86.3 %, at 8 x 96 84.0 %;
+    // [8192, 6000] (750) at 8 x 96 94.8 %, at 4 x 192 91.7 %; [32768, 32000]
+    // bf16 at V = 16 x 256 (V = 8 x 512 is slower).
+    const auto slots = [&](int v) { return ceil_div(ceil_div(g.nint, v), 32) * 32 * v; };
     int V = ceil_div(g.nint, 8) >= 64 ? 8 : 4;
     while (V < kBlockMaxChunks && ceil_div(g.nint, V) > 256)
         V *= 2;
+    if (V == 8 && (slots(8) - g.nint) * 10 > slots(8) && slots(4) < slots(8))
+        V = 4;
     int64_t threads = ceil_div(ceil_div(g.nint, V), 32) * 32;
     if (threads < 64)
         threads = 64;
