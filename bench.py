@@ -404,6 +404,23 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
             rc = fwd_ws(xp, yp, rows, cols, dt, wp, need, s)
             if rc != 0:
                 raise osd.SoftmaxError(rc)
+    elif args.variant is not None:
+        vcode = osd.VARIANTS[args.variant]
+        rc, plan = osd.softmax_plan(osd.softmax_device_query()[1], ptrs[0][0], ptrs[0][1], rows, cols, dt, vcode)
+        if rc != 0:
+            return {"metric": METRIC, "impl": "ours", "unsupported": f"variant {args.variant}: "
+                    f"{osd.softmax_strerror(rc)}", "config": {"workload": w.name, "variant": args.variant}}
+        variant = args.variant
+        fwd_v = osd.lib().softmax_fwd_variant
+
+        def api(dev_in, out, i=0):
+            osd.softmax(dev_in[0], out=out, variant=args.variant)
+
+        def step(i):
+            xp, yp = ptrs[i % nbuf]
+            rc = fwd_v(xp, yp, rows, cols, dt, vcode, s)
+            if rc != 0:
+                raise osd.SoftmaxError(rc)
     else:
         def step(i):
             xp, yp = ptrs[i % nbuf]
@@ -566,8 +583,14 @@ def main():
     ap.add_argument("--workspace", action="store_true",
                     help="forward through softmax_fwd_ws with a workspace the bench allocates (lets few, very "
                          "long rows use every SM)")
+    ap.add_argument("--variant", default=None,
+                    help="forward only: force this kernel (rowgroup, block, block_tma, stream, splitk, "
+                         "splitk_grid) through softmax_fwd_variant instead of the dispatcher's choice; a variant "
+                         "that cannot serve the shape prints an 'unsupported' line and exits 0")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.variant is not None and (args.op != "forward" or args.workspace):
+        ap.error("--variant applies to the forward softmax without --workspace")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, ws, _ = dist_setup(args.gpus)
