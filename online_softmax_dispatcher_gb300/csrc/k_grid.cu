@@ -155,16 +155,17 @@ __device__ __forceinline__ void md_absorb(MD &md, const uint4 (&raw)[K])
         md.d = md.m == -INFINITY ? 0.f : md.d * M::exp_of(md.m - mt);
         md.m = mt;
     }
-    float s = 0.f;
+    // four partial sums: a dependency chain of K * E / 4 additions, not K * E
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < K; u++) {
         float f[E];
         chunk_exp<DT>(raw[u], md.m, f);
 #pragma unroll
         for (int e = 0; e < E; e++)
-            s += f[e];
+            s[e & 3] += f[e];
     }
-    md.d += s;
+    md.d += (s[0] + s[1]) + (s[2] + s[3]);
 }
 
 // merge_partials spread over the CTA: thread i loads partial i (all P in one
@@ -321,26 +322,41 @@ __global__ void __launch_bounds__(kGridThreads, 1) k_grid_ring(const GridArgs a)
                     abort_flag = 1;
                 }
                 float mx = chunk_max<DT>(edge);
-                if (!abort_flag)
-                    for (int c = tid; c < n; c += T)
+                if (!abort_flag) {
+                    float mx2 = -INFINITY;
+                    int c = tid;
+                    for (; c + T < n; c += 2 * T) {
                         mx = fmaxf(mx, chunk_max<DT>(lds_chunk(buf + 16u * (uint32_t)c)));
+                        mx2 = fmaxf(mx2, chunk_max<DT>(lds_chunk(buf + 16u * (uint32_t)(c + T))));
+                    }
+                    if (c < n)
+                        mx = fmaxf(mx, chunk_max<DT>(lds_chunk(buf + 16u * (uint32_t)c)));
+                    mx = fmaxf(mx, mx2);
+                }
                 mx = block_max(mx, smax);
-                CSum acc{0.f, 0.f};
+                // one compensated accumulator per slot of a chunk: E independent
+                // dependency chains, merged in a fixed order
+                CSum acc[E];
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    acc[e] = M::zero();
                 if (!abort_flag && mx != -INFINITY) {
                     float f[E];
                     chunk_exp<DT>(edge, mx, f);
 #pragma unroll
                     for (int e = 0; e < E; e++)
-                        M::add(acc, f[e]);
+                        M::add(acc[e], f[e]);
+#pragma unroll 2
                     for (int c = tid; c < n; c += T) {
                         chunk_exp<DT>(lds_chunk(buf + 16u * (uint32_t)c), mx, f);
 #pragma unroll
                         for (int e = 0; e < E; e++)
-                            M::add(acc, f[e]);
+                            M::add(acc[e], f[e]);
                     }
                 }
-                acc = block_sum<DT>(acc, ssum);
-                partial = make_float4(mx, acc.s, acc.c, 0.f);
+                CSum tot = M::merge(M::merge(acc[0], acc[1]), M::merge(acc[2], acc[3]));
+                tot = block_sum<DT>(tot, ssum);
+                partial = make_float4(mx, tot.s, tot.c, 0.f);
             } else {
                 // 16-bit: one online (m, d) pass, each piece as it lands
                 MD md{-INFINITY, 0.f};
@@ -404,6 +420,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) k_grid_ring(const GridArgs a)
                     f[e] *= inv;
                 store_chunk<DT, ALIGNED>(g, sh.edge_k, a.cols, pack<DT>(f), a.y_vec != 0);
             }
+#pragma unroll 4
             for (int c = tid; c < n; c += T) {
                 float f[E];
                 chunk_exp<DT>(lds_chunk(buf + 16u * (uint32_t)c), m, f);
