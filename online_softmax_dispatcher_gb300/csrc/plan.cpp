@@ -86,7 +86,12 @@ void plan_rowgroup(const Geometry &g, int64_t rows, const softmax_device_info &d
         G = next_pow2(n);
         V = 1;
     } else {
-        const int64_t vt = kRowgroupMaxFloats / g.E;
+        // chunks per lane: up to 32 floats' worth (8 fp32 / 4 16-bit chunks),
+        // but 2 for 16-bit rows of 17 - 64 chunks: twice the lanes on a row
+        // measured faster there ([65536, 512] fp16: 32 x 2 at 94.7 %, 16 x 4
+        // at 93.4 %; 256 columns +0.8 points; 128 columns -0.6 points, so
+        // those stay at 4)
+        const int64_t vt = (g.E == 8 && n > 16) ? 2 : kRowgroupMaxFloats / g.E;
         G = next_pow2(ceil_div(n, vt));
         if (G < 2)
             G = 2;
@@ -94,10 +99,11 @@ void plan_rowgroup(const Geometry &g, int64_t rows, const softmax_device_info &d
             G = 32;
         V = next_pow2(ceil_div(n, G));
     }
-    // 256-thread CTAs, halved (down to one warp) while that leaves SMs idle:
-    // few rows then spread over more SMs ([128, 1000] fp32: 16 CTAs of 8 rows
-    // each ran at 284 - 301 GB/s, one 64-thread CTA a row at 344 GB/s)
-    int64_t T = kRowgroupThreads;
+    // 128-thread CTAs (measured 0.3 - 0.6 points above 256 on 128 - 1024
+    // column rows), halved (down to one warp) while that leaves SMs idle: few
+    // rows then spread over more SMs ([128, 1000] fp32: 16 CTAs of 8 rows each
+    // ran at 284 - 301 GB/s, one 64-thread CTA a row at 344 GB/s)
+    int64_t T = kRowgroupThreads / 2;
     while (T / 2 >= (G > 32 ? G : 32) && ceil_div(rows, T / G) < dev.sm_count)
         T /= 2;
     p.variant = SOFTMAX_VARIANT_ROWGROUP;
