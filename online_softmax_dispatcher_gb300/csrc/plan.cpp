@@ -462,14 +462,18 @@ int plan_masked(const softmax_device_info &dev, const void *x, const void *y, in
     if (v == SOFTMAX_VARIANT_ROWGROUP) {
         if (!rg_fits)
             return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
-        int64_t G = n <= 4 ? next_pow2(n) : next_pow2(ceil_div(n, 4));
+        // as the forward: 2 chunks a lane for 16-bit rows of 17 - 64 chunks,
+        // 128-thread CTAs (measured on the attention workload with scale 1/8
+        // and a causal cut: 93.6 % against 86.0 % at 16 lanes x 4 chunks in
+        // 256-thread CTAs)
+        int64_t G = n <= 4 ? next_pow2(n) : next_pow2(ceil_div(n, (g.E == 8 && n > 16) ? 2 : 4));
         if (G > 32)
             G = 32;
         p.variant = v;
         p.lanes_per_row = (int)G;
         p.chunks_per_thread = (int)next_pow2(ceil_div(n, G));
-        p.block_threads = kRowgroupThreads;
-        const int64_t ctas = ceil_div(rows, kRowgroupThreads / G);
+        p.block_threads = kRowgroupThreads / 2;
+        const int64_t ctas = ceil_div(rows, kRowgroupThreads / 2 / G);
         p.grid_x = ctas < INT32_MAX ? ctas : INT32_MAX;
     } else if (v == SOFTMAX_VARIANT_BLOCK) {
         if (!blk_fits)
@@ -581,8 +585,10 @@ int plan_norm(const softmax_device_info &dev, int kind, const void *x, const voi
         p.variant = v;
         p.lanes_per_row = (int)G;
         p.chunks_per_thread = (int)V;
-        p.block_threads = kRowgroupThreads;
-        const int64_t ctas = ceil_div(rows, kRowgroupThreads / G);
+        // 128-thread CTAs ([32760, 384] fp16 LayerNorm: 71.6 % against 69.3 %
+        // in 256-thread CTAs)
+        p.block_threads = kRowgroupThreads / 2;
+        const int64_t ctas = ceil_div(rows, kRowgroupThreads / 2 / G);
         p.grid_x = ctas < INT32_MAX ? ctas : INT32_MAX;
     } else if (v == SOFTMAX_VARIANT_BLOCK) {
         if (!blk_fits)
