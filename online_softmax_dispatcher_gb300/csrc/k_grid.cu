@@ -62,7 +62,6 @@ struct GridArgs {
     int P;    // CTAs per row
     int Q;    // ring form: shared-memory buffers (0: streaming form)
     int buf;  // ring form: bytes per buffer
-    int lag;  // ring form: rows a CTA's output trails its statistics (1 when Q >= 2, else 0)
     int y_vec;
     float4 *part;      // [rows * P] partial statistics
     unsigned *arrive;  // [rows][2] arrival counters, one per launch parity
@@ -282,7 +281,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) k_grid_ring(const GridArgs a)
     const int Q = a.Q;
     const int nr = a.rows > gy ? (int)((a.rows - gy + G - 1) / G) : 0;
     const uint32_t seg0 = smem_u32(seg), bar0 = smem_u32(bars);
-    const int lag = a.lag;
+    const int lag = Q >= 2 ? 1 : 0;  // rows a CTA's output trails its statistics
 
     grid_prepare_next(a);
     if (tid == 0) {
@@ -616,9 +615,7 @@ int launch_grid(const Launch &l)
     const unsigned gen = pl.gen[s] + 1u;
     const int Q = l.plan.stages;
     GridArgs args{(const char *)l.x, (char *)l.y, l.rows, l.cols, (int)l.plan.grid_x, Q,
-                  Q > 0 ? l.plan.smem_bytes / Q : 0,
-                  Q > 1 ? 1 : 0,
-                  l.plan.y_vector,
+                  Q > 0 ? l.plan.smem_bytes / Q : 0, l.plan.y_vector,
                   pl.part + (size_t)s * kGridMaxPartials, pl.arrive + (size_t)s * 2 * kGridMaxRows, gen,
                   l.dev_err};
     int rc;
