@@ -754,14 +754,14 @@ __device__ __forceinline__ MD warp_md(MD v)
 // may be reused by the next reduction call (the leading barrier protects it).
 __device__ __forceinline__ float block_max(float v, float *slots)
 {
-    v = group_max<32>(v);
+    v = warp_max_redux(v);  // one instruction per warp stage, not a 5-step butterfly
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     __syncthreads();
     if (lane == 0)
         slots[warp] = v;
     __syncthreads();
     v = lane < nw ? slots[lane] : -INFINITY;
-    return group_max<32>(v);
+    return warp_max_redux(v);
 }
 
 template <int DT>
