@@ -178,11 +178,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                 }
                 release(item);
             }
-            mt = group_max<32>(mt);
+            mt = warp_max_redux(mt);
             if (lane == 0)
                 red_a[cw] = mt;
             named_sync(1, kSplitConsumers);
-            mt = group_max<32>(lane < kSplitConsumerWarps ? red_a[lane] : -INFINITY);
+            mt = warp_max_redux(lane < kSplitConsumerWarps ? red_a[lane] : -INFINITY);
             named_sync(1, kSplitConsumers);
             exchange(0, mt, 0.f);
             m = -INFINITY;

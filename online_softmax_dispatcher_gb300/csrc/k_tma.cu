@@ -166,12 +166,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_tma(const TmaParams p)
             float m = -INFINITY;
             for (int64_t c = cf + gt; c <= cl; c += GT)
                 m = fmaxf(m, chunk_max<DT>(read_raw(c)));
-            m = group_max<32>(m);
+            m = warp_max_redux(m);
             if (W > 1) {
                 if (lane == 0)
                     red_max[group][wig] = m;
                 named_sync(bar_id, bar_threads);
-                m = group_max<32>(lane < W ? red_max[group][lane] : -INFINITY);
+                m = warp_max_redux(lane < W ? red_max[group][lane] : -INFINITY);
             }
 
             Acc acc = M::zero();

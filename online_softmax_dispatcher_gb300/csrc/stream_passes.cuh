@@ -136,7 +136,7 @@ __device__ __forceinline__ void merge_partials(const float4 *ws, int64_t r, int 
         float mloc = -INFINITY;
         for (int i = lane; i < P; i += 32)
             mloc = fmaxf(mloc, __ldcg(&ws[r * P + i]).x);
-        m = group_max<32>(mloc);
+        m = warp_max_redux(mloc);
         CSum acc{0.f, 0.f};
         for (int i = lane; i < P; i += 32) {
             const float4 q = __ldcg(&ws[r * P + i]);
