@@ -106,6 +106,29 @@ def pin_planted_peak(o):
         assert np.allclose(others, rest, rtol=1e-14, atol=0)
 
 
+def pin_ramp_geometric(o):
+    # the HIP softmax tutorial's large-cols run (4 rows of 32768; its printed
+    # outputs grow by e^(1/32) from one column to the next, as a ramp
+    # x_j = j / 32 gives; input not printed): softmax of an arithmetic ramp is
+    # a normalised geometric sequence, y_j = q^(n-1-j) (1 - q) / (1 - q^n),
+    # q = e^(-1/32)
+    n = 32768
+    j = np.arange(n, dtype=np.float64)
+    x = np.stack([j / 32.0, j / 32.0 - 100.0, j / 32.0 + 7.25, (n - 1 - j) / 32.0])
+    y = o.softmax_f64(x)
+    q = math.exp(-1.0 / 32.0)
+    want = np.exp((j - (n - 1)) / 32.0) * (1.0 - q) / (1.0 - q ** n)
+    # (the first ~9000 columns lie below double's normal range: exact up to
+    # the absolute floor there)
+    for r in range(3):
+        assert np.allclose(y[r], want, rtol=1e-12, atol=1e-300)
+    assert np.allclose(y[3], want[::-1], rtol=1e-12, atol=1e-300)
+    big = y[0, :-1] > 1e-290
+    assert big.sum() > 20000
+    ratio = y[0, 1:][big] / y[0, :-1][big]
+    assert np.allclose(ratio, math.exp(1.0 / 32.0), rtol=1e-13, atol=0)
+
+
 def pin_compensated_sum(o):
     # one 0 and N entries of -40: y_0 = 1 / (1 + N e^-40).  N e^-40 ~ 4e-13 is made
     # of terms far below half an ulp of 1, so only a compensated sum keeps it.

@@ -8,6 +8,8 @@ configuration the benchmark times (the dispatcher's choice); edge shapes
 each variant caches), unaligned pointers, a y on a different 16-byte phase
 than x, special values and bitwise shift invariance.  Output buffers sit
 between canary guard bands, checked after each kernel."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -215,6 +217,23 @@ def test_bf16_subnormal_outputs():
         assert rc == 0
         check(xb, y, 2)
         assert (y[:, :] != 0).sum() >= 6
+
+
+def test_ramp_rows():
+    # the HIP softmax tutorial's large-cols shape (4 x 32768) on a ramp
+    # x_j = j / 32 (its printed outputs grow by e^(1/32) per column): every
+    # variant that accepts the shape, against the oracle, and the ratio of
+    # neighbouring outputs within the fp32 tolerance
+    n = 32768
+    j = np.arange(n, dtype=np.float64)
+    x = np.stack([j / 32.0, j / 32.0 - 100.0, j / 32.0 + 7.25, (n - 1 - j) / 32.0]).astype(np.float32)
+    for v in variants_for(4, n, 0):
+        rc, y = run(x, 0, variant=v)
+        assert rc == 0, v
+        check(x, y, 0)
+        r = y[0, 1:].astype(np.float64) / y[0, :-1]
+        big = y[0, :-1] > 1e-30
+        assert np.allclose(r[big], math.exp(1.0 / 32.0), rtol=5e-6), v
 
 
 def test_shift_invariance_bitwise():
