@@ -243,10 +243,10 @@ void plan_wide(const Geometry &g, int64_t rows, const softmax_device_info &dev, 
     p.grid_y = rows;
 }
 
-// SPLITK_GRID: P CTAs per row, all resident (cooperative launch).  fp16 /
-// bf16 rows whose share fits one CTA's shared memory at one CTA per SM take
-// the resident form (the share is read from HBM once, into shared memory);
-// the rest take the streaming form at two CTAs per SM.
+// SPLITK_GRID: P CTAs per row, all resident (cooperative launch).  Rows whose
+// CTA share fits a shared-memory buffer at one CTA per SM take the ring form
+// (each share read from HBM once, into shared memory); the rest take the
+// streaming form at two CTAs per SM.
 bool grid_possible(int64_t rows, const softmax_device_info &dev)
 {
     return dev.cc_major >= 9 && rows >= 1 && rows * 2 <= dev.sm_count && rows <= kGridMaxRows;

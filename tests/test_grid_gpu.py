@@ -45,7 +45,7 @@ def test_grid_full_size_workloads(name):
 @pytest.mark.parametrize("dt", [0, 1, 2])
 def test_grid_shapes_and_offsets(dt):
     rng = np.random.default_rng(300 + dt)
-    # resident (16-bit shares that fit shared memory) and streamed forms, ragged
+    # ring (shares that fit shared memory) and streamed forms, ragged
     # rows, few and many CTAs per row
     for rows, cols in ((1, 300001), (3, 1 << 20), (4, (1 << 21) + 5), (7, 150003), (2, 1 << 23), (76, 20000)):
         x = rng.normal(0, 4, (rows, cols))
