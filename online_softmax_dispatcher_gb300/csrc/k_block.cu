@@ -1,6 +1,7 @@
 // k_block.cu -- one CTA per row, the row cached in registers: one HBM read and
 // one HBM write per element for rows of up to 512 threads x 16 chunks x 16 B
-// = 128 KiB.
+// = 128 KiB (past 256 threads at 16 chunks one CTA fills an SM: the grid is
+// then one CTA per SM looping over rows, each prefetching its next row into L2).
 //
 // A row off the 16-byte grid is read as its interior chunks (16-byte vectors,
 // interior chunk q to thread q mod T) plus at most 2E - 2 edge elements, one
@@ -22,8 +23,11 @@
 
 namespace osd {
 
-template <int DT, int V, int PH>
-__global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
+// LOOP: 16 chunks at more than 256 threads (one CTA per SM, looping over
+// rows); the other instances keep two CTAs per SM at 16 chunks.
+template <int DT, int V, int PH, bool LOOP>
+__global__ void __launch_bounds__(V >= 16 ? (LOOP ? 512 : 256) : block_max_threads_ct(V),
+                                  V >= 16 ? (LOOP ? 1 : 2) : (V >= 8 ? 2 : 1))
     k_block(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols)
 {
     pdl_enter();
@@ -40,6 +44,14 @@ __global__ void __launch_bounds__(block_max_threads_ct(V), V >= 8 ? 2 : 1)
     const int t = threadIdx.x;
 
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        // LOOP: one CTA per SM (up to 512 threads x 16 chunks, rows of up to
+        // 128 KiB) looping over rows: ask L2 for the CTA's next row, so HBM
+        // keeps streaming while this row is reduced and written.  (A separate
+        // instance: the check alone, in the other kernels, cost up to 6 points.)
+        if constexpr (LOOP) {
+            if (threadIdx.x == 0 && r + gridDim.x < rows)
+                prefetch_row_l2(x + (r + gridDim.x) * cols * Fmt<DT>::kBytes, cols * Fmt<DT>::kBytes);
+        }
         const ShortRow g = short_row<DT, PH == kPhAligned>(x, y, r, (int)cols);
         // Thread t takes interior chunks q = t + i * T - sh: the shift sh puts
         // every 8th slot on a 128-byte line, so a warp's 32 chunks span 4
@@ -139,7 +151,12 @@ namespace {
 template <int DT, int V, int PH>
 int launch_one(const Launch &l)
 {
-    return launch_pdl(k_block<DT, V, PH>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+    if constexpr (V >= 16) {
+        if (l.plan.block_threads > 256)
+            return launch_pdl(k_block<DT, V, PH, true>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads),
+                              0, (cudaStream_t)l.stream, no_attr(), (const char *)l.x, (char *)l.y, l.rows, l.cols);
+    }
+    return launch_pdl(k_block<DT, V, PH, false>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
                       (cudaStream_t)l.stream, no_attr(), (const char *)l.x, (char *)l.y, l.rows, l.cols);
 }
 

@@ -17,7 +17,7 @@ constexpr int kBlockMaxChunks = 16;     // V of the block-per-row kernel
 constexpr int kStreamThreads = 512;     // CTA size of the streaming kernel
 constexpr int kStreamUnroll = 8;        // 16-byte loads in flight per thread per step
 constexpr int kWideStep = 4;            // the same for the wide split: 64 registers at two 512-thread CTAs per SM
-constexpr int kGridThreads = 512;       // SPLITK_GRID: CTA size (resident and streaming forms)
+constexpr int kGridThreads = 512;       // SPLITK_GRID: CTA size (ring and streaming forms)
 constexpr int kGridSlots = 16;          // SPLITK_GRID: scratch slots (launches in flight at once)
 constexpr int kGridMaxRows = 128;       // SPLITK_GRID: rows a slot serves
 constexpr int kGridMaxPartials = 4096;  // SPLITK_GRID: rows x CTAs per row a slot serves
@@ -36,7 +36,7 @@ constexpr int kTmaStaticSmem = 4096;    // BLOCK_TMA static shared memory (barri
 // Largest CTA size the block kernel is compiled for at a given V.  V >= 8 is
 // compiled for two resident CTAs per SM, so that one CTA's loads overlap the
 // other's reductions; the register file then bounds threads x registers.
-constexpr int block_max_threads_ct(int v) { return v >= 16 ? 256 : (v >= 8 ? 512 : 1024); }
+constexpr int block_max_threads_ct(int v) { return v >= 8 ? 512 : 1024; }
 inline int block_max_threads(int v) { return block_max_threads_ct(v); }
 
 struct Launch {
