@@ -236,6 +236,22 @@ def test_ramp_rows():
         assert np.allclose(r, math.exp(1.0 / 32.0), rtol=5e-6), v
 
 
+def test_looping_block_rows():
+    # rows of 64 - 128 KiB: 16 chunks a thread past 256 threads, one CTA per SM
+    # looping over more rows than SMs, each prefetching its next row into L2;
+    # off the 16-byte grid (the dispatcher's choice) and forced on the grid
+    rng = np.random.default_rng(41)
+    block = osd.VARIANTS["block"]
+    for rows, cols, dt, off, v in ((400, 50257, 2, 0, 0), (300, 50003, 1, 1, 0), (200, 30000, 0, 0, block),
+                                   (170, 65536, 2, 0, 0)):
+        x = rng.normal(0, 3, (rows, cols))
+        x[:, ::1009] += 25.0
+        x = x.astype(NUMPY[dt]) if dt != 2 else W._round_to(x, "bf16")
+        rc, y = run(x, dt, variant=v, x_off=off, y_off=off)
+        assert rc == 0, (rows, cols, dt)
+        check(x, y, dt)
+
+
 def test_shift_invariance_bitwise():
     rng = np.random.default_rng(9)
     for cols in (300, 5003, 40000):
