@@ -79,7 +79,9 @@ typedef enum {
 typedef enum {
     SOFTMAX_VARIANT_AUTO = 0,      /* let the dispatcher choose */
     SOFTMAX_VARIANT_ROWGROUP = 1,  /* G = 1..32 lanes per row, row cached in registers */
-    SOFTMAX_VARIANT_BLOCK = 2,     /* one CTA per row, row cached in registers */
+    SOFTMAX_VARIANT_BLOCK = 2,     /* one CTA per row, row cached in registers (rows of up to
+                                      8192 chunks of 16 bytes; past 4096, one CTA per SM
+                                      looping over rows) */
     SOFTMAX_VARIANT_BLOCK_TMA = 3, /* persistent CTAs, rows staged in shared memory by bulk
                                       async copies (TMA engine), one HBM read per element */
     SOFTMAX_VARIANT_STREAM = 4,    /* one CTA per row, online (m, d) pass then a re-read pass;
