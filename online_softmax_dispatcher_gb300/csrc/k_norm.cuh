@@ -105,7 +105,9 @@ struct RowCache {
 // One row for a team of L threads (lane = this thread's index in the team).
 // NE edge elements per thread; `valid` false for a lane group past the last
 // row (it still takes part in the team's reductions).
-template <int DT, int KIND, int V, int MODE, int NE, bool KEEP, class Red>
+// AFF false: no gain and no bias (the caller knows), so the output loop
+// carries no test of the vectors at all.
+template <int DT, int KIND, int V, int MODE, int NE, bool KEEP, bool AFF, class Red>
 __device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool valid, int lane, int L, float inv_n,
                                          Red red)
 {
@@ -201,22 +203,29 @@ __device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool vali
     for (int i = 0; i < V; i++) {
         if (has(i)) {
             const int q = lane + i * L;
-            float f[E], gv[E], bv[E];
+            float f[E];
             c.get(i, f);
-            if (a.gamma)
-                vec_chunk<DT, MODE>(a.gamma, g, q, gv);
-            if (KIND == kNormLayer && a.beta)
-                vec_chunk<DT, MODE>(a.beta, g, q, bv);
+            if constexpr (AFF) {
+                float gv[E], bv[E];
+                if (a.gamma)
+                    vec_chunk<DT, MODE>(a.gamma, g, q, gv);
+                if (KIND == kNormLayer && a.beta)
+                    vec_chunk<DT, MODE>(a.beta, g, q, bv);
 #pragma unroll
-            for (int e = 0; e < E; e++) {
-                const float z = fmaf(f[e], rs, nmr);
-                if (a.gamma || (KIND == kNormLayer && a.beta)) {
-                    const float gg = a.gamma ? gv[e] : 1.0f;
-                    const float bb = (KIND == kNormLayer && a.beta) ? bv[e] : 0.0f;
-                    f[e] = fmaf(z, gg, bb);
-                } else {
-                    f[e] = z;
+                for (int e = 0; e < E; e++) {
+                    const float z = fmaf(f[e], rs, nmr);
+                    if (a.gamma || (KIND == kNormLayer && a.beta)) {
+                        const float gg = a.gamma ? gv[e] : 1.0f;
+                        const float bb = (KIND == kNormLayer && a.beta) ? bv[e] : 0.0f;
+                        f[e] = fmaf(z, gg, bb);
+                    } else {
+                        f[e] = z;
+                    }
                 }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    f[e] = fmaf(f[e], rs, nmr);
             }
             store_interior<DT, PH>(g, q, pack<DT>(f));
         }
@@ -225,15 +234,19 @@ __device__ __forceinline__ void norm_row(const NormArgs &a, int64_t r, bool vali
     for (int u = 0; u < NE; u++) {
         if (je[u] >= 0) {
             const float z = fmaf(xe[u], rs, nmr);
-            const float gg = a.gamma ? ld_elem<DT>(a.gamma, je[u]) : 1.0f;
-            const float bb = (KIND == kNormLayer && a.beta) ? ld_elem<DT>(a.beta, je[u]) : 0.0f;
-            st_elem<DT>(g.yr, je[u], fmaf(z, gg, bb));
+            if constexpr (AFF) {
+                const float gg = a.gamma ? ld_elem<DT>(a.gamma, je[u]) : 1.0f;
+                const float bb = (KIND == kNormLayer && a.beta) ? ld_elem<DT>(a.beta, je[u]) : 0.0f;
+                st_elem<DT>(g.yr, je[u], fmaf(z, gg, bb));
+            } else {
+                st_elem<DT>(g.yr, je[u], z);
+            }
         }
     }
 }
 
 // G lanes per row, 256 / G rows per CTA per step.
-template <int DT, int KIND, int G, int V, int MODE>
+template <int DT, int KIND, int G, int V, int MODE, bool AFF>
 __global__ void __launch_bounds__(kRowgroupThreads) k_norm_rowgroup(const NormArgs a)
 {
     pdl_enter();
@@ -246,7 +259,7 @@ __global__ void __launch_bounds__(kRowgroupThreads) k_norm_rowgroup(const NormAr
     // butterflies see converged warps
     for (int64_t base = (int64_t)blockIdx.x * groups; base < a.rows; base += stride) {
         const int64_t r = base + threadIdx.x / G;
-        norm_row<DT, KIND, V, MODE, NE, true>(a, r, r < a.rows, gl, G, inv_n, GroupSum<DT, G>{});
+        norm_row<DT, KIND, V, MODE, NE, true, AFF>(a, r, r < a.rows, gl, G, inv_n, GroupSum<DT, G>{});
     }
 }
 
@@ -259,7 +272,7 @@ __global__ void __launch_bounds__(1024) k_norm_block(const NormArgs a)
     constexpr int NE = MODE == kNormFast ? 0 : 1;  // >= 32 threads: one edge element each at most
     const float inv_n = 1.0f / (float)a.cols;
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
-        norm_row<DT, KIND, V, MODE, NE, false>(a, r, true, threadIdx.x, blockDim.x, inv_n, CtaSum<DT>{slots});
+        norm_row<DT, KIND, V, MODE, NE, false, true>(a, r, true, threadIdx.x, blockDim.x, inv_n, CtaSum<DT>{slots});
 }
 
 namespace norm_detail {
@@ -274,8 +287,12 @@ inline NormArgs args_of(const NormLaunch &l)
 template <int DT, int KIND, int G, int V, int MODE>
 int rg_one(const NormLaunch &l)
 {
-    return launch_pdl(k_norm_rowgroup<DT, KIND, G, V, MODE>, dim3((unsigned)l.plan.grid_x),
-                      dim3(l.plan.block_threads), 0, (cudaStream_t)l.stream, no_attr(), args_of(l));
+    const NormArgs a = args_of(l);
+    if (a.gamma || a.beta)
+        return launch_pdl(k_norm_rowgroup<DT, KIND, G, V, MODE, true>, dim3((unsigned)l.plan.grid_x),
+                          dim3(l.plan.block_threads), 0, (cudaStream_t)l.stream, no_attr(), a);
+    return launch_pdl(k_norm_rowgroup<DT, KIND, G, V, MODE, false>, dim3((unsigned)l.plan.grid_x),
+                      dim3(l.plan.block_threads), 0, (cudaStream_t)l.stream, no_attr(), a);
 }
 
 template <int DT, int KIND, int V, int MODE>
