@@ -308,3 +308,27 @@ def test_other_operations_dispatch(lib):
     assert rc == B.ERR_INVALID_ARG
     rc, p = B.norm_plan(GB300, 0, BASE, BASE + (1 << 36), 0, 3, 0)
     assert rc == B.OK and p.grid_x == 0
+
+
+def test_long_block_rows_dispatch(lib):
+    # rows of 64 - 128 KiB: off the 16-byte grid the block kernel at 16 chunks
+    # and up to 512 threads, one CTA per SM looping over rows; on the grid the
+    # bulk-copy tiles; past 8192 chunks neither holds the row in registers
+    y = BASE + (1 << 36)
+    rc, p = B.softmax_plan(GB300, BASE, y, 16384, 50257, 2)
+    assert rc == B.OK and p.variant == B.VARIANT_BLOCK
+    assert p.chunks_per_thread == 16 and 256 < p.block_threads <= 512 and p.grid_x == 152
+    assert p.block_threads * 16 >= 50257 * 2 // 16
+    rc, p = B.softmax_plan(GB300, BASE, y, 100, 50257, 2)
+    assert rc == B.OK and p.variant == B.VARIANT_BLOCK and p.grid_x == 100     # fewer rows than SMs
+    rc, p = B.softmax_plan(GB300, BASE, y, 16384, 40000, 1)                      # on the grid: 5000 chunks
+    assert rc == B.OK and p.variant == B.VARIANT_BLOCK_TMA
+    rc, p = B.softmax_plan(GB300, BASE, y, 16384, 40000, 1, B.VARIANT_BLOCK)    # still allowed when forced
+    assert rc == B.OK and p.chunks_per_thread == 16 and p.grid_x == 152
+    rc, p = B.softmax_plan(GB300, BASE, y, 8192, 65536, 2)                       # 8192 chunks exactly
+    assert rc == B.OK and p.variant == B.VARIANT_BLOCK and p.block_threads == 512
+    rc, _ = B.softmax_plan(GB300, BASE, y, 8192, 65544, 2, B.VARIANT_BLOCK)      # 8193 chunks
+    assert rc == B.ERR_UNSUPPORTED_SHAPE
+    # up to 64 KiB rows keep one CTA per row
+    rc, p = B.softmax_plan(GB300, BASE, y, 32768, 32000, 2)
+    assert rc == B.OK and p.variant == B.VARIANT_BLOCK and p.block_threads == 256 and p.grid_x == 32768
