@@ -289,7 +289,15 @@ def test_other_operations_dispatch(lib):
             # one 512-thread CTA per SM: the grid is one CTA per SM, looping over rows
             assert p.grid_x == 152 and p.block_threads == 512
     rc, p = B.softmax_masked_plan(GB300, BASE, BASE + (1 << 36), 65536, 512, 1)
+    # 2 chunks a lane for 16-bit rows of 17 - 64 chunks, 128-thread CTAs
     assert rc == B.OK and p.variant == B.VARIANT_ROWGROUP
+    assert (p.lanes_per_row, p.chunks_per_thread, p.block_threads) == (32, 2, 128)
+    rc, p = B.softmax_bwd_plan(GB300, y, dy, dx, 65536, 512, 1)
+    assert rc == B.OK and (p.lanes_per_row, p.chunks_per_thread, p.block_threads) == (32, 2, 128)
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 65536, 512, 1)
+    assert rc == B.OK and (p.lanes_per_row, p.chunks_per_thread, p.block_threads, p.grid_x) == (32, 2, 128, 16384)
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 262144, 128, 1)    # 16 chunks: 4 a lane
+    assert rc == B.OK and (p.lanes_per_row, p.chunks_per_thread) == (4, 4)
     for name, (v, G, V) in {"ln_fp16_131040x192": (B.VARIANT_ROWGROUP, 8, 3),
                             "ln_fp16_32760x384": (B.VARIANT_ROWGROUP, 16, 3),
                             "rms_bf16_16384x4096": (B.VARIANT_BLOCK, 0, 4)}.items():
@@ -297,7 +305,7 @@ def test_other_operations_dispatch(lib):
         rc, p = B.norm_plan(GB300, w.kind, BASE, BASE + (1 << 36), w.rows, w.cols, w.dtype_code)
         assert rc == B.OK and p.variant == v and p.chunks_per_thread == V, (name, p.as_dict())
         if G:
-            assert p.lanes_per_row == G
+            assert p.lanes_per_row == G and p.block_threads == 128
     # arguments are checked as the launching calls check them
     assert lib.softmax_bwd_plan(None, y, dy, dx, 2, 3, 0, 0, None) == B.ERR_INVALID_ARG
     rc, _ = B.softmax_bwd_plan(GB300, y, dy, dx, 2, 3, 7)
