@@ -146,9 +146,11 @@ int softmax_fwd_variant(const void *x, void *y, int64_t rows, int64_t cols, int 
  *   causal_q   0 (no causal cut) or the query block length.  A row with no
  *              visible key is all -inf and comes out NaN, as the definition
  *              gives.
- * Accuracy: as softmax_fwd against the exact softmax of z, with z formed in
- * binary64; fp16 / bf16 additionally allow 2^-22 * max_j |z_j| relative (z is
- * one fp32 FMA there), fp32 keeps 2e-6 (z is carried as a two-float pair).
+ * Accuracy: as softmax_fwd (fp32 2e-6 relative; fp16 / bf16 within 1 ulp of
+ * the correctly rounded result) against the exact softmax of z formed from
+ * the float `scale` as passed, whatever the size of the logits: fp32 carries
+ * z as a two-float pair, fp16 / bf16 rows whose largest logit reaches 512 in
+ * magnitude do too (below that one fp32 FMA is accurate enough).
  * Rows up to 2048 chunks of 16 bytes (32 KiB: 16384 fp16 / bf16 or 8192 fp32
  * keys): SOFTMAX_ERR_UNSUPPORTED_SHAPE beyond.  Alignment, streams, errors:
  * as softmax_fwd.
@@ -236,7 +238,9 @@ int softmax_workspace_size(const void *x, const void *y, int64_t rows, int64_t c
  * SOFTMAX_ERR_UNSUPPORTED_SHAPE.  On a 152-SM GB300 any rows <= 4096 fits.
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress); make that first call before any stream
- * capture.  Every call shares the array and it keeps the last call's
+ * capture.  If the lookup fails, the call returns SOFTMAX_ERR_CUDA and the
+ * next call on that device looks it up again (only a successful lookup is
+ * kept).  Every call shares the array and it keeps the last call's
  * contents; nothing in it needs to start at zero (the first launch writes
  * every slot the second reads).  Calls that overlap on the GPU -- on
  * different streams, or from different host threads -- race on the array and

@@ -45,8 +45,7 @@ thread_local int t_last_cuda_error = 0;
 constexpr int kMaxDevices = 64;
 
 struct DeviceCache {
-    std::once_flag once;
-    int status = SOFTMAX_OK;
+    InitOnSuccess init;
     softmax_device_info info = {};
     unsigned int *error_word = nullptr;
 };
@@ -59,16 +58,15 @@ int cuda_fail(cudaError_t e)
     return SOFTMAX_ERR_CUDA;
 }
 
-void init_device(DeviceCache &c, int dev)
+// Fills c for device dev (current); SOFTMAX_OK or the failing call's status.
+int init_device(DeviceCache &c, int dev)
 {
     int v = 0;
     cudaError_t e;
 #define OSD_ATTR(field, attr)                                 \
     e = cudaDeviceGetAttribute(&v, attr, dev);                \
-    if (e != cudaSuccess) {                                   \
-        c.status = cuda_fail(e);                              \
-        return;                                               \
-    }                                                         \
+    if (e != cudaSuccess)                                     \
+        return cuda_fail(e);                                  \
     c.info.field = v;
     OSD_ATTR(sm_count, cudaDevAttrMultiProcessorCount)
     OSD_ATTR(max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin)
@@ -79,11 +77,10 @@ void init_device(DeviceCache &c, int dev)
 #undef OSD_ATTR
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_device_error);
-    if (e != cudaSuccess) {
-        c.status = cuda_fail(e);
-        return;
-    }
+    if (e != cudaSuccess)
+        return cuda_fail(e);
     c.error_word = static_cast<unsigned int *>(p);
+    return SOFTMAX_OK;
 }
 
 int current_device(DeviceCache **out)
@@ -95,9 +92,9 @@ int current_device(DeviceCache **out)
     if (dev < 0 || dev >= kMaxDevices)
         return SOFTMAX_ERR_INVALID_ARG;
     DeviceCache &c = g_devices[dev];
-    std::call_once(c.once, init_device, std::ref(c), dev);
-    if (c.status != SOFTMAX_OK)
-        return c.status;
+    const int rc = c.init.run([&] { return init_device(c, dev); });  // device dev is current here
+    if (rc != SOFTMAX_OK)
+        return rc;
     *out = &c;
     return SOFTMAX_OK;
 }

@@ -11,8 +11,12 @@
 //   rounding is round-to-nearest-even, as the half kernels of "[CUDA] safe
 //   online softmax" (section 2.1) and "Softmax on DCU" (section 4.5) do.
 // * exp: for fp16 / bf16 outputs exp(x - m) = 2^((x - m) * log2 e) on the SFU
-//   (ex2.approx, subnormal results kept: no .ftz); its ~2^-22 relative error is
-//   far below half an ulp of either 16-bit format.  For fp32 outputs the shift
+//   (ex2.approx.ftz: results below 2^-126 flush to zero); its ~2^-22 relative
+//   error is far below half an ulp of either 16-bit format.  bf16 reaches
+//   subnormal outputs, so its exps are taken pre-scaled by 2^64 (the argument
+//   is (x - m) log2 e + 64; the scale cancels in y) and only terms below
+//   2^-190, which bf16 rounds to 0 anyway, flush (Math<DT> below).  fp16
+//   outputs are 0 below 2^-25 and need no scale.  For fp32 outputs the shift
 //   t = x - m is split exactly into t + r (Knuth's TwoSum) and
 //   exp(x - m) = expf(t) * (1 + r), which keeps the result within a few fp32
 //   ulps even when |x - m| is in the hundreds.

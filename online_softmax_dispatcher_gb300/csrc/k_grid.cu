@@ -501,8 +501,7 @@ static __device__ __align__(256) float4 g_grid_part[kGridSlots][kGridMaxPartials
 static __device__ unsigned g_grid_arrive[kGridSlots][2 * kGridMaxRows];
 
 struct GridPool {
-    std::once_flag once;
-    cudaError_t status = cudaSuccess;
+    InitOnSuccess init;
     float4 *part = nullptr;
     unsigned *arrive = nullptr;
     cudaEvent_t ev[kGridSlots] = {};
@@ -515,17 +514,26 @@ struct GridPool {
 
 GridPool g_pools[64];
 
-void pool_init(GridPool &pl)
+// The device addresses of the scratch arrays and the slots' events, for the
+// current device.  Safe to call again after a failure: events made by an
+// earlier attempt are kept.
+int pool_init(GridPool &pl)
 {
     void *p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_grid_part);
+    if (e != cudaSuccess)
+        return (int)e;
     pl.part = static_cast<float4 *>(p);
-    if (e == cudaSuccess)
-        e = cudaGetSymbolAddress(&p, g_grid_arrive);
+    e = cudaGetSymbolAddress(&p, g_grid_arrive);
+    if (e != cudaSuccess)
+        return (int)e;
     pl.arrive = static_cast<unsigned *>(p);
-    for (int i = 0; i < kGridSlots && e == cudaSuccess; i++)
-        e = cudaEventCreateWithFlags(&pl.ev[i], cudaEventDisableTiming);
-    pl.status = e;
+    for (int i = 0; i < kGridSlots; i++)
+        if (pl.ev[i] == nullptr && (e = cudaEventCreateWithFlags(&pl.ev[i], cudaEventDisableTiming)) != cudaSuccess) {
+            pl.ev[i] = nullptr;
+            return (int)e;
+        }
+    return 0;
 }
 
 template <int DT, bool A, bool RES>
@@ -600,9 +608,9 @@ int launch_grid(const Launch &l)
     if (d < 0 || d >= 64)
         return (int)cudaErrorInvalidDevice;
     GridPool &pl = g_pools[d];
-    std::call_once(pl.once, pool_init, std::ref(pl));  // device d is current here
-    if (pl.status != cudaSuccess)
-        return (int)pl.status;
+    const int pe = pl.init.run([&] { return pool_init(pl); });  // device d is current here
+    if (pe != 0)
+        return pe;
     if (l.rows > kGridMaxRows || l.plan.grid_x * l.rows > kGridMaxPartials || l.plan.stages > kGridMaxRing)
         return (int)cudaErrorInvalidValue;
     const unsigned s = pl.next.fetch_add(1, std::memory_order_relaxed) % kGridSlots;
@@ -646,7 +654,7 @@ int reset_grid_scratch()
     if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64)
         return 0;
     GridPool &pl = g_pools[d];
-    if (!pl.arrive || pl.status != cudaSuccess)
+    if (!pl.arrive)
         return 0;
     for (int s = 0; s < kGridSlots; s++)
         pl.mu[s].lock();

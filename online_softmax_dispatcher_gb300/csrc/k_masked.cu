@@ -8,11 +8,17 @@
 //
 // * z_j = scale * x_j + mask[r % mask_rows, j]; with causal_q > 0 every key
 //   j > i + (cols - causal_q), i = r % causal_q, is cut (z_j = -inf).
-// * fp16 / bf16: z is one fp32 FMA (its rounding, 2^-24 |z|, is far below
-//   half an ulp of the output for logits of moderate size); fp32: z is kept as
-//   an unevaluated pair zh + zl (the product split exactly by an FMA, the mask
-//   added with TwoSum), and exp(z - m) = expf(th) (1 + tl + zl) with
-//   th + tl = zh - m exactly, so fp32 keeps its 2e-6 bound.
+// * fp32: z is kept as an unevaluated pair zh + zl (the product split exactly
+//   by an FMA, the mask added with TwoSum), and exp(z - m) = expf(th)
+//   (1 + tl + zl) with th + tl = zh - m exactly, so fp32 keeps its 2e-6 bound.
+// * fp16 / bf16: z is one fp32 FMA, whose rounding moves exp(z_j - m) by up to
+//   2^-24 (|z_j| + |m|) relative.  An output that is not below the 16-bit
+//   range has z_j >= m - 100, so while |m| < kPairFreeMax = 512 that is under
+//   2^-24 * 1124 = 6.7e-5, well inside half an fp16 ulp (2^-12 at least), and
+//   the row keeps its single-float logits.  A row whose max logit is larger in
+//   magnitude forms the pairs (re-reading x where the kernel kept only the
+//   logits) and exponentiates 2^((zh - m) log2e + zl log2e) by two FMAs, so
+//   the bound of the plain softmax holds whatever the size of the logits.
 // * ROWGROUP form (G lanes per row, the logits kept in registers) for rows of
 //   up to 32 lanes x 32 floats; BLOCK form (one CTA per row, x kept packed in
 //   registers, the mask chunk re-read through L1 and the logits recomputed in
@@ -23,6 +29,8 @@
 //   computed once: chunks wholly past the causal limit are not read, only the
 //   one the limit falls in cuts values one by one.  The mask's presence and
 //   the rows' 16-byte phases are template parameters.
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -66,11 +74,15 @@ constexpr int kMFast = 0;
 constexpr int kMSame = 1;
 constexpr int kMOther = 2;
 
-// exp(z - m) for a logit z = zh + zl (fp32) or zh (fp16 / bf16).  16-bit:
-// one FMA z log2e + c with c = bias - m log2e, computed once per row: the
-// rounding of m log2e scales the whole row's exps by one common factor, which
-// the normalisation cancels.
-template <int DT>
+// 16-bit rows whose max logit is smaller than this in magnitude need no low
+// parts (the header's bound).
+constexpr float kPairFreeMax = 512.f;
+
+// exp(z - m) for a logit z = zh + zl (PAIR) or zh.  16-bit: one FMA
+// z log2e + c with c = bias - m log2e, computed once per row (the rounding of
+// m log2e scales the whole row's exps by one common factor, which the
+// normalisation cancels), and with a pair a second FMA adding zl log2e.
+template <int DT, bool PAIR>
 __device__ __forceinline__ float exp_logit(float zh, float zl, float m, float c)
 {
     if constexpr (DT == kF32) {
@@ -79,6 +91,9 @@ __device__ __forceinline__ float exp_logit(float zh, float zl, float m, float c)
         const float e = expf(th);
         const float r = tl + zl;
         return (fabsf(r) < INFINITY) ? fmaf(e, r, e) : e;
+    } else if constexpr (PAIR) {
+        (void)m;
+        return ex2_ftz(fmaf(zl, kLog2e, fmaf(zh, kLog2e, c)));
     } else {
         (void)m;
         (void)zl;
@@ -95,17 +110,28 @@ __device__ __forceinline__ float exp_offset(float m)
         return Math<DT>::kExpBias - m * kLog2e;
 }
 
-// The logit of one value: zh (and the fp32 low part zl) of scale * x + mv.
-template <int DT>
+// The logit of one value.  PAIR: zh + zl = scale * x + mv up to a rounding of
+// the (tiny) low part; where zh is not finite (a -inf mask or input cuts the
+// value, or a NaN) zl is 0, so that it cannot turn the cut value's exp into
+// NaN.  Else zh = scale * x + mv by one FMA and zl = 0.
+template <bool PAIR, bool HAS_MASK>
 __device__ __forceinline__ void logit(float scale, float xv, float mv, float &zh, float &zl)
 {
-    if constexpr (DT == kF32) {
+    if constexpr (PAIR) {
         const float ph = scale * xv;
-        const float pl = fmaf(scale, xv, -ph);
-        float s, err;
-        two_sum(ph, mv, s, err);
-        zh = s;
-        zl = err + pl;
+        const float pl = fmaf(scale, xv, -ph);  // exact: scale * x = ph + pl
+        if constexpr (HAS_MASK) {
+            float s, err;
+            two_sum(ph, mv, s, err);
+            zh = s;
+            zl = err + pl;
+        } else {
+            (void)mv;
+            zh = ph;
+            zl = pl;
+        }
+        if (!(fabsf(zh) < INFINITY))
+            zl = 0.f;
     } else {
         zh = fmaf(scale, xv, mv);
         zl = 0.f;
@@ -114,7 +140,7 @@ __device__ __forceinline__ void logit(float scale, float xv, float mv, float &zh
 
 // Logits of interior chunk q holding nv visible values (0 < nv <= E); slots
 // past nv are cut to -inf.
-template <int DT, int MODE, bool HAS_MASK>
+template <int DT, int MODE, bool HAS_MASK, bool PAIR>
 __device__ __forceinline__ void chunk_logits(const MaskedArgs &a, const ShortRow &g, const char *mrow, bool m_vec,
                                              int q, int nv, const uint4 &xc, float (&zh)[Fmt<DT>::kPerChunk],
                                              float (&zl)[Fmt<DT>::kPerChunk])
@@ -135,7 +161,7 @@ __device__ __forceinline__ void chunk_logits(const MaskedArgs &a, const ShortRow
     }
 #pragma unroll
     for (int e = 0; e < E; e++)
-        logit<DT>(a.scale, xf[e], HAS_MASK ? mf[e] : 0.f, zh[e], zl[e]);
+        logit<PAIR, HAS_MASK>(a.scale, xf[e], HAS_MASK ? mf[e] : 0.f, zh[e], zl[e]);
     if (nv < E) {
 #pragma unroll
         for (int e = 0; e < E; e++)
@@ -183,7 +209,12 @@ struct MaxSumGroup {
 // registers (lanes per row); else x stays packed and the logits are recomputed
 // in each pass (CTA per row, with the 128-byte-line chunk map).  Interior
 // chunks wholly past the causal limit are neither read nor exponentiated; only
-// the chunk the limit falls in tests its values one by one.
+// the chunk the limit falls in tests its values one by one.  16-bit rows take
+// single-float logits in the max pass.  Without KEEP the later passes form
+// pairs (they form the logits again anyway).  KEEP rows form pairs only when
+// the max turns out large in magnitude (a decision the whole team shares, as
+// it shares m), reading x again for them (from L2: the row was just loaded,
+// and no output of it is stored yet, so an in-place call reads x too).
 template <int DT, int V, int MODE, bool HAS_MASK, int NE, bool KEEP, class Red>
 __device__ __forceinline__ void masked_row(const MaskedArgs &a, int64_t r, bool valid, int lane, int L, Red red)
 {
@@ -191,6 +222,7 @@ __device__ __forceinline__ void masked_row(const MaskedArgs &a, int64_t r, bool 
     constexpr int E = Fmt<DT>::kPerChunk;
     constexpr int S = Fmt<DT>::kBytes;
     constexpr int PH = MODE == kMFast ? kPhAligned : (MODE == kMSame ? kPhSame : kPhOther);
+    constexpr bool PAIR1 = DT == kF32;  // the max pass forms pairs (fp32 always needs them)
     const int64_t rr = valid ? r : 0;
     const ShortRow g = short_row<DT, MODE == kMFast>(a.x, a.y, rr, (int)a.cols);
     const char *mrow = HAS_MASK ? a.mask + (rr % a.mask_rows) * a.cols * S : nullptr;
@@ -216,6 +248,7 @@ __device__ __forceinline__ void masked_row(const MaskedArgs &a, int64_t r, bool 
         nv[i] = (unsigned)q < (unsigned)span ? (left < 0 ? 0 : (left > E ? E : left)) : 0;
         xc[i] = nv[i] > 0 ? ld_chunk(g.x0 + ((int64_t)(g.kf + q) << 4)) : make_uint4(0, 0, 0, 0);
     }
+    // edge elements (a few per lane at most) always carry pairs
     int je[NE > 0 ? NE : 1];
     float eh[NE > 0 ? NE : 1], el[NE > 0 ? NE : 1];
 #pragma unroll
@@ -225,22 +258,24 @@ __device__ __forceinline__ void masked_row(const MaskedArgs &a, int64_t r, bool 
         eh[u] = -INFINITY;
         el[u] = 0.f;
         if (je[u] >= 0 && je[u] < lim)
-            logit<DT>(a.scale, ld_elem<DT>(g.xr, je[u]), HAS_MASK ? ld_elem<DT>(mrow, je[u]) : 0.f, eh[u], el[u]);
+            logit<true, HAS_MASK>(a.scale, ld_elem<DT>(g.xr, je[u]), HAS_MASK ? ld_elem<DT>(mrow, je[u]) : 0.f,
+                                  eh[u], el[u]);
     }
 
-    float zh[KEEP ? V : 1][E], zl[KEEP ? V : 1][E];
+    float zh[KEEP ? V : 1][E], zl[KEEP && PAIR1 ? V : 1][E];
     float m = -INFINITY;
 #pragma unroll
     for (int i = 0; i < V; i++) {
         if (nv[i] > 0) {
             float h[E], l[E];
-            chunk_logits<DT, MODE, HAS_MASK>(a, g, mrow, m_vec, q0 + i * L, nv[i], xc[i], h, l);
+            chunk_logits<DT, MODE, HAS_MASK, PAIR1>(a, g, mrow, m_vec, q0 + i * L, nv[i], xc[i], h, l);
 #pragma unroll
             for (int e = 0; e < E; e++) {
                 m = fmaxf(m, h[e]);
                 if constexpr (KEEP) {
                     zh[i][e] = h[e];
-                    zl[i][e] = l[e];
+                    if constexpr (PAIR1)
+                        zl[i][e] = l[e];
                 }
             }
         }
@@ -250,66 +285,86 @@ __device__ __forceinline__ void masked_row(const MaskedArgs &a, int64_t r, bool 
         m = fmaxf(m, eh[u]);
     m = red.max(m);
     const float c = exp_offset<DT>(m);
+    const bool pair = PAIR1 || !KEEP || !(fabsf(m) < kPairFreeMax);
 
+    // exps of the interior chunks, summed (and kept, KEEP)
     typename M::Acc acc = M::zero();
+    auto exp_pass = [&](auto pair_tag) {
+        constexpr bool P = decltype(pair_tag)::value;
 #pragma unroll
-    for (int i = 0; i < V; i++) {
-        if (nv[i] > 0) {
-            float h[E], l[E];
-            if constexpr (KEEP) {
+        for (int i = 0; i < V; i++) {
+            if (nv[i] > 0) {
+                float h[E], l[E];
+                if constexpr (KEEP && P == PAIR1) {
+#pragma unroll
+                    for (int e = 0; e < E; e++) {
+                        h[e] = zh[i][e];
+                        l[e] = PAIR1 ? zl[i][e] : 0.f;
+                    }
+                } else if constexpr (KEEP) {
+                    // 16-bit row with large logits: x again, for the pairs
+                    const uint4 xr = ld_chunk(g.x0 + ((int64_t)(g.kf + q0 + i * L) << 4));
+                    chunk_logits<DT, MODE, HAS_MASK, P>(a, g, mrow, m_vec, q0 + i * L, nv[i], xr, h, l);
+                } else {
+                    opaque(xc[i]);
+                    chunk_logits<DT, MODE, HAS_MASK, P>(a, g, mrow, m_vec, q0 + i * L, nv[i], xc[i], h, l);
+                }
 #pragma unroll
                 for (int e = 0; e < E; e++) {
-                    h[e] = zh[i][e];
-                    l[e] = zl[i][e];
+                    const float ev = exp_logit<DT, P>(h[e], l[e], m, c);
+                    M::add(acc, ev);
+                    if constexpr (KEEP)
+                        zh[i][e] = ev;
                 }
-            } else {
-                opaque(xc[i]);
-                chunk_logits<DT, MODE, HAS_MASK>(a, g, mrow, m_vec, q0 + i * L, nv[i], xc[i], h, l);
-            }
-#pragma unroll
-            for (int e = 0; e < E; e++) {
-                const float ev = exp_logit<DT>(h[e], l[e], m, c);
-                M::add(acc, ev);
-                if constexpr (KEEP)
-                    zh[i][e] = ev;
             }
         }
-    }
+    };
+    if (pair)
+        exp_pass(std::true_type{});
+    else
+        exp_pass(std::false_type{});
 #pragma unroll
     for (int u = 0; u < NE; u++) {
-        eh[u] = je[u] >= 0 ? exp_logit<DT>(eh[u], el[u], m, c) : 0.f;
+        eh[u] = je[u] >= 0 ? exp_logit<DT, true>(eh[u], el[u], m, c) : 0.f;
         M::add(acc, eh[u]);
     }
     acc = red.sum(acc);
     const float inv = 1.0f / M::value(acc);
     if (!valid)
         return;
+    auto out_pass = [&](auto pair_tag) {
+        constexpr bool P = decltype(pair_tag)::value;
 #pragma unroll
-    for (int i = 0; i < V; i++) {
-        const int q = q0 + i * L;
-        if ((unsigned)q < (unsigned)span) {
-            float o[E];
-            if (nv[i] > 0) {
-                if constexpr (KEEP) {
+        for (int i = 0; i < V; i++) {
+            const int q = q0 + i * L;
+            if ((unsigned)q < (unsigned)span) {
+                float o[E];
+                if (nv[i] > 0) {
+                    if constexpr (KEEP) {
 #pragma unroll
-                    for (int e = 0; e < E; e++)
-                        o[e] = zh[i][e] * inv;
+                        for (int e = 0; e < E; e++)
+                            o[e] = zh[i][e] * inv;
+                    } else {
+                        float h[E], l[E];
+                        opaque(xc[i]);
+                        chunk_logits<DT, MODE, HAS_MASK, P>(a, g, mrow, m_vec, q, nv[i], xc[i], h, l);
+#pragma unroll
+                        for (int e = 0; e < E; e++)
+                            o[e] = exp_logit<DT, P>(h[e], l[e], m, c) * inv;
+                    }
                 } else {
-                    float h[E], l[E];
-                    opaque(xc[i]);
-                    chunk_logits<DT, MODE, HAS_MASK>(a, g, mrow, m_vec, q, nv[i], xc[i], h, l);
 #pragma unroll
                     for (int e = 0; e < E; e++)
-                        o[e] = exp_logit<DT>(h[e], l[e], m, c) * inv;
+                        o[e] = 0.f * inv;  // a cut chunk: exp(-inf) = 0 (NaN for a row with no visible key)
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < E; e++)
-                    o[e] = 0.f * inv;  // a cut chunk: exp(-inf) = 0 (NaN for a row with no visible key)
+                store_interior<DT, PH>(g, q, pack<DT>(o));
             }
-            store_interior<DT, PH>(g, q, pack<DT>(o));
         }
-    }
+    };
+    if constexpr (KEEP)
+        out_pass(std::false_type{});  // the exps are kept
+    else
+        out_pass(std::true_type{});
 #pragma unroll
     for (int u = 0; u < NE; u++)
         if (je[u] >= 0)

@@ -4,6 +4,9 @@
 
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "softmax.h"
 
 struct CUstream_st;
@@ -38,6 +41,33 @@ constexpr int kTmaStaticSmem = 4096;    // BLOCK_TMA static shared memory (barri
 // other's reductions; the register file then bounds threads x registers.
 constexpr int block_max_threads_ct(int v) { return v >= 8 ? 512 : 1024; }
 inline int block_max_threads(int v) { return block_max_threads_ct(v); }
+
+// A per-device initialisation that is remembered only once it has succeeded.
+// run(f) calls f (which returns 0 on success, else an error code) until one
+// call succeeds; later calls return 0 without calling it.  A failed attempt --
+// say, a first call made while the stream is being captured into a graph --
+// leaves nothing behind, so the next call retries it rather than failing for
+// the life of the process.  Thread-safe.
+class InitOnSuccess {
+public:
+    template <class F>
+    int run(F &&f)
+    {
+        if (done_.load(std::memory_order_acquire))
+            return 0;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (done_.load(std::memory_order_relaxed))
+            return 0;
+        const int rc = f();
+        if (rc == 0)
+            done_.store(true, std::memory_order_release);
+        return rc;
+    }
+
+private:
+    std::mutex mu_;
+    std::atomic<bool> done_{false};
+};
 
 struct Launch {
     const void *x;

@@ -12,13 +12,12 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds its 64 KiB until the process exits.  In host code its name is
 // only a host-side stand-in, not a device address; the device address is
-// looked up with cudaGetSymbolAddress once per device, with that device
-// current, on the first call made on that device, and then passed to the
-// kernels.
+// looked up with cudaGetSymbolAddress, with that device current, by the first
+// call made on that device, and then passed to the kernels.  Only a lookup
+// that succeeded is remembered: if it fails (for instance in a first call made
+// while the stream is being captured), the call returns the CUDA error and the
+// next call on that device tries again.
 #include <cuda_runtime.h>
-
-#include <functional>
-#include <mutex>
 
 #include "launch.h"
 #include "softmax.h"
@@ -36,18 +35,20 @@ static __device__ __align__(256) float4 g_noalloc_scratch[kNoAllocSlots];
 namespace {
 
 struct Scratch {
-    std::once_flag once;
-    cudaError_t status = cudaSuccess;
+    InitOnSuccess init;
     float4 *ptr = nullptr;  // device address of g_noalloc_scratch on this device
 };
 
 Scratch g_scratch[64];
 
-void lookup_scratch(Scratch &s)
+int lookup_scratch(Scratch &s)
 {
     void *p = nullptr;
-    s.status = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess)
+        return (int)e;
     s.ptr = static_cast<float4 *>(p);
+    return 0;
 }
 
 }  // namespace
@@ -74,9 +75,9 @@ OSD_API int softmax_fwd_noalloc(const void *x, void *y, int64_t rows, int64_t co
     if (d < 0 || d >= 64)
         return SOFTMAX_ERR_INVALID_ARG;
     Scratch &s = g_scratch[d];
-    std::call_once(s.once, lookup_scratch, std::ref(s));  // device d is current here
-    if (s.status != cudaSuccess)
-        return record_cuda_error((int)s.status);
+    const int le0 = s.init.run([&] { return lookup_scratch(s); });  // device d is current here
+    if (le0 != 0)
+        return record_cuda_error(le0);
     softmax_launch_plan plan;
     rc = softmax_plan(&dev, x, y, rows, cols, dtype, SOFTMAX_VARIANT_SPLITK_WIDE, &plan);
     if (rc != SOFTMAX_OK)
