@@ -14,9 +14,11 @@ step reads x from and writes y to HBM.  value = algorithmic bytes
 Extra keys: `e2e` (the same metric through the public API with pinned host
 buffers, host->device copy of x and device->host copy of y inside the timed
 region), `roofline` (the dominant kernel's achieved bandwidth against the
-measured HBM copy peak), `latency_us` (median single-launch time, cold L2),
-`clocks` (nvidia-smi samples during the timed region), `cpu_baseline` (the
-fp64 oracle on the host's cores over a bounded sample, rank 0 only).
+measured HBM copy peak, and against the rated one), `latency_us` (median
+single-launch time, cold L2), `clocks` (nvidia-smi samples during the timed
+region), `per_config` (the forward softmax of every softmax workload, each
+timed the same way in the same process), `cpu_baseline` (the fp64 oracle on
+all the host's cores and on one core over a bounded sample, rank 0 only).
 
 --impl reference times the oracle itself on the host cores (the pages'
 method has no runnable reference implementation here) on the same config.
@@ -41,6 +43,11 @@ sys.path.insert(0, ROOT)
 METRIC = "softmax GB/s (read+write) and % of GB300 HBM peak; latency at [4,32,512,512] fp16"
 DEFAULT_WORKLOAD = "attn_fp16_65536x512"
 FALLBACK_HBM_GBS = 6800.0
+# NVIDIA's rated HBM3e bandwidth of one GB300 GPU (8 TB/s); the memory clock
+# nvidia-smi reports (3996 MHz, double data rate) on the 8192-bit bus gives
+# 8184 GB/s.  A copy kernel reaches about 6.8 TB/s of it.
+RATED_HBM_GBS = 8000.0
+RATED_SOURCE = "NVIDIA's rated GB300 HBM3e bandwidth, 8 TB/s"
 
 
 def load_peaks() -> dict:
@@ -269,12 +276,66 @@ def oracle_sample_rows(w, target_elems: int = 1 << 25) -> int:
     return max(1, min(w.rows, target_elems // w.cols))
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline_leg(w, op: str) -> dict:
+    """The oracle on all host cores (the sample of oracle_sample_rows), then on
+    one core over a smaller sample; both as GB/s of the same algorithmic bytes."""
+    import oracle
+
+    res = time_oracle(w, op, oracle_sample_rows(w), reps=5, budget_s=20.0)
+    o = oracle.default()
+    all_cores = o.num_threads()
+    o.set_num_threads(1)
+    try:
+        one = time_oracle(w, op, oracle_sample_rows(w, 1 << 22), reps=3, budget_s=15.0)
+    finally:
+        o.set_num_threads(all_cores)
+    res["one_core"] = {"value": one["value"], "unit": "GB/s", "cores": 1, "sample": one["sample"],
+                       "seconds_per_pass": one["seconds_per_pass"]}
+    res["host_cpu"] = {"model": cpu_model(), "os_cpu_count": os.cpu_count()}
+    return res
+
+
+def masked_visible_elems(rows: int, cols: int, causal_q: int) -> int:
+    """Elements of x the causal masked softmax must read: row r sees keys
+    j <= r % causal_q + (cols - causal_q)."""
+    if causal_q <= 0:
+        return rows * cols
+    per_q = [min(cols, max(0, i + (cols - causal_q) + 1)) for i in range(causal_q)]
+    full, rest = divmod(rows, causal_q)
+    return full * sum(per_q) + sum(per_q[:rest])
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 
 def find_workload(W, args):
     """The workload named by --workload (softmax or normalisation workloads);
     --op norm defaults to the first normalisation workload."""
+    if args.shape:
+        rows, cols, dt = args.shape.split(",")
+        if dt not in W.DTYPE_CODES:
+            raise SystemExit(f"--shape dtype must be one of {list(W.DTYPE_CODES)}")
+        return W.Workload(f"shape_{dt}_{int(rows)}x{int(cols)}", int(rows), int(cols), dt, "normal1", 99,
+                          f"{dt} [{int(rows)}, {int(cols)}], N(0, 1) (an ad-hoc shape)")
     name = args.workload
     if args.op == "norm":
         if name == DEFAULT_WORKLOAD:
@@ -372,6 +433,10 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         masked = osd.lib().softmax_fwd_masked
         causal_q = min(512, rows)
         variant = "masked"
+        # the bytes the method must move: the visible part of x (keys past the
+        # causal limit are never read), all of y
+        esz = set_bytes // (2 * rows * cols)
+        set_bytes = masked_visible_elems(rows, cols, causal_q) * esz + rows * cols * esz
         rc, plan = osd.softmax_masked_plan(osd.softmax_device_query()[1], ptrs[0][0], ptrs[0][1], rows, cols, dt)
         if rc != 0:
             raise osd.SoftmaxError(rc)
@@ -517,12 +582,15 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
                    "variant": variant, "plan": plan.as_dict(),
                    "l2": f"rotating {nbuf} buffer sets, {nbuf * set_bytes / 2**20:.0f} MiB > 2x L2 "
                          f"({l2 / 2**20:.0f} MiB)",
-                   "pct_of_peak": round(100 * value / ws / peaks["hbm_gbs"], 2),
+                   "pct_of_peak": round(100 * value / ws / RATED_HBM_GBS, 2),
+                   "pct_of_peak_source": RATED_SOURCE,
+                   "pct_of_measured_peak": round(100 * value / ws / peaks["hbm_gbs"], 2),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "latency_us": round(latency_us, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": f"{peaks['source']} hbm_gbs (copy of 1 Gi bf16)",
+                     "frac_of_rated": round(achieved / RATED_HBM_GBS, 4), "rated_source": RATED_SOURCE,
                      "algorithmic_bytes_per_launch": set_bytes,
                      "traffic": traffic, "traffic_source": tsrc},
         "e2e": {"value": round(set_bytes / (e2e_ms / 1e3) / 1e9 * ws, 2), "unit": "GB/s",
@@ -532,9 +600,94 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         "gpu_launches": args.steps * (2 if variant == "splitk_wide" else 1),
         "clocks": clocks,
     }
+    if args.op == "masked":
+        res["roofline"]["algorithmic_bytes_note"] = (
+            "visible x (keys past the causal limit are never read) + all of y")
+    if per_config_wanted(args):
+        # free the headline's buffers first: the vocabulary workload needs ~8 GB
+        del xs, ys, dev_ins, out_devs
+        torch.cuda.empty_cache()
+        res["per_config"] = run_per_config(args, ws)
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = time_oracle(w, args.op, oracle_sample_rows(w), reps=5, budget_s=20.0)
+        res["cpu_baseline"] = cpu_baseline_leg(w, args.op)
     return res if rank == 0 else None
+
+
+def per_config_wanted(args) -> bool:
+    return (args.op == "forward" and not args.workspace and args.variant is None and args.rows is None
+            and args.shape is None and not args.no_per_config)
+
+
+def time_forward(w, args, ws: int) -> dict:
+    """softmax_fwd on workload w, timed like the headline: W warm-up steps, then
+    K steps between barrier + synchronize, CUDA events on the launching stream,
+    consecutive steps on rotating buffer sets totalling > 2x L2."""
+    import torch
+
+    import online_softmax_dispatcher_gb300 as osd
+    from online_softmax_dispatcher_gb300 import workloads as W
+
+    dev = torch.device("cuda")
+    x_dev = W.as_torch(W.generate(w), w.dtype).to(dev)
+    set_bytes = w.bytes_moved()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nbuf = max(2, -(-int(2.5 * l2) // set_bytes) + 1)
+    xs = [x_dev] + [x_dev.clone() for _ in range(nbuf - 1)]
+    ys = [torch.empty_like(x_dev) for _ in range(nbuf)]
+    plan = osd.plan_for(xs[0], ys[0])
+    variant = osd.softmax_variant_name(plan.variant)
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    fwd = osd.lib().softmax_fwd
+    ptrs = [(a.data_ptr(), b.data_ptr()) for a, b in zip(xs, ys)]
+
+    def step(i):
+        xp, yp = ptrs[i % nbuf]
+        rc = fwd(xp, yp, w.rows, w.cols, w.dtype_code, s)
+        if rc != 0:
+            raise osd.SoftmaxError(rc)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    peaks = load_peaks()
+    gbs = set_bytes * args.steps * ws / (ms / 1e3) / 1e9
+    traffic, tsrc = recorded_traffic(w.name, variant, plan.as_dict())
+    out = {"workload": w.name, "rows": w.rows, "cols": w.cols, "dtype": w.dtype, "variant": variant,
+           "plan": plan.as_dict(), "ms_per_step": round(ms / args.steps, 5), "value": round(gbs, 2),
+           "unit": "GB/s", "frac": round(gbs / ws / peaks["hbm_gbs"], 4),
+           "frac_of_rated": round(gbs / ws / RATED_HBM_GBS, 4), "algorithmic_bytes_per_launch": set_bytes,
+           "traffic_ratio": round(traffic / set_bytes, 4) if traffic else None, "traffic_source": tsrc,
+           "l2": f"rotating {nbuf} buffer sets, {nbuf * set_bytes / 2**20:.0f} MiB"}
+    del xs, ys, x_dev
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_per_config(args, ws: int) -> dict:
+    """Every softmax workload but the headline's, through softmax_fwd, timed
+    with the same --steps / --warmup; clocks sampled over the whole set."""
+    from online_softmax_dispatcher_gb300 import workloads as W
+
+    rank = int(os.environ.get("RANK", "0"))
+    sampler = ClockSampler(gpu_id_for_nvsmi()).start() if rank == 0 else None
+    t0 = time.time()
+    lines = [time_forward(w, args, ws) for name, w in W.WORKLOADS.items() if name != args.workload]
+    t1 = time.time()
+    samples = sampler.stop() if sampler is not None else []
+    return {"timing": "same --steps/--warmup as the headline, CUDA events, rotating buffers > 2x L2",
+            "peak": load_peaks()["hbm_gbs"], "rated_peak": RATED_HBM_GBS, "lines": lines,
+            "clocks": summarize_clocks(samples, t0, t1)}
 
 
 def run_reference(args, rank: int, ws: int) -> dict | None:
@@ -572,6 +725,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--shape", default=None, metavar="ROWS,COLS,DTYPE",
+                    help="an ad-hoc softmax shape instead of --workload: N(0, 1) inputs of that shape and dtype "
+                         "(fp32, fp16, bf16), for sweeps and per-kernel profiles")
     ap.add_argument("--rows", type=int, default=None,
                     help="time only the first ROWS rows of the workload (for small profiling captures)")
     ap.add_argument("--op", choices=("forward", "backward", "masked", "norm"), default="forward",
@@ -588,7 +744,11 @@ def main():
                          "splitk_grid) through softmax_fwd_variant instead of the dispatcher's choice; a variant "
                          "that cannot serve the shape prints an 'unsupported' line and exits 0")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config lines (the forward softmax of every other softmax workload)")
     args = ap.parse_args()
+    if args.shape is not None and args.op == "norm":
+        ap.error("--shape is for the softmax operations (norm workloads are named by --workload)")
     if args.variant is not None and (args.op != "forward" or args.workspace):
         ap.error("--variant applies to the forward softmax without --workspace")
     if args.warmup < 3:

@@ -149,8 +149,9 @@ int softmax_fwd_variant(const void *x, void *y, int64_t rows, int64_t cols, int 
  * Accuracy: as softmax_fwd (fp32 2e-6 relative; fp16 / bf16 within 1 ulp of
  * the correctly rounded result) against the exact softmax of z formed from
  * the float `scale` as passed, whatever the size of the logits: fp32 carries
- * z as a two-float pair, fp16 / bf16 rows whose largest logit reaches 512 in
- * magnitude do too (below that one fp32 FMA is accurate enough).
+ * z as a two-float pair; fp16 / bf16 form z - max with a rounding relative to
+ * z - max itself wherever the row's largest logit reaches 512 in magnitude
+ * (below that one fp32 FMA for z is accurate enough).
  * Rows up to 2048 chunks of 16 bytes (32 KiB: 16384 fp16 / bf16 or 8192 fp32
  * keys): SOFTMAX_ERR_UNSUPPORTED_SHAPE beyond.  Alignment, streams, errors:
  * as softmax_fwd.

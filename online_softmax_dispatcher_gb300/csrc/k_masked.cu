@@ -11,14 +11,20 @@
 // * fp32: z is kept as an unevaluated pair zh + zl (the product split exactly
 //   by an FMA, the mask added with TwoSum), and exp(z - m) = expf(th)
 //   (1 + tl + zl) with th + tl = zh - m exactly, so fp32 keeps its 2e-6 bound.
-// * fp16 / bf16: z is one fp32 FMA, whose rounding moves exp(z_j - m) by up to
-//   2^-24 (|z_j| + |m|) relative.  An output that is not below the 16-bit
-//   range has z_j >= m - 100, so while |m| < kPairFreeMax = 512 that is under
+// * fp16 / bf16: the max pass takes z as one fp32 FMA (any shift m works:
+//   softmax does not depend on it).  Its rounding moves exp(z_j - m) by up to
+//   2^-24 (|z_j| + |m|) relative; an output that is not below the 16-bit range
+//   has z_j >= m - 100, so while |m| < kPairFreeMax = 512 that stays under
 //   2^-24 * 1124 = 6.7e-5, well inside half an fp16 ulp (2^-12 at least), and
-//   the row keeps its single-float logits.  A row whose max logit is larger in
-//   magnitude forms the pairs (re-reading x where the kernel kept only the
-//   logits) and exponentiates 2^((zh - m) log2e + zl log2e) by two FMAs, so
-//   the bound of the plain softmax holds whatever the size of the logits.
+//   the exps are taken from those logits.  Otherwise the shifted logit
+//   t = z - m is formed directly from x: fma(scale, x, -m) rounds the exact
+//   product minus m once (with a mask, (mask - m) is first split exactly by
+//   TwoSum), so t carries an error of about 2^-24 |t|, not 2^-24 |z|, and the
+//   16-bit outputs keep the bound of the plain softmax however large the
+//   logits are.  The CTA-per-row form always does this (it forms the logits
+//   again in each pass anyway); the lanes-per-row form sends a warp with such
+//   a row down a separate, rare path (masked_row_shifted) so that the common
+//   path keeps its registers.
 // * ROWGROUP form (G lanes per row, the logits kept in registers) for rows of
 //   up to 32 lanes x 32 floats; BLOCK form (one CTA per row, x kept packed in
 //   registers, the mask chunk re-read through L1 and the logits recomputed in
@@ -29,8 +35,6 @@
 //   computed once: chunks wholly past the causal limit are not read, only the
 //   one the limit falls in cuts values one by one.  The mask's presence and
 //   the rows' 16-byte phases are template parameters.
-#include <type_traits>
-
 #include "common.cuh"
 #include "launch.h"
 
@@ -74,81 +78,71 @@ constexpr int kMFast = 0;
 constexpr int kMSame = 1;
 constexpr int kMOther = 2;
 
-// 16-bit rows whose max logit is smaller than this in magnitude need no low
-// parts (the header's bound).
+// 16-bit rows of the lanes-per-row form whose max logit is smaller than this
+// in magnitude take their exps from the single-float logits (the header's
+// bound).
 constexpr float kPairFreeMax = 512.f;
 
-// exp(z - m) for a logit z = zh + zl (PAIR) or zh.  16-bit: one FMA
-// z log2e + c with c = bias - m log2e, computed once per row (the rounding of
-// m log2e scales the whole row's exps by one common factor, which the
-// normalisation cancels), and with a pair a second FMA adding zl log2e.
-template <int DT, bool PAIR>
-__device__ __forceinline__ float exp_logit(float zh, float zl, float m, float c)
+// exp(z - m) for an fp32 logit z = zh + zl.
+__device__ __forceinline__ float exp_logit32(float zh, float zl, float m)
 {
-    if constexpr (DT == kF32) {
-        float th, tl;
-        two_sum(zh, -m, th, tl);
-        const float e = expf(th);
-        const float r = tl + zl;
-        return (fabsf(r) < INFINITY) ? fmaf(e, r, e) : e;
-    } else if constexpr (PAIR) {
-        (void)m;
-        return ex2_ftz(fmaf(zl, kLog2e, fmaf(zh, kLog2e, c)));
+    float th, tl;
+    two_sum(zh, -m, th, tl);
+    const float e = expf(th);
+    const float r = tl + zl;
+    return (fabsf(r) < INFINITY) ? fmaf(e, r, e) : e;
+}
+
+// t = scale * x + mv - m for a 16-bit value, rounded about once relative to
+// t itself (the header's account).  A -inf mask or a NaN leaves t -inf or
+// NaN, as the definition does.
+template <bool HAS_MASK>
+__device__ __forceinline__ float shifted_logit16(float scale, float xv, float mv, float m)
+{
+    if constexpr (HAS_MASK) {
+        float uh, ul;
+        two_sum(mv, -m, uh, ul);
+        const float t = fmaf(scale, xv, uh);
+        return fabsf(ul) < INFINITY ? t + ul : t;
     } else {
-        (void)m;
-        (void)zl;
-        return ex2_ftz(fmaf(zh, kLog2e, c));
+        (void)mv;
+        return fmaf(scale, xv, -m);
     }
 }
 
+// The (scaled) 16-bit exp of a shifted logit: 2^(t log2e + bias), the bias of
+// Math<DT> (bf16 keeps its subnormal outputs; it cancels in y).
 template <int DT>
-__device__ __forceinline__ float exp_offset(float m)
+__device__ __forceinline__ float exp_shifted16(float t)
 {
-    if constexpr (DT == kF32)
-        return 0.f;
-    else
-        return Math<DT>::kExpBias - m * kLog2e;
+    return ex2_ftz(fmaf(t, kLog2e, DT == kBF16 ? Math<kBF16>::kExpBias : 0.f));
 }
 
-// The logit of one value.  PAIR: zh + zl = scale * x + mv up to a rounding of
-// the (tiny) low part; where zh is not finite (a -inf mask or input cuts the
-// value, or a NaN) zl is 0, so that it cannot turn the cut value's exp into
-// NaN.  Else zh = scale * x + mv by one FMA and zl = 0.
-template <bool PAIR, bool HAS_MASK>
+// The logit of one value: zh (and the fp32 low part zl) of scale * x + mv.
+template <int DT>
 __device__ __forceinline__ void logit(float scale, float xv, float mv, float &zh, float &zl)
 {
-    if constexpr (PAIR) {
+    if constexpr (DT == kF32) {
         const float ph = scale * xv;
-        const float pl = fmaf(scale, xv, -ph);  // exact: scale * x = ph + pl
-        if constexpr (HAS_MASK) {
-            float s, err;
-            two_sum(ph, mv, s, err);
-            zh = s;
-            zl = err + pl;
-        } else {
-            (void)mv;
-            zh = ph;
-            zl = pl;
-        }
-        if (!(fabsf(zh) < INFINITY))
-            zl = 0.f;
+        const float pl = fmaf(scale, xv, -ph);
+        float s, err;
+        two_sum(ph, mv, s, err);
+        zh = s;
+        zl = err + pl;
     } else {
         zh = fmaf(scale, xv, mv);
         zl = 0.f;
     }
 }
 
-// Logits of interior chunk q holding nv visible values (0 < nv <= E); slots
-// past nv are cut to -inf.
-template <int DT, int MODE, bool HAS_MASK, bool PAIR>
-__device__ __forceinline__ void chunk_logits(const MaskedArgs &a, const ShortRow &g, const char *mrow, bool m_vec,
-                                             int q, int nv, const uint4 &xc, float (&zh)[Fmt<DT>::kPerChunk],
-                                             float (&zl)[Fmt<DT>::kPerChunk])
+// The mask values of interior chunk q: one vector load where the mask row
+// shares x's 16-byte phase, else element by element.
+template <int DT, int MODE, bool HAS_MASK>
+__device__ __forceinline__ void chunk_mask(const ShortRow &g, const char *mrow, bool m_vec, int q,
+                                           float (&mf)[Fmt<DT>::kPerChunk])
 {
     constexpr int E = Fmt<DT>::kPerChunk;
     constexpr int S = Fmt<DT>::kBytes;
-    float xf[E], mf[E];
-    unpack<DT>(xc, xf);
     if constexpr (HAS_MASK) {
         if (MODE == kMFast || m_vec) {
             unpack<DT>(ld_chunk_cached(mrow - g.head * S + ((int64_t)(g.kf + q) << 4)), mf);
@@ -158,10 +152,27 @@ __device__ __forceinline__ void chunk_logits(const MaskedArgs &a, const ShortRow
             for (int e = 0; e < E; e++)
                 mf[e] = ld_elem<DT>(mrow, j0 + e);
         }
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; e++)
+            mf[e] = 0.f;
     }
+}
+
+// Logits of interior chunk q holding nv visible values (0 < nv <= E); slots
+// past nv are cut to -inf.
+template <int DT, int MODE, bool HAS_MASK>
+__device__ __forceinline__ void chunk_logits(const MaskedArgs &a, const ShortRow &g, const char *mrow, bool m_vec,
+                                             int q, int nv, const uint4 &xc, float (&zh)[Fmt<DT>::kPerChunk],
+                                             float (&zl)[Fmt<DT>::kPerChunk])
+{
+    constexpr int E = Fmt<DT>::kPerChunk;
+    float xf[E], mf[E];
+    unpack<DT>(xc, xf);
+    chunk_mask<DT, MODE, HAS_MASK>(g, mrow, m_vec, q, mf);
 #pragma unroll
     for (int e = 0; e < E; e++)
-        logit<PAIR, HAS_MASK>(a.scale, xf[e], HAS_MASK ? mf[e] : 0.f, zh[e], zl[e]);
+        logit<DT>(a.scale, xf[e], mf[e], zh[e], zl[e]);
     if (nv < E) {
 #pragma unroll
         for (int e = 0; e < E; e++)
@@ -169,6 +180,30 @@ __device__ __forceinline__ void chunk_logits(const MaskedArgs &a, const ShortRow
                 zh[e] = -INFINITY;
                 zl[e] = 0.f;
             }
+    }
+}
+
+// The exps exp(z - m) of interior chunk q (0 for the slots past nv), formed
+// from x: fp32 through the logit pairs, 16-bit through the shifted logits.
+template <int DT, int MODE, bool HAS_MASK>
+__device__ __forceinline__ void chunk_exps(const MaskedArgs &a, const ShortRow &g, const char *mrow, bool m_vec,
+                                           int q, int nv, const uint4 &xc, float m,
+                                           float (&ev)[Fmt<DT>::kPerChunk])
+{
+    constexpr int E = Fmt<DT>::kPerChunk;
+    if constexpr (DT == kF32) {
+        float h[E], l[E];
+        chunk_logits<DT, MODE, HAS_MASK>(a, g, mrow, m_vec, q, nv, xc, h, l);
+#pragma unroll
+        for (int e = 0; e < E; e++)
+            ev[e] = exp_logit32(h[e], l[e], m);
+    } else {
+        float xf[E], mf[E];
+        unpack<DT>(xc, xf);
+        chunk_mask<DT, MODE, HAS_MASK>(g, mrow, m_vec, q, mf);
+#pragma unroll
+        for (int e = 0; e < E; e++)
+            ev[e] = e < nv ? exp_shifted16<DT>(shifted_logit16<HAS_MASK>(a.scale, xf[e], mf[e], m)) : 0.f;
     }
 }
 
@@ -205,16 +240,39 @@ struct MaxSumGroup {
     }
 };
 
-// One row for a team of L threads.  KEEP: the logits, then their exps, stay in
-// registers (lanes per row); else x stays packed and the logits are recomputed
-// in each pass (CTA per row, with the 128-byte-line chunk map).  Interior
-// chunks wholly past the causal limit are neither read nor exponentiated; only
-// the chunk the limit falls in tests its values one by one.  16-bit rows take
-// single-float logits in the max pass.  Without KEEP the later passes form
-// pairs (they form the logits again anyway).  KEEP rows form pairs only when
-// the max turns out large in magnitude (a decision the whole team shares, as
-// it shares m), reading x again for them (from L2: the row was just loaded,
-// and no output of it is stored yet, so an in-place call reads x too).
+// The rest of a 16-bit row for the lanes-per-row form once its max m is known
+// and at least kPairFreeMax in magnitude: every visible value again, from x
+// read element by element (from L2: the row was just loaded, and none of its
+// output is stored yet, so an in-place call still reads x), its exp taken
+// from the shifted logit -- once for the sum, once for the output.  Out of
+// line and with only values as arguments, so that this rare path adds no
+// registers or local memory to the common one.  Lane `lane` of a team of L
+// takes elements lane, lane + L, ...  Called by whole warps.
+template <int DT, bool HAS_MASK, class Red>
+__device__ __noinline__ void masked_row_shifted(const char *xr, char *yr, const char *mrow, int cols, int lim,
+                                                float scale, float m, int lane, int L, bool valid, Red red)
+{
+    float acc = 0.f;
+    for (int j = lane; j < lim; j += L)
+        acc += exp_shifted16<DT>(
+            shifted_logit16<HAS_MASK>(scale, ld_elem<DT>(xr, j), HAS_MASK ? ld_elem<DT>(mrow, j) : 0.f, m));
+    acc = red.sum(acc);
+    const float inv = 1.0f / acc;
+    if (!valid)
+        return;
+    for (int j = lane; j < cols; j += L) {
+        const float e = j < lim ? exp_shifted16<DT>(shifted_logit16<HAS_MASK>(
+                                      scale, ld_elem<DT>(xr, j), HAS_MASK ? ld_elem<DT>(mrow, j) : 0.f, m))
+                                : 0.f;
+        st_elem<DT>(yr, j, e * inv);
+    }
+}
+
+// One row for a team of L threads.  KEEP: the logits, then their exps, stay
+// in registers (lanes per row); else x stays packed and the exps are formed
+// again for the output (CTA per row, with the 128-byte-line chunk map).  Interior chunks wholly past the causal limit are neither read nor
+// exponentiated; only the chunk the limit falls in tests its values one by
+// one.
 template <int DT, int V, int MODE, bool HAS_MASK, int NE, bool KEEP, class Red>
 __device__ __forceinline__ void masked_row(const MaskedArgs &a, int64_t r, bool valid, int lane, int L, Red red)
 {
@@ -222,7 +280,7 @@ __device__ __forceinline__ void masked_row(const MaskedArgs &a, int64_t r, bool 
     constexpr int E = Fmt<DT>::kPerChunk;
     constexpr int S = Fmt<DT>::kBytes;
     constexpr int PH = MODE == kMFast ? kPhAligned : (MODE == kMSame ? kPhSame : kPhOther);
-    constexpr bool PAIR1 = DT == kF32;  // the max pass forms pairs (fp32 always needs them)
+    constexpr bool KEEP_Z = KEEP && DT == kF32;  // fp32 logit pairs kept from the max pass
     const int64_t rr = valid ? r : 0;
     const ShortRow g = short_row<DT, MODE == kMFast>(a.x, a.y, rr, (int)a.cols);
     const char *mrow = HAS_MASK ? a.mask + (rr % a.mask_rows) * a.cols * S : nullptr;
@@ -248,123 +306,124 @@ __device__ __forceinline__ void masked_row(const MaskedArgs &a, int64_t r, bool 
         nv[i] = (unsigned)q < (unsigned)span ? (left < 0 ? 0 : (left > E ? E : left)) : 0;
         xc[i] = nv[i] > 0 ? ld_chunk(g.x0 + ((int64_t)(g.kf + q) << 4)) : make_uint4(0, 0, 0, 0);
     }
-    // edge elements (a few per lane at most) always carry pairs
+    // edge elements: fp32 keeps the logit pair (eh, el), 16-bit the value and
+    // its mask value; ev the exp once m is known
     int je[NE > 0 ? NE : 1];
     float eh[NE > 0 ? NE : 1], el[NE > 0 ? NE : 1];
+    float m = -INFINITY;
 #pragma unroll
     for (int u = 0; u < NE; u++) {
         const int p = lane + u * L;
         je[u] = (valid && p < g.ne) ? edge_col(g, p) : -1;
         eh[u] = -INFINITY;
         el[u] = 0.f;
-        if (je[u] >= 0 && je[u] < lim)
-            logit<true, HAS_MASK>(a.scale, ld_elem<DT>(g.xr, je[u]), HAS_MASK ? ld_elem<DT>(mrow, je[u]) : 0.f,
-                                  eh[u], el[u]);
+        if (je[u] >= 0 && je[u] < lim) {
+            const float xv = ld_elem<DT>(g.xr, je[u]), mv = HAS_MASK ? ld_elem<DT>(mrow, je[u]) : 0.f;
+            if constexpr (DT == kF32) {
+                logit<DT>(a.scale, xv, mv, eh[u], el[u]);
+                m = fmaxf(m, eh[u]);
+            } else {
+                eh[u] = xv;
+                el[u] = mv;
+                float zh, zl;
+                logit<DT>(a.scale, xv, mv, zh, zl);
+                m = fmaxf(m, zh);
+            }
+        }
     }
 
-    float zh[KEEP ? V : 1][E], zl[KEEP && PAIR1 ? V : 1][E];
-    float m = -INFINITY;
+    float zh[KEEP ? V : 1][E], zl[KEEP_Z ? V : 1][E];
 #pragma unroll
     for (int i = 0; i < V; i++) {
         if (nv[i] > 0) {
             float h[E], l[E];
-            chunk_logits<DT, MODE, HAS_MASK, PAIR1>(a, g, mrow, m_vec, q0 + i * L, nv[i], xc[i], h, l);
+            chunk_logits<DT, MODE, HAS_MASK>(a, g, mrow, m_vec, q0 + i * L, nv[i], xc[i], h, l);
 #pragma unroll
             for (int e = 0; e < E; e++) {
                 m = fmaxf(m, h[e]);
-                if constexpr (KEEP) {
+                if constexpr (KEEP)
                     zh[i][e] = h[e];
-                    if constexpr (PAIR1)
-                        zl[i][e] = l[e];
-                }
+                if constexpr (KEEP_Z)
+                    zl[i][e] = l[e];
+            }
+        }
+    }
+    m = red.max(m);
+    if constexpr (KEEP && DT != kF32) {
+        // warp-uniform, so that the reductions inside stay converged
+        if (__any_sync(0xffffffffu, !(fabsf(m) < kPairFreeMax))) {
+            masked_row_shifted<DT, HAS_MASK>(g.xr, g.yr, mrow, (int)a.cols, lim, a.scale, m, lane, L, valid, red);
+            return;
+        }
+    }
+    // 16-bit rows of the lanes-per-row form: exp(zh - m) = 2^(zh log2e + c)
+    // with c = bias - m log2e formed once (its rounding scales the whole row's
+    // exps by one factor, which the normalisation cancels)
+    const float c16 = DT == kBF16 ? Math<kBF16>::kExpBias - m * kLog2e : -m * kLog2e;
+
+    typename M::Acc acc = M::zero();
+#pragma unroll
+    for (int i = 0; i < V; i++) {
+        if (nv[i] > 0) {
+            float ev[E];
+            if constexpr (KEEP_Z) {
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    ev[e] = exp_logit32(zh[i][e], zl[i][e], m);
+            } else if constexpr (KEEP) {
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    ev[e] = ex2_ftz(fmaf(zh[i][e], kLog2e, c16));
+            } else {
+                opaque(xc[i]);
+                chunk_exps<DT, MODE, HAS_MASK>(a, g, mrow, m_vec, q0 + i * L, nv[i], xc[i], m, ev);
+            }
+#pragma unroll
+            for (int e = 0; e < E; e++) {
+                M::add(acc, ev[e]);
+                if constexpr (KEEP)
+                    zh[i][e] = ev[e];
             }
         }
     }
 #pragma unroll
-    for (int u = 0; u < NE; u++)
-        m = fmaxf(m, eh[u]);
-    m = red.max(m);
-    const float c = exp_offset<DT>(m);
-    const bool pair = PAIR1 || !KEEP || !(fabsf(m) < kPairFreeMax);
-
-    // exps of the interior chunks, summed (and kept, KEEP)
-    typename M::Acc acc = M::zero();
-    auto exp_pass = [&](auto pair_tag) {
-        constexpr bool P = decltype(pair_tag)::value;
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            if (nv[i] > 0) {
-                float h[E], l[E];
-                if constexpr (KEEP && P == PAIR1) {
-#pragma unroll
-                    for (int e = 0; e < E; e++) {
-                        h[e] = zh[i][e];
-                        l[e] = PAIR1 ? zl[i][e] : 0.f;
-                    }
-                } else if constexpr (KEEP) {
-                    // 16-bit row with large logits: x again, for the pairs
-                    const uint4 xr = ld_chunk(g.x0 + ((int64_t)(g.kf + q0 + i * L) << 4));
-                    chunk_logits<DT, MODE, HAS_MASK, P>(a, g, mrow, m_vec, q0 + i * L, nv[i], xr, h, l);
-                } else {
-                    opaque(xc[i]);
-                    chunk_logits<DT, MODE, HAS_MASK, P>(a, g, mrow, m_vec, q0 + i * L, nv[i], xc[i], h, l);
-                }
-#pragma unroll
-                for (int e = 0; e < E; e++) {
-                    const float ev = exp_logit<DT, P>(h[e], l[e], m, c);
-                    M::add(acc, ev);
-                    if constexpr (KEEP)
-                        zh[i][e] = ev;
-                }
-            }
-        }
-    };
-    if (pair)
-        exp_pass(std::true_type{});
-    else
-        exp_pass(std::false_type{});
-#pragma unroll
     for (int u = 0; u < NE; u++) {
-        eh[u] = je[u] >= 0 ? exp_logit<DT, true>(eh[u], el[u], m, c) : 0.f;
+        if constexpr (DT == kF32)
+            eh[u] = je[u] >= 0 ? exp_logit32(eh[u], el[u], m) : 0.f;
+        else
+            eh[u] = (je[u] >= 0 && je[u] < lim) ? exp_shifted16<DT>(shifted_logit16<HAS_MASK>(a.scale, eh[u], el[u], m))
+                                                : 0.f;
         M::add(acc, eh[u]);
     }
     acc = red.sum(acc);
     const float inv = 1.0f / M::value(acc);
     if (!valid)
         return;
-    auto out_pass = [&](auto pair_tag) {
-        constexpr bool P = decltype(pair_tag)::value;
 #pragma unroll
-        for (int i = 0; i < V; i++) {
-            const int q = q0 + i * L;
-            if ((unsigned)q < (unsigned)span) {
-                float o[E];
-                if (nv[i] > 0) {
-                    if constexpr (KEEP) {
-#pragma unroll
-                        for (int e = 0; e < E; e++)
-                            o[e] = zh[i][e] * inv;
-                    } else {
-                        float h[E], l[E];
-                        opaque(xc[i]);
-                        chunk_logits<DT, MODE, HAS_MASK, P>(a, g, mrow, m_vec, q, nv[i], xc[i], h, l);
-#pragma unroll
-                        for (int e = 0; e < E; e++)
-                            o[e] = exp_logit<DT, P>(h[e], l[e], m, c) * inv;
-                    }
-                } else {
+    for (int i = 0; i < V; i++) {
+        const int q = q0 + i * L;
+        if ((unsigned)q < (unsigned)span) {
+            float o[E];
+            if (nv[i] > 0) {
+                if constexpr (KEEP) {
 #pragma unroll
                     for (int e = 0; e < E; e++)
-                        o[e] = 0.f * inv;  // a cut chunk: exp(-inf) = 0 (NaN for a row with no visible key)
+                        o[e] = zh[i][e] * inv;
+                } else {
+                    opaque(xc[i]);
+                    chunk_exps<DT, MODE, HAS_MASK>(a, g, mrow, m_vec, q, nv[i], xc[i], m, o);
+#pragma unroll
+                    for (int e = 0; e < E; e++)
+                        o[e] *= inv;
                 }
-                store_interior<DT, PH>(g, q, pack<DT>(o));
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    o[e] = 0.f * inv;  // a cut chunk: exp(-inf) = 0 (NaN for a row with no visible key)
             }
+            store_interior<DT, PH>(g, q, pack<DT>(o));
         }
-    };
-    if constexpr (KEEP)
-        out_pass(std::false_type{});  // the exps are kept
-    else
-        out_pass(std::true_type{});
+    }
 #pragma unroll
     for (int u = 0; u < NE; u++)
         if (je[u] >= 0)

@@ -747,8 +747,15 @@ extern "C" __attribute__((visibility("default"))) int softmax_plan(
     if (v == SOFTMAX_VARIANT_AUTO) {
         const bool few_rows = rows * 2 <= dev->sm_count;
         const bool long_rows = g.nch_max >= int64_t(8) * (kSplitStageBytes / 16);
-        if (rowgroup_fits(g))
+        // a row to itself on an SM (rows <= SMs) that one warp would hold at
+        // more than 4 chunks a lane (fp32 rows of 129 - 256 chunks): one CTA
+        // per row spreads it over two warps ([128, 1000] fp32: 339 - 366 GB/s
+        // against 326 - 353 for one warp a row; launch-bound either way)
+        const bool lone_wide_rows = rows <= dev->sm_count && g.nint > int64_t(32) * 4;
+        if (rowgroup_fits(g) && !lone_wide_rows)
             v = SOFTMAX_VARIANT_ROWGROUP;
+        else if (rowgroup_fits(g))
+            v = SOFTMAX_VARIANT_BLOCK;
         else if (few_rows && long_rows && grid_possible(rows, *dev))
             v = SOFTMAX_VARIANT_SPLITK_GRID;
         else if (few_rows && long_rows && splitk_possible(rows, *dev))

@@ -139,6 +139,7 @@ class Oracle:
                                    ctypes.c_double, i64, ctypes.c_double, ctypes.c_double,
                                    ctypes.POINTER(CheckResult)]
         L.oracle_num_threads.argtypes = []
+        L.oracle_set_num_threads.argtypes = [i32]
         L.oracle_softmax_bwd_f64.argtypes = [vp, vp, i64, i64, vp]
         L.oracle_softmax_masked.argtypes = [vp, i32, i64, i64, ctypes.c_double, vp, i64, i64, vp]
         L.oracle_check_masked.argtypes = [vp, vp, i32, i64, i64, ctypes.c_double, vp, i64, i64, ctypes.c_double,
@@ -150,7 +151,7 @@ class Oracle:
         L.oracle_check_norm.argtypes = [i32, vp, vp, i32, i64, i64, vp, vp, ctypes.c_double, vp, vp,
                                         ctypes.c_double, i64, ctypes.c_double, ctypes.POINTER(CheckResult)]
         for name in ("oracle_decode", "oracle_encode", "oracle_softmax_f64", "oracle_softmax",
-                     "oracle_online_softmax_f64", "oracle_check", "oracle_num_threads",
+                     "oracle_online_softmax_f64", "oracle_check", "oracle_num_threads", "oracle_set_num_threads",
                      "oracle_softmax_bwd_f64", "oracle_check_bwd", "oracle_softmax_masked",
                      "oracle_check_masked", "oracle_norm_f64", "oracle_check_norm"):
             getattr(L, name).restype = ctypes.c_int
@@ -341,6 +342,10 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
+
+    def set_num_threads(self, n: int) -> int:
+        """OpenMP threads for later oracle calls from this host thread; returns the number in force."""
+        return int(self.lib.oracle_set_num_threads(int(n)))
 
 
 def default() -> Oracle:

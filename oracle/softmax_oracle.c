@@ -608,6 +608,21 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Set the number of OpenMP threads later parallel regions started from the
+ * calling host thread use (n >= 1; the CPU baseline times the oracle on all
+ * cores and on one).  Returns the number in force afterwards. */
+int oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 /* ------------------------------------------------------------------------ */
 /* backward: dx = y * (dy - sum_k dy_k y_k)                                   */
 /* ------------------------------------------------------------------------ */
