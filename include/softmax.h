@@ -97,7 +97,11 @@ typedef enum {
                                         grid_y groups of grid_x CTAs, one CTA per SM, a group
                                         takes every grid_y-th row in turn, each CTA's share of
                                         a row held in one of `stages` shared-memory buffers (one
-                                        HBM read); streaming form (stages 0): grid_y = rows */
+                                        HBM read); pipelined form (lanes_per_row > 0): grid_y =
+                                        1, every CTA on every row, the rows in turn through the
+                                        buffers, a fold team of lanes_per_row threads working on
+                                        one row while the rest of the CTA writes the row before;
+                                        streaming form (stages 0): grid_y = rows */
     SOFTMAX_VARIANT_COUNT = 8
 } softmax_variant;
 
@@ -318,7 +322,8 @@ typedef struct {
 typedef struct {
     int variant;            /* softmax_variant chosen (never AUTO) */
     int lanes_per_row;      /* threads that share one row: ROWGROUP G (1..32); BLOCK_TMA
-                               32 x warps per row group (32..512); else 0 */
+                               32 x warps per row group (32..512); SPLITK_GRID pipelined
+                               form: threads of a CTA that fold (the rest write); else 0 */
     int chunks_per_thread;  /* 16-byte chunks each thread caches (ROWGROUP, BLOCK), or loads in
                                flight per thread per streaming step (STREAM, SPLITK); else 0 */
     int rows_per_tile;      /* BLOCK_TMA: consecutive rows moved by one bulk copy; else 0 */

@@ -67,6 +67,7 @@ struct GridArgs {
     unsigned *arrive;  // [rows][2] arrival counters, one per launch parity
     unsigned gen;      // this launch's number in its slot (its parity picks the counter)
     unsigned *err;
+    int nf;            // pipelined form: threads that fold (the rest write); 0 in the other forms
 };
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
@@ -167,64 +168,94 @@ __device__ __forceinline__ void md_absorb(MD &md, const uint4 (&raw)[K])
     md.d += (s[0] + s[1]) + (s[2] + s[3]);
 }
 
-// merge_partials spread over the CTA: thread i loads partial i (all P in one
-// round trip through L2 rather than P / 32 dependent ones per warp), then the
-// block reductions combine them in a fixed order, so every CTA of the row holds
-// bit-identical (m, 1/d).  All threads call it.
-template <int DT>
-__device__ __forceinline__ void merge_partials_cta(const float4 *ws, int64_t r, int P, float &m, float &inv,
-                                                   float *smax, typename Math<DT>::Acc *ssum, MD *smd)
+// ---------------------------------------------------------------- team reductions
+
+constexpr int kPipeMaxPerLane = kGridPipeMaxCtas / 32;  // partials each lane of the merging warp holds
+// Bulk copies per share in the pipelined form.  Its shares are a quarter to a
+// half of the ring form's, and a fold thread must find several chunks per
+// piece to keep independent work in flight: with 8 pieces it found one or two,
+// and the fold became a chain of dependent steps (0.35 us a piece).
+constexpr int kPipePieces = 2;
+
+__device__ __forceinline__ void named_sync(int id, int n)
 {
-    const int T = blockDim.x;
-    if constexpr (DT == kF32) {
-        float4 q[2];
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// (m, d) over a warp: the max in one instruction, each lane's sum rescaled to
+// it once, then an xor butterfly of plain additions (both partners of a step
+// add the same two numbers, so every lane ends with the same value).
+template <int DT>
+__device__ __forceinline__ MD warp_md_max_first(MD v)
+{
+    const float m = warp_max_redux(v.m);
+    float d = (v.m == -INFINITY) ? 0.f : v.d * Math<DT>::exp_of(v.m - m);
 #pragma unroll
-        for (int j = 0; j < 2; j++) {
-            const int i = threadIdx.x + j * T;
-            q[j] = i < P ? __ldcg(&ws[r * P + i]) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-        }
-        float mloc = fmaxf(q[0].x, q[1].x);
-        for (int i = threadIdx.x + 2 * T; i < P; i += T)
-            mloc = fmaxf(mloc, __ldcg(&ws[r * P + i]).x);
-        m = block_max(mloc, smax);
-        CSum acc{0.f, 0.f};
-        auto add = [&](const float4 &v) {
-            if (v.x != -INFINITY) {
-                const float f = Math<kF32>::exp_shift(v.x, m);
-                Math<kF32>::add(acc, v.y * f);
-                Math<kF32>::add(acc, v.z * f);
-            }
-        };
-        add(q[0]);
-        add(q[1]);
-        for (int i = threadIdx.x + 2 * T; i < P; i += T)
-            add(__ldcg(&ws[r * P + i]));
-        acc = block_sum<kF32>(acc, ssum);
-        inv = 1.0f / (acc.s + acc.c);
-    } else {
-        MD md{-INFINITY, 0.f};
-        for (int i = threadIdx.x; i < P; i += T) {
-            const float4 v = __ldcg(&ws[r * P + i]);
-            md = md_merge<DT>(md, MD{v.x, v.y});
-        }
-        md = block_md<DT>(md, smd);
-        m = md.m;
-        inv = 1.0f / md.d;
+    for (int o = 16; o > 0; o >>= 1)
+        d += __shfl_xor_sync(0xFFFFFFFFu, d, o);
+    return MD{m, d};
+}
+
+// The P partials of row r merged by one warp: lane i loads partials i, i + 32,
+// ... (one round trip through L2), the max in one instruction, then the
+// rescaled sums -- each lane in a fixed order, then an xor butterfly -- so
+// every CTA of the row computes bit-identical (m, 1/d).  Called by a whole
+// warp after an acquire of the row's count that the warp has synchronised on.
+template <int DT>
+__device__ __forceinline__ void merge_partials_warp(const float4 *part, int64_t r, int P, float &m_out,
+                                                    float &inv_out)
+{
+    const int lane = threadIdx.x & 31;
+    float pm[kPipeMaxPerLane], ps[kPipeMaxPerLane], pc[kPipeMaxPerLane];
+    float mloc = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kPipeMaxPerLane; j++) {
+        const int i = lane + 32 * j;
+        const float4 v = i < P ? __ldcg(&part[r * P + i]) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        pm[j] = v.x;
+        ps[j] = v.y;
+        pc[j] = v.z;
+        mloc = fmaxf(mloc, v.x);
     }
+    const float m = warp_max_redux(mloc);
+    if constexpr (DT == kF32) {
+        CSum acc{0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < kPipeMaxPerLane; j++) {
+            if (pm[j] != -INFINITY) {
+                const float f = Math<kF32>::exp_shift(pm[j], m);
+                Math<kF32>::add(acc, ps[j] * f);
+                Math<kF32>::add(acc, pc[j] * f);
+            }
+        }
+        acc = group_sum<kF32, 32>(acc);
+        inv_out = 1.0f / (acc.s + acc.c);
+    } else {
+        float d = 0.f;
+#pragma unroll
+        for (int j = 0; j < kPipeMaxPerLane; j++)
+            if (pm[j] != -INFINITY)
+                d += ps[j] * Math<DT>::exp_of(pm[j] - m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            d += __shfl_xor_sync(0xFFFFFFFFu, d, o);
+        inv_out = 1.0f / d;
+    }
+    m_out = m;
 }
 
 // Load CTA p's share of row r (its whole chunks, n of them) into ring buffer
-// `dst` as kGridPieces bulk copies, one mbarrier each.  One thread.
-template <int DT, bool ALIGNED>
+// `dst` as PIECES bulk copies, one mbarrier each.  One thread.
+template <int DT, bool ALIGNED, int PIECES = kGridPieces>
 __device__ __forceinline__ void grid_issue(const GridArgs &a, int64_t r, int p, uint32_t dst, uint32_t bar0)
 {
     const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, r, a.cols);
     const Share sh = share_of<DT, ALIGNED>(g, a.cols, a.P, p, 0);
     const int n = (int)(sh.fe - sh.fb);
-    const int piece = (n + kGridPieces - 1) / kGridPieces;
+    const int piece = (n + PIECES - 1) / PIECES;
     // the buffer's previous contents were read through the generic proxy
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    for (int i = 0; i < kGridPieces; i++) {
+    for (int i = 0; i < PIECES; i++) {
         const int c0 = i * piece, cnt = n - c0 < piece ? n - c0 : piece;
         if (cnt <= 0)
             break;
@@ -275,6 +306,7 @@ __global__ void __launch_bounds__(kGridThreads, 1) k_grid_ring(const GridArgs a)
     __shared__ float smax[32];
     __shared__ typename M::Acc ssum[32];
     __shared__ MD smd[32];
+    __shared__ float2 mi;  // (m, 1/d) of the row being written
     __shared__ volatile int abort_flag;
     const int p = blockIdx.x, gy = blockIdx.y, G = gridDim.y;
     const int tid = threadIdx.x, T = blockDim.x;
@@ -354,8 +386,16 @@ __global__ void __launch_bounds__(kGridThreads, 1) k_grid_ring(const GridArgs a)
                     }
                 }
                 CSum tot = M::merge(M::merge(acc[0], acc[1]), M::merge(acc[2], acc[3]));
-                tot = block_sum<DT>(tot, ssum);
-                partial = make_float4(mx, tot.s, tot.c, 0.f);
+                // warps' sums into slots, merged by warp 0 (only thread 0 publishes)
+                tot = group_sum<DT, 32>(tot);
+                __syncthreads();
+                if ((tid & 31) == 0)
+                    ssum[tid >> 5] = tot;
+                __syncthreads();
+                if (tid < 32) {
+                    tot = group_sum<DT, 32>((tid << 5) < T ? ssum[tid] : M::zero());
+                    partial = make_float4(mx, tot.s, tot.c, 0.f);
+                }
             } else {
                 // 16-bit: one online (m, d) pass, each piece as it lands
                 MD md{-INFINITY, 0.f};
@@ -381,8 +421,17 @@ __global__ void __launch_bounds__(kGridThreads, 1) k_grid_ring(const GridArgs a)
                         md_absorb<DT, K>(md, raw);
                     }
                 }
-                md = block_md<DT>(md, smd);
-                partial = make_float4(md.m, md.d, 0.f, 0.f);
+                // the CTA's (m, d): warps' pairs (max first) into slots, merged by
+                // warp 0 -- only thread 0 needs it, to publish it
+                md = warp_md_max_first<DT>(md);
+                __syncthreads();  // the slots' previous readers are done
+                if ((tid & 31) == 0)
+                    smd[tid >> 5] = md;
+                __syncthreads();
+                if (tid < 32) {
+                    md = warp_md_max_first<DT>((tid << 5) < T ? smd[tid] : MD{-INFINITY, 0.f});
+                    partial = make_float4(md.m, md.d, 0.f, 0.f);
+                }
             }
             // (the block reduction's barriers make a time-out seen by any thread seen by all)
             if (abort_flag)
@@ -406,8 +455,14 @@ __global__ void __launch_bounds__(kGridThreads, 1) k_grid_ring(const GridArgs a)
             if (abort_flag)
                 break;
             // (thread 0's acquire and the barrier order the partials' loads)
-            float m, inv;
-            merge_partials_cta<DT>(a.part, r, a.P, m, inv, smax, ssum, smd);
+            if (tid < 32) {
+                float mm, ii;
+                merge_partials_warp<DT>(a.part, r, a.P, mm, ii);
+                if (tid == 0)
+                    mi = make_float2(mm, ii);
+            }
+            __syncthreads();
+            const float m = mi.x, inv = mi.y;
             const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, r, a.cols);
             const Share sh = share_of<DT, ALIGNED>(g, a.cols, a.P, p, tid);
             const int n = (int)(sh.fe - sh.fb);
@@ -443,6 +498,250 @@ __global__ void __launch_bounds__(kGridThreads, 1) k_grid_ring(const GridArgs a)
                     for (int i = 0; i < kGridPieces; i++)
                         (void)mbar_wait(bar0 + 8u * (kGridPieces * b + i), (uint32_t)(pending[b] / Q) & 1u,
                                         &abort_flag, false);
+        }
+        __syncthreads();
+    }
+}
+
+// Pipelined form: one CTA per SM, all P of them on every row; CTA p holds share
+// p of each row, the rows passing in order through a ring of Q shared-memory
+// buffers filled by bulk copies (x read from HBM once).  The CTA's warps split
+// into two teams that work on different rows at once:
+// * fold team (the first nf threads): for each row in turn, waits for its
+//   share's pieces and folds them as they land, reduces over the team only
+//   (warp max in one instruction, team slots behind a named barrier) and
+//   publishes the CTA's partial at the row's grid barrier -- then goes on to
+//   the next row without waiting for the barrier;
+// * write team (the rest): for each row in turn, waits at its grid barrier
+//   (one thread polls), merges the P partials in one warp, writes the share
+//   from shared memory, and refills the buffer with the row Q places further
+//   on.
+// So the loads and fold of row k + 1 overlap the barrier, merge and output of
+// row k, and the rows' barriers are normally complete by the time the write
+// team asks.  The teams share only the buffers (mbarriers of the bulk copies)
+// and the abort flag.  Every wait is bounded; on a time-out every thread still
+// walks its team's barrier sequence, skipping the work, and the CTA waits
+// (bounded) for its copies in flight before it leaves.
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(kGridThreads, 1) k_grid_pipe(const GridArgs a)
+{
+    pdl_enter();
+    using M = Math<DT>;
+    constexpr int E = Fmt<DT>::kPerChunk;
+    constexpr int K = 4;  // chunks per fold thread per step
+    constexpr int kFoldWarpsMax = kGridThreads / 32;
+    extern __shared__ __align__(128) unsigned char seg[];
+    __shared__ __align__(8) uint64_t bars[kGridMaxRing * kPipePieces];
+    __shared__ int pending[kGridMaxRing];           // row whose copies into a buffer are unawaited, or -1
+    __shared__ float4 fslot[2][kFoldWarpsMax];      // fold warps' partials, by row parity
+    __shared__ float2 mrow[2];                      // (m, 1/d) of the row the write team writes, by parity
+    __shared__ volatile int abort_flag;
+    const int p = blockIdx.x, P = a.P, Q = a.Q, NF = a.nf;
+    const int R = (int)a.rows;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t seg0 = smem_u32(seg), bar0 = smem_u32(bars);
+
+    grid_prepare_next(a);
+    if (tid == 0) {
+        for (int i = 0; i < Q * kPipePieces; i++)
+            mbar_init(bar0 + 8u * i, 1);
+        abort_flag = 0;
+        mbar_init_fence();
+        for (int b = 0; b < Q; b++) {
+            pending[b] = b < R ? b : -1;
+            if (b < R)
+                grid_issue<DT, ALIGNED, kPipePieces>(a, b, p, seg0 + (uint32_t)b * a.buf, bar0 + 8u * kPipePieces * b);
+        }
+    }
+    __syncthreads();
+
+    if (tid < NF) {
+        // ---------------- fold team
+        const int tf = tid, wf = tf >> 5, nwf = NF >> 5;
+        for (int k = 0; k < R; k++) {
+            const int b = k % Q;
+            const uint32_t par = (uint32_t)(k / Q) & 1u, buf = seg0 + (uint32_t)b * a.buf;
+            const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, k, a.cols);
+            const Share sh = share_of<DT, ALIGNED>(g, a.cols, P, p, tf);
+            const int n = (int)(sh.fe - sh.fb);
+            const int piece = (n + kPipePieces - 1) / kPipePieces;
+            const uint4 edge = sh.edge_k >= 0 ? load_chunk<DT, ALIGNED>(g, sh.edge_k, a.cols) : neg_inf_chunk<DT>();
+            float4 partial = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+            if constexpr (DT == kF32) {
+                // fp32: the share's max, then the compensated sum of exp(x - max)
+                bool ok = true;
+                for (int i = 0; i < kPipePieces && i * piece < n && ok; i++)
+                    ok = mbar_wait(bar0 + 8u * (kPipePieces * b + i), par, &abort_flag);
+                if (!ok) {
+                    if (!abort_flag)
+                        atomicOr(a.err, kErrFullWait);
+                    abort_flag = 1;
+                }
+                float mx = chunk_max<DT>(edge);
+                if (!abort_flag) {
+                    float mx2 = -INFINITY;
+                    int c = tf;
+                    for (; c + NF < n; c += 2 * NF) {
+                        mx = fmaxf(mx, chunk_max<DT>(lds_chunk(buf + 16u * (uint32_t)c)));
+                        mx2 = fmaxf(mx2, chunk_max<DT>(lds_chunk(buf + 16u * (uint32_t)(c + NF))));
+                    }
+                    if (c < n)
+                        mx = fmaxf(mx, chunk_max<DT>(lds_chunk(buf + 16u * (uint32_t)c)));
+                    mx = fmaxf(mx, mx2);
+                }
+                mx = warp_max_redux(mx);
+                if (lane == 0)
+                    fslot[k & 1][wf].x = mx;
+                named_sync(1, NF);
+                mx = -INFINITY;
+                for (int w = 0; w < nwf; w++)
+                    mx = fmaxf(mx, fslot[k & 1][w].x);
+                CSum acc[E];
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    acc[e] = M::zero();
+                if (!abort_flag && mx != -INFINITY) {
+                    float f[E];
+                    chunk_exp<DT>(edge, mx, f);
+#pragma unroll
+                    for (int e = 0; e < E; e++)
+                        M::add(acc[e], f[e]);
+#pragma unroll 2
+                    for (int c = tf; c < n; c += NF) {
+                        chunk_exp<DT>(lds_chunk(buf + 16u * (uint32_t)c), mx, f);
+#pragma unroll
+                        for (int e = 0; e < E; e++)
+                            M::add(acc[e], f[e]);
+                    }
+                }
+                CSum tot = M::merge(M::merge(acc[0], acc[1]), M::merge(acc[2], acc[3]));
+                tot = group_sum<DT, 32>(tot);
+                if (lane == 0) {
+                    fslot[k & 1][wf].y = tot.s;
+                    fslot[k & 1][wf].z = tot.c;
+                }
+                named_sync(1, NF);
+                if (tf == 0) {
+                    CSum all = M::zero();
+                    for (int w = 0; w < nwf; w++)
+                        all = M::merge(all, CSum{fslot[k & 1][w].y, fslot[k & 1][w].z});
+                    partial = make_float4(mx, all.s, all.c, 0.f);
+                }
+            } else {
+                // 16-bit: one online (m, d) pass, each piece as it lands
+                MD md{-INFINITY, 0.f};
+                {
+                    uint4 one[1] = {edge};
+                    md_absorb<DT, 1>(md, one);
+                }
+                for (int i = 0; i < kPipePieces && i * piece < n; i++) {
+                    if (!mbar_wait(bar0 + 8u * (kPipePieces * b + i), par, &abort_flag)) {
+                        if (!abort_flag)
+                            atomicOr(a.err, kErrFullWait);
+                        abort_flag = 1;
+                    }
+                    if (abort_flag)
+                        break;
+                    const int c0 = i * piece, c1 = n - c0 < piece ? n : c0 + piece;
+                    // K chunks a step while a thread has K, then one at a time:
+                    // no exps spent on padding
+                    int c = c0 + tf;
+                    for (; c + (K - 1) * NF < c1; c += NF * K) {
+                        uint4 raw[K];
+#pragma unroll
+                        for (int u = 0; u < K; u++)
+                            raw[u] = lds_chunk(buf + 16u * (uint32_t)(c + u * NF));
+                        md_absorb<DT, K>(md, raw);
+                    }
+                    for (; c < c1; c += NF) {
+                        uint4 one[1] = {lds_chunk(buf + 16u * (uint32_t)c)};
+                        md_absorb<DT, 1>(md, one);
+                    }
+                }
+                md = warp_md_max_first<DT>(md);
+                if (lane == 0)
+                    fslot[k & 1][wf] = make_float4(md.m, md.d, 0.f, 0.f);
+                named_sync(1, NF);
+                if (tf == 0) {
+                    MD all{-INFINITY, 0.f};
+                    for (int w = 0; w < nwf; w++)
+                        all = md_merge<DT>(all, MD{fslot[k & 1][w].x, fslot[k & 1][w].y});
+                    partial = make_float4(all.m, all.d, 0.f, 0.f);
+                }
+            }
+            if (tf == 0 && !abort_flag) {
+                pending[b] = -1;
+                grid_publish(a, k, p, partial);
+            }
+        }
+    } else {
+        // ---------------- write team
+        const int to = tid - NF, wo = to >> 5, NO = blockDim.x - NF;
+        for (int k = 0; k < R; k++) {
+            const int b = k % Q;
+            const uint32_t buf = seg0 + (uint32_t)b * a.buf;
+            if (wo == 0) {
+                int ok = 1;
+                if (lane == 0 && !abort_flag)
+                    ok = grid_wait_row(a, k) ? 1 : 0;
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);  // (also orders lane 0's acquire before the loads)
+                if (!ok && lane == 0) {
+                    atomicOr(a.err, kErrGridWait);
+                    abort_flag = 1;
+                }
+                __syncwarp();
+                if (!abort_flag) {
+                    float m, inv;
+                    merge_partials_warp<DT>(a.part, k, P, m, inv);
+                    if (lane == 0)
+                        mrow[k & 1] = make_float2(m, inv);
+                }
+            }
+            named_sync(2, NO);
+            if (!abort_flag) {
+                const float m = mrow[k & 1].x, inv = mrow[k & 1].y;
+                const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, k, a.cols);
+                const Share sh = share_of<DT, ALIGNED>(g, a.cols, P, p, to);
+                const int n = (int)(sh.fe - sh.fb);
+                if (sh.edge_k >= 0) {
+                    float f[E];
+                    chunk_exp<DT>(load_chunk<DT, ALIGNED>(g, sh.edge_k, a.cols), m, f);
+#pragma unroll
+                    for (int e = 0; e < E; e++)
+                        f[e] *= inv;
+                    store_chunk<DT, ALIGNED>(g, sh.edge_k, a.cols, pack<DT>(f), a.y_vec != 0);
+                }
+#pragma unroll 4
+                for (int c = to; c < n; c += NO) {
+                    float f[E];
+                    chunk_exp<DT>(lds_chunk(buf + 16u * (uint32_t)c), m, f);
+#pragma unroll
+                    for (int e = 0; e < E; e++)
+                        f[e] *= inv;
+                    store_chunk<DT, ALIGNED>(g, sh.fb + c, a.cols, pack<DT>(f), a.y_vec != 0);
+                }
+            }
+            named_sync(2, NO);  // buffer b is consumed
+            if (to == 0 && !abort_flag && k + Q < R) {
+                pending[b] = k + Q;
+                grid_issue<DT, ALIGNED, kPipePieces>(a, k + Q, p, buf, bar0 + 8u * kPipePieces * b);
+            }
+        }
+    }
+    __syncthreads();
+    if (abort_flag) {
+        if (tid == 0) {
+            // no copy may still be landing in shared memory when the CTA leaves
+            for (int b = 0; b < Q; b++) {
+                if (pending[b] < 0)
+                    continue;
+                const RowGeom g = row_geom<DT, ALIGNED>(a.x, a.y, pending[b], a.cols);
+                const Share sh = share_of<DT, ALIGNED>(g, a.cols, P, p, 0);
+                const int n = (int)(sh.fe - sh.fb), piece = (n + kPipePieces - 1) / kPipePieces;
+                for (int i = 0; i < kPipePieces && i * piece < n; i++)
+                    (void)mbar_wait(bar0 + 8u * (kPipePieces * b + i), (uint32_t)(pending[b] / Q) & 1u, &abort_flag,
+                                    false);
+            }
         }
         __syncthreads();
     }
@@ -536,10 +835,12 @@ int pool_init(GridPool &pl)
     return 0;
 }
 
-template <int DT, bool A, bool RES>
+// FORM: 0 streaming, 1 ring, 2 pipelined
+template <int DT, bool A, int FORM>
 int grid_launch_one(const Launch &l, const GridArgs &args)
 {
-    auto kern = RES ? &k_grid_ring<DT, A> : &k_grid_stream<DT, A>;
+    constexpr bool RES = FORM >= 1;  // shares held in shared memory
+    auto kern = FORM == 2 ? &k_grid_pipe<DT, A> : (FORM == 1 ? &k_grid_ring<DT, A> : &k_grid_stream<DT, A>);
     if (RES) {
         // opt in once per device to the largest segment the planner gives this
         // kernel (the device's opt-in limit less the static shared memory)
@@ -580,10 +881,12 @@ int grid_launch_one(const Launch &l, const GridArgs &args)
 template <int DT>
 int grid_dt(const Launch &l, const GridArgs &args)
 {
-    const bool res = l.plan.stages >= 1;
+    const int form = l.plan.stages < 1 ? 0 : (l.plan.lanes_per_row > 0 ? 2 : 1);
     if (l.plan.aligned)
-        return res ? grid_launch_one<DT, true, true>(l, args) : grid_launch_one<DT, true, false>(l, args);
-    return res ? grid_launch_one<DT, false, true>(l, args) : grid_launch_one<DT, false, false>(l, args);
+        return form == 2 ? grid_launch_one<DT, true, 2>(l, args)
+                         : (form == 1 ? grid_launch_one<DT, true, 1>(l, args) : grid_launch_one<DT, true, 0>(l, args));
+    return form == 2 ? grid_launch_one<DT, false, 2>(l, args)
+                     : (form == 1 ? grid_launch_one<DT, false, 1>(l, args) : grid_launch_one<DT, false, 0>(l, args));
 }
 
 }  // namespace
@@ -625,7 +928,7 @@ int launch_grid(const Launch &l)
     GridArgs args{(const char *)l.x, (char *)l.y, l.rows, l.cols, (int)l.plan.grid_x, Q,
                   Q > 0 ? l.plan.smem_bytes / Q : 0, l.plan.y_vector,
                   pl.part + (size_t)s * kGridMaxPartials, pl.arrive + (size_t)s * 2 * kGridMaxRows, gen,
-                  l.dev_err};
+                  l.dev_err, Q > 0 ? l.plan.lanes_per_row : 0};
     int rc;
     switch (l.dtype) {
     case kF32:

@@ -26,6 +26,8 @@ constexpr int kGridMaxRows = 128;       // SPLITK_GRID: rows a slot serves
 constexpr int kGridMaxPartials = 4096;  // SPLITK_GRID: rows x CTAs per row a slot serves
 constexpr int kGridMaxRing = 8;         // SPLITK_GRID ring form: shared-memory buffers
 constexpr int kGridStaticSmem = 2048;   // SPLITK_GRID ring form: static shared memory, upper bound
+constexpr int kGridPipeFold = 256;      // SPLITK_GRID pipelined form: threads of the fold team
+constexpr int kGridPipeMaxCtas = 256;   // SPLITK_GRID pipelined form: CTAs whose partials one warp merges
 constexpr int kMaxCluster = 16;         // non-portable cluster size limit
 constexpr int kSplitStages = 6;         // SPLITK: shared-memory ring depth
 constexpr int kSplitStageBytes = 32768; // SPLITK: bytes per stage (one bulk copy)

@@ -259,14 +259,17 @@ bool grid_possible(int64_t rows, const softmax_device_info &dev)
 void plan_grid(const Geometry &g, int64_t rows, const softmax_device_info &dev, softmax_launch_plan &p)
 {
     const int64_t budget = int64_t(dev.max_smem_optin) - kGridStaticSmem;
+    p.variant = SOFTMAX_VARIANT_SPLITK_GRID;
+    p.chunks_per_thread = kWideStep;
+    p.block_threads = kGridThreads;
     // Ring form: G groups of P = SMs / G CTAs, one CTA per SM.  Each row a CTA
-    // takes in turn costs it a fixed ~5 us (its fold at one 512-thread CTA per
-    // SM, two block reductions, the release, the merge's round trip), so the
-    // plan takes the fewest rows per group for which a CTA's share of a row
-    // fits one buffer and the partials fit a scratch slot, and for that count
-    // the fewest groups (the most CTAs on a row: the smallest shares, the
-    // deepest ring).
-    int64_t P = 0, G = 0, buf = 0;
+    // takes in turn costs it a fixed few microseconds (its fold, the block
+    // reductions, the release, the merge's round trip), so the plan takes the
+    // fewest rows per group (npg) for which a CTA's share of a row fits one
+    // buffer and the partials fit a scratch slot, and for that count the
+    // fewest groups (the most CTAs on a row: the smallest shares, the deepest
+    // ring).
+    int64_t P = 0, G = 0, buf = 0, npg_found = 0;
     for (int64_t npg = 1; npg <= rows; npg++) {
         const int64_t gg = ceil_div(rows, npg);
         if (npg > 1 && ceil_div(rows, gg) != npg)
@@ -280,11 +283,35 @@ void plan_grid(const Geometry &g, int64_t rows, const softmax_device_info &dev, 
         P = pp;
         G = gg;
         buf = bb;
+        npg_found = npg;
         break;
     }
-    p.variant = SOFTMAX_VARIANT_SPLITK_GRID;
-    p.chunks_per_thread = kWideStep;
-    p.block_threads = kGridThreads;
+    // Pipelined form, where the ring would give a group several rows in turn:
+    // every SM on every row, the rows in turn through Q >= 2 buffers, a fold
+    // team working on one row while the write team waits at the grid barrier
+    // of the row before and writes it, so that those rows' fixed costs overlap
+    // each other and the loads.  Measured on [4, 4194304]: fp32 (ring: 2
+    // groups of 76 CTAs, two rows each) 44.4 us pipelined against 47.2 us;
+    // fp16 (ring: one row per group of 38 CTAs) 24.7 us pipelined against
+    // 20.5 us, so one row per group stays with the ring.
+    if (npg_found != 1 && rows >= 2 && dev.sm_count <= kGridPipeMaxCtas &&
+        int64_t(dev.sm_count) * rows <= kGridMaxPartials) {
+        const int64_t PP = dev.sm_count;
+        const int64_t bb = ceil_div(ceil_div(g.nch_max, PP) * 16, 128) * 128;
+        int64_t Q = budget / bb;
+        if (Q > rows)
+            Q = rows;
+        if (Q > kGridMaxRing)
+            Q = kGridMaxRing;
+        if (Q >= 2) {
+            p.lanes_per_row = kGridPipeFold;
+            p.stages = (int)Q;
+            p.smem_bytes = (int)(Q * bb);
+            p.grid_x = PP;
+            p.grid_y = 1;
+            return;
+        }
+    }
     if (P > 0) {
         int64_t Q = ceil_div(rows, G);
         if (Q > budget / buf)
@@ -405,7 +432,18 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
             return SOFTMAX_ERR_INVALID_ARG;
         if (p.grid_x < 1 || p.grid_x * rows > kGridMaxPartials || V != kWideStep)
             return SOFTMAX_ERR_INVALID_ARG;
-        if (p.stages >= 1) {
+        if (p.lanes_per_row != 0) {
+            // pipelined form: one group of P CTAs (one per SM) on every row, Q
+            // buffers, a fold team of lanes_per_row threads and a write team
+            if (p.stages < 1 || p.stages > kGridMaxRing || p.grid_y != 1 || p.grid_x > dev.sm_count ||
+                p.grid_x > kGridPipeMaxCtas || p.lanes_per_row < 32 || p.lanes_per_row % 32 != 0 ||
+                p.lanes_per_row >= p.block_threads || p.smem_bytes % p.stages != 0)
+                return SOFTMAX_ERR_INVALID_ARG;
+            const int64_t buf = p.smem_bytes / p.stages;
+            if (buf % 16 != 0 || buf < ceil_div(g.nch_max, p.grid_x) * 16 ||
+                p.smem_bytes > dev.max_smem_optin - kGridStaticSmem)
+                return SOFTMAX_ERR_INVALID_ARG;
+        } else if (p.stages >= 1) {
             // ring form: G groups of P CTAs, one CTA per SM, Q buffers that each
             // hold a CTA's share of a row
             if (p.stages > kGridMaxRing || p.grid_y < 1 || p.grid_y > rows ||

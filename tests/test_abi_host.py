@@ -154,14 +154,19 @@ def test_dispatch_of_workloads(lib, name):
     if name == "fp32_128x1000":
         assert p.block_threads == 64 and p.chunks_per_thread == 4 and p.grid_x == 128
     if p.variant == B.VARIANT_SPLITK_GRID:
-        # ring form, one CTA per SM: fp16, one group of 38 CTAs per row (a
-        # 220 KB share each); fp32, two groups of 76 CTAs taking two rows each
-        # (220 KB shares, one buffer)
-        G = 4 if w.dtype == "fp16" else 2
-        P = 152 // G
-        assert p.grid_x == P and p.grid_y == G and p.block_threads == 512 and p.cluster_x == 1
-        buf = -(-(-(-(w.cols * w.elem_bytes // 16) // P) * 16) // 128) * 128
-        assert p.stages == 1 and p.smem_bytes == buf <= 232448 - 2048
+        assert p.block_threads == 512 and p.cluster_x == 1
+        if w.dtype == "fp16":
+            # ring form, one row per group: 4 groups of 38 CTAs, a 220 KB share each
+            assert (p.grid_x, p.grid_y, p.stages, p.lanes_per_row) == (38, 4, 1, 0)
+            buf = -(-(-(-(w.cols * w.elem_bytes // 16) // 38) * 16) // 128) * 128
+            assert p.smem_bytes == buf <= 232448 - 2048
+        else:
+            # the ring would give each group two rows in turn: the pipelined
+            # form, every CTA on every row, two 110 KB buffers the rows pass
+            # through two at a time, a 256-thread fold team
+            assert (p.grid_x, p.grid_y, p.stages, p.lanes_per_row) == (152, 1, 2, 256)
+            buf = -(-(-(-(w.cols * w.elem_bytes // 16) // 152) * 16) // 128) * 128
+            assert p.smem_bytes == 2 * buf <= 232448 - 2048
 
 
 @pytest.mark.parametrize("dt,elem", [(0, 4), (1, 2), (2, 2)])
@@ -217,11 +222,22 @@ def test_grid_split_limits(lib):
     assert rc == B.OK and p.stages == 0 and p.grid_x == 304 and p.grid_y == 1   # 64 MiB: streamed
     rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 2, 1 << 24, 1, B.VARIANT_SPLITK_GRID)
     assert rc == B.OK and p.stages == 1 and (p.grid_x, p.grid_y) == (152, 1)     # two rows, one buffer
+    assert p.lanes_per_row == 0                                                   # ring form
+    # one row per group when the shares fit: the ring form
     rc, p = B.softmax_plan(GB300, BASE + 2, BASE + (1 << 36) + 2, 3, (1 << 21) + 7, 2, B.VARIANT_SPLITK_GRID)
-    assert rc == B.OK and p.aligned == 0 and p.stages == 1 and (p.grid_x, p.grid_y) == (50, 3)
+    assert rc == B.OK and p.aligned == 0 and (p.grid_x, p.grid_y, p.stages, p.lanes_per_row) == (50, 3, 1, 0)
+    # where the ring would give a group several rows in turn: the pipelined form
+    # (every CTA on every row, a 256-thread fold team), as many buffers as fit,
+    # at most one per row and at most 8.  16 rows of 2 MiB: the ring would take
+    # 8 groups of 19 CTAs, two rows each
     rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 16, 1 << 20, 1, B.VARIANT_SPLITK_GRID)
-    # 16 rows of 2 MiB: 8 groups of 19 CTAs, two rows each through a ring of two buffers
-    assert rc == B.OK and (p.grid_x, p.grid_y, p.stages) == (19, 8, 2)
+    assert rc == B.OK and (p.grid_x, p.grid_y, p.stages, p.lanes_per_row) == (152, 1, 8, 256)
+    assert p.smem_bytes == 8 * (-(-(-(-(1 << 17) // 152) * 16) // 128) * 128)
+    # the pipelined form's partials (rows x 152) must fit a scratch slot (4096)
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 26, 1 << 20, 1, B.VARIANT_SPLITK_GRID)
+    assert rc == B.OK and p.lanes_per_row == 256 and p.grid_y == 1
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 36), 27, 1 << 20, 1, B.VARIANT_SPLITK_GRID)
+    assert rc == B.OK and p.lanes_per_row == 0 and p.grid_y > 1
 
 
 

@@ -45,9 +45,11 @@ def test_grid_full_size_workloads(name):
 @pytest.mark.parametrize("dt", [0, 1, 2])
 def test_grid_shapes_and_offsets(dt):
     rng = np.random.default_rng(300 + dt)
-    # ring (shares that fit shared memory) and streamed forms, ragged
-    # rows, few and many CTAs per row
-    for rows, cols in ((1, 300001), (3, 1 << 20), (4, (1 << 21) + 5), (7, 150003), (2, 1 << 23), (76, 20000)):
+    # pipelined (every CTA on every row), ring (shares that fit shared
+    # memory) and streamed forms, ragged rows, few and many CTAs per row, more
+    # rows than buffers
+    for rows, cols in ((1, 300001), (3, 1 << 20), (4, (1 << 21) + 5), (7, 150003), (2, 1 << 23), (76, 20000),
+                       (11, (1 << 19) + 1), (26, 1 << 18), (5, 3 << 20)):
         x = rng.normal(0, 4, (rows, cols))
         x[:, ::97] += 60.0
         x = _quant(x, dt)
@@ -140,8 +142,10 @@ def _grid_plan(rows, cols, dt, x_off=0, y_off=0):
 
 @pytest.mark.parametrize("dt", [0, 1, 2])
 def test_grid_ring_groups_and_depths(dt):
-    # hand-made ring plans: every CTA on every row (G = 1) with a ring of 1 to
-    # 4 buffers, two groups, one group per row; and plans the checks refuse
+    # hand-made plans: the ring form with every CTA on every row (G = 1) and a
+    # ring of 1 to 4 buffers, two groups, one group per row; the pipelined form
+    # with 1 to 4 buffers and fold teams of 128, 256 and 384 threads; and plans
+    # the checks refuse
     rng = np.random.default_rng(310 + dt)
     rows, cols = 4, (1 << 20) + 3
     x = rng.normal(0, 3, (rows, cols))
@@ -160,15 +164,21 @@ def test_grid_ring_groups_and_depths(dt):
     for G, Q in ((1, 1), (1, 2), (1, 4), (2, 1), (2, 2), (4, 1)):
         P = S // G
         if Q * buf_for(P) <= budget:
-            good.append(dict(grid_x=P, grid_y=G, stages=Q, smem_bytes=Q * buf_for(P)))
-    assert len(good) >= 4
+            good.append(dict(grid_x=P, grid_y=G, stages=Q, smem_bytes=Q * buf_for(P), lanes_per_row=0))
+    for Q, NF in ((1, 256), (2, 128), (3, 384), (4, 256)):
+        if Q * buf_for(S) <= budget:
+            good.append(dict(grid_x=S, grid_y=1, stages=Q, smem_bytes=Q * buf_for(S), lanes_per_row=NF))
+    assert len(good) >= 8
     for ch in good:
         q = osd.LaunchPlan(**{**p.as_dict(), **ch})
         rc, y = run(x, dt, plan=q, x_off=1, y_off=1)
         assert rc == 0, ch
         check(x, y, dt)
-    bad = [dict(grid_y=rows + 1), dict(grid_x=S + 1, grid_y=1), dict(stages=9, smem_bytes=9 * 128),
-           dict(smem_bytes=(p.smem_bytes // p.stages // 32 * 16) * p.stages), dict(smem_bytes=p.smem_bytes + 8)]
+    ring = dict(lanes_per_row=0)
+    bad = [dict(ring, grid_y=rows + 1), dict(ring, grid_x=S + 1, grid_y=1), dict(ring, stages=9, smem_bytes=9 * 128),
+           dict(smem_bytes=(p.smem_bytes // p.stages // 32 * 16) * p.stages), dict(smem_bytes=p.smem_bytes + 8),
+           dict(grid_y=2), dict(grid_x=S + 1), dict(lanes_per_row=48), dict(lanes_per_row=512),
+           dict(lanes_per_row=16), dict(stages=0, smem_bytes=0)]
     for ch in bad:
         q = osd.LaunchPlan(**{**p.as_dict(), **ch})
         rc, _ = run(x, dt, plan=q, x_off=1, y_off=1)
