@@ -175,10 +175,12 @@ def test_grid_ring_groups_and_depths(dt):
         assert rc == 0, ch
         check(x, y, dt)
     ring = dict(lanes_per_row=0)
+    pipe = dict(grid_x=S, grid_y=1, stages=2, smem_bytes=2 * buf_for(S), lanes_per_row=256)
     bad = [dict(ring, grid_y=rows + 1), dict(ring, grid_x=S + 1, grid_y=1), dict(ring, stages=9, smem_bytes=9 * 128),
            dict(smem_bytes=(p.smem_bytes // p.stages // 32 * 16) * p.stages), dict(smem_bytes=p.smem_bytes + 8),
-           dict(grid_y=2), dict(grid_x=S + 1), dict(lanes_per_row=48), dict(lanes_per_row=512),
-           dict(lanes_per_row=16), dict(stages=0, smem_bytes=0)]
+           dict(pipe, grid_y=2), dict(pipe, grid_x=S + 1), dict(pipe, lanes_per_row=48),
+           dict(pipe, lanes_per_row=512), dict(pipe, lanes_per_row=16), dict(pipe, stages=0, smem_bytes=0),
+           dict(pipe, smem_bytes=2 * (buf_for(S) - 128))]
     for ch in bad:
         q = osd.LaunchPlan(**{**p.as_dict(), **ch})
         rc, _ = run(x, dt, plan=q, x_off=1, y_off=1)
