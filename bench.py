@@ -197,7 +197,8 @@ def kernel_fingerprint(variant: str) -> str:
     csrc = os.path.join(ROOT, "online_softmax_dispatcher_gb300", "csrc")
     files = {"rowgroup": ("k_rowgroup.cuh",), "block": ("k_block.cu",), "block_tma": ("k_tma.cu",),
              "stream": ("k_stream.cu", "stream_passes.cuh"), "splitk": ("k_splitk.cu",),
-             "splitk_grid": ("k_grid.cu", "stream_passes.cuh"), "splitk_wide": ("k_wide.cu", "stream_passes.cuh"),
+             "splitk_grid": ("k_grid.cu", "split_parts.cuh", "stream_passes.cuh"),
+             "splitk_wide": ("k_wide.cu", "stream_passes.cuh"),
              "layernorm": ("k_norm.cuh",), "rmsnorm": ("k_norm.cuh",), "backward": ("k_bwd.cu",),
              "masked": ("k_masked.cu",)}
     h = hashlib.sha256()
