@@ -785,15 +785,11 @@ extern "C" __attribute__((visibility("default"))) int softmax_plan(
     if (v == SOFTMAX_VARIANT_AUTO) {
         const bool few_rows = rows * 2 <= dev->sm_count;
         const bool long_rows = g.nch_max >= int64_t(8) * (kSplitStageBytes / 16);
-        // a row to itself on an SM (rows <= SMs) that one warp would hold at
-        // more than 4 chunks a lane (fp32 rows of 129 - 256 chunks): one CTA
-        // per row spreads it over two warps ([128, 1000] fp32: 339 - 366 GB/s
-        // against 326 - 353 for one warp a row; launch-bound either way)
-        const bool lone_wide_rows = rows <= dev->sm_count && g.nint > int64_t(32) * 4;
-        if (rowgroup_fits(g) && !lone_wide_rows)
+        // (a launch-bound 1 MB call such as [128, 1000] fp32 measured within
+        // run-to-run noise either way: lanes per row 2.97 - 3.14 us, one CTA
+        // per row 3.02 - 3.10 us over two builds and boxes)
+        if (rowgroup_fits(g))
             v = SOFTMAX_VARIANT_ROWGROUP;
-        else if (rowgroup_fits(g))
-            v = SOFTMAX_VARIANT_BLOCK;
         else if (few_rows && long_rows && grid_possible(rows, *dev))
             v = SOFTMAX_VARIANT_SPLITK_GRID;
         else if (few_rows && long_rows && splitk_possible(rows, *dev))
