@@ -494,13 +494,16 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
             if rc != 0:
                 raise osd.SoftmaxError(rc)
 
+    # the clock sampler starts (and settles) before the warm-up steps, so
+    # that the timed region follows the warm-up with no idle gap: an idle
+    # GPU takes its first launch back at 1.5 - 3x the time of the next ones
+    sampler = ClockSampler(gpu_id_for_nvsmi()).start() if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.3)
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(gpu_id_for_nvsmi()).start() if rank == 0 else None
-    if sampler is not None:
-        time.sleep(0.3)
     # ---- timed region: K steps
     barrier(ws)
     torch.cuda.synchronize()
