@@ -35,6 +35,12 @@
 //   computed once: chunks wholly past the causal limit are not read, only the
 //   one the limit falls in cuts values one by one.  The mask's presence and
 //   the rows' 16-byte phases are template parameters.
+// * Lean form (k_masked_lean): the lanes-per-row case of 16-bit rows on the
+//   16-byte grid with no additive mask and a positive scale -- causal
+//   attention scores -- with the max taken on packed x and no per-row 64-bit
+//   division (its own account is above the kernel).
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -460,6 +466,162 @@ __global__ void __launch_bounds__(512) k_masked_block(const MaskedArgs a)
                                                      MaxSumCta<DT>{smax, ssum});
 }
 
+// ---------------------------------------------------------------- lean form
+//
+// The common attention case with its own, smaller instruction budget: 16-bit
+// rows on the 16-byte grid, no additive mask, 0 < scale < inf, fewer than
+// 2^31 rows.  The general kernel above spends ~19 instructions per element
+// there and is bound by instruction issue, not by HBM.  Here:
+// * scale > 0 makes fl(scale * x) non-decreasing in x, so the row's max
+//   logit is fl(scale * max_j x_j): the max is taken on the packed 16-bit
+//   pairs (one instruction per two values), the cut values of the chunk the
+//   causal limit falls in first set to -inf in the packed words.  This is the
+//   same m the general kernel finds.
+// * exp(z_j - m) = 2^(x_j * fl(scale log2e) + c), c = bias - fl(m log2e)
+//   formed once per row: c's rounding is common to the row (the
+//   normalisation cancels it), and per element the exponent carries about
+//   2^-24 (|z_j| log2e + |t_j|) -- with |m| < kPairFreeMax and z_j >= m - 100
+//   for any output above the 16-bit range, below 2^-24 * 1030 = 6.2e-5
+//   (4.3e-5 relative in the exp), the same class as the general kernel's
+//   bound.  Rows with |m| >= kPairFreeMax go down masked_row_shifted.
+// * r mod causal_q by a multiply-high with a host-made constant: the
+//   round-up method of Granlund and Montgomery, "Division by invariant
+//   integers using multiplication" (PLDI 1994), for dividends below 2^31:
+//   with l = ceil(log2 q) and M = floor(2^32 (2^l - q) / q) + 1,
+//   floor(r / q) = (umulhi(M, r) + r) >> l.
+struct LeanArgs {
+    const char *x;
+    char *y;
+    uint32_t rows;
+    int cols;
+    float scale;
+    int causal_q;  // 0: no causal cut
+    uint32_t q_magic;
+    uint32_t q_shift;
+};
+
+// Slots nv.. of a chunk set to -inf (0 < nv < E), on the packed words.
+template <int DT>
+__device__ __forceinline__ uint4 cut_chunk(const uint4 &c, int nv)
+{
+    constexpr uint32_t ni = Fmt<DT>::kNegInf;
+    uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        if (2 * k + 1 >= nv)
+            w[k] = 2 * k < nv ? ((w[k] & 0xFFFFu) | (ni << 16)) : (ni | (ni << 16));
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Max of the V chunks' slots as a float: packed pairwise maxima, one
+// conversion at the end (the max of representable values is exact).
+template <int DT, int V>
+__device__ __forceinline__ float packed_max(const uint4 (&xc)[V])
+{
+    using H2 = typename std::conditional<DT == kF16, __half2, __nv_bfloat162>::type;
+    H2 h[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        const uint32_t w = k == 0 ? xc[0].x : k == 1 ? xc[0].y : k == 2 ? xc[0].z : xc[0].w;
+        *reinterpret_cast<uint32_t *>(&h[k]) = w;
+    }
+#pragma unroll
+    for (int i = 1; i < V; i++) {
+        const uint32_t w[4] = {xc[i].x, xc[i].y, xc[i].z, xc[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            H2 t;
+            *reinterpret_cast<uint32_t *>(&t) = w[k];
+            h[k] = __hmax2(h[k], t);
+        }
+    }
+    const H2 r = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
+    return fmaxf(__low2float(r), __high2float(r));
+}
+
+template <int DT, int G, int V>
+__global__ void __launch_bounds__(kRowgroupThreads) k_masked_lean(const LeanArgs a)
+{
+    pdl_enter();
+    constexpr int E = Fmt<DT>::kPerChunk;
+    constexpr int S = Fmt<DT>::kBytes;
+    const int groups = blockDim.x / G;
+    const int lane = threadIdx.x & (G - 1);
+    const float sl2e = a.scale * kLog2e;
+    const int span = a.cols / E;  // rows on the 16-byte grid: every chunk is interior
+    const int64_t stride = (int64_t)gridDim.x * groups;
+    // every thread of a CTA runs the same number of iterations, so the
+    // butterflies see converged warps
+    for (int64_t base = (int64_t)blockIdx.x * groups; base < a.rows; base += stride) {
+        const int64_t r64 = base + threadIdx.x / G;
+        const bool valid = r64 < a.rows;
+        const uint32_t r = valid ? (uint32_t)r64 : 0u;
+        int lim = 0;
+        if (valid) {
+            lim = a.cols;
+            if (a.causal_q > 0) {
+                const uint32_t quo = (__umulhi(r, a.q_magic) + r) >> a.q_shift;
+                lim = (int)(r - quo * (uint32_t)a.causal_q) + (a.cols - a.causal_q) + 1;
+            }
+        }
+        const char *xr = a.x + (int64_t)r * a.cols * S;
+        char *yr = a.y + (int64_t)r * a.cols * S;
+        uint4 xc[V];
+        int nv[V];
+#pragma unroll
+        for (int i = 0; i < V; i++) {
+            const int q = lane + i * G;
+            const int left = lim - q * E;
+            nv[i] = q < span ? (left < 0 ? 0 : (left > E ? E : left)) : 0;
+            xc[i] = nv[i] > 0 ? ld_chunk(xr + ((int64_t)q << 4)) : neg_inf_chunk<DT>();
+            if (nv[i] > 0 && nv[i] < E)
+                xc[i] = cut_chunk<DT>(xc[i], nv[i]);
+        }
+        const float mz = a.scale * MaxGroup<G>{}(packed_max<DT, V>(xc));
+        // warp-uniform, so that the reductions inside stay converged
+        if (__any_sync(0xffffffffu, valid && !(fabsf(mz) < kPairFreeMax))) {
+            masked_row_shifted<DT, false>(xr, yr, nullptr, a.cols, lim, a.scale, mz, lane, G, valid,
+                                          MaxSumGroup<DT, G>{});
+            continue;
+        }
+        const float c = Math<DT>::kExpBias - mz * kLog2e;
+        float ev[V][E];
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < V; i++) {
+            if (nv[i] > 0) {
+                float xf[E];
+                unpack<DT>(xc[i], xf);
+#pragma unroll
+                for (int e = 0; e < E; e++) {
+                    ev[i][e] = ex2_ftz(fmaf(xf[e], sl2e, c));  // a cut slot: 2^-inf = 0
+                    acc += ev[i][e];
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; e++)
+                    ev[i][e] = 0.f;
+            }
+        }
+        acc = SumGroup<DT, G>{}(acc);
+        const float inv = 1.0f / acc;
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < V; i++) {
+                const int q = lane + i * G;
+                if (q < span) {
+                    float o[E];
+#pragma unroll
+                    for (int e = 0; e < E; e++)
+                        o[e] = ev[i][e] * inv;
+                    st_chunk_stream(yr + ((int64_t)q << 4), pack<DT>(o));
+                }
+            }
+        }
+    }
+}
+
 namespace {
 
 MaskedArgs args_of(const MaskedLaunch &l)
@@ -578,9 +740,80 @@ int mblk_dt(const MaskedLaunch &l)
     }
 }
 
+// The lean form's conditions: a lanes-per-row plan for 16-bit rows on the
+// 16-byte grid, no additive mask, a positive finite scale, and row indices and
+// causal_q below 2^31 (32-bit division by the host's constant).
+bool lean_fits(const MaskedLaunch &l)
+{
+    return l.dtype != kF32 && l.plan.variant == SOFTMAX_VARIANT_ROWGROUP && l.plan.aligned && l.mask == nullptr &&
+           l.scale > 0.f && l.scale <= 3.4028234663852886e38f && l.rows <= INT32_MAX && l.causal_q <= INT32_MAX &&
+           l.cols <= INT32_MAX;
+}
+
+LeanArgs lean_args_of(const MaskedLaunch &l)
+{
+    LeanArgs a{(const char *)l.x, (char *)l.y, (uint32_t)l.rows, (int)l.cols, l.scale, (int)l.causal_q, 1u, 0u};
+    if (l.causal_q > 1) {
+        const uint64_t q = (uint64_t)l.causal_q;
+        uint32_t lg = 0;
+        while ((1ull << lg) < q)
+            lg++;  // ceil(log2 q)
+        a.q_shift = lg;
+        a.q_magic = (uint32_t)((((1ull << lg) - q) << 32) / q + 1);
+    }
+    return a;
+}
+
+template <int DT, int G, int V>
+int lean_one(const MaskedLaunch &l)
+{
+    return launch_pdl(k_masked_lean<DT, G, V>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+                      (cudaStream_t)l.stream, no_attr(), lean_args_of(l));
+}
+
+template <int DT, int G>
+int lean_v(const MaskedLaunch &l)
+{
+    switch (l.plan.chunks_per_thread) {
+    case 1:
+        return lean_one<DT, G, 1>(l);
+    case 2:
+        return lean_one<DT, G, 2>(l);
+    case 4:
+        return lean_one<DT, G, 4>(l);
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+template <int DT>
+int lean_dt(const MaskedLaunch &l)
+{
+    switch (l.plan.lanes_per_row) {
+    case 1:
+        return l.plan.chunks_per_thread == 1 ? lean_one<DT, 1, 1>(l) : (int)cudaErrorInvalidValue;
+    case 2:
+        return lean_v<DT, 2>(l);
+    case 4:
+        return lean_v<DT, 4>(l);
+    case 8:
+        return lean_v<DT, 8>(l);
+    case 16:
+        return lean_v<DT, 16>(l);
+    case 32:
+        return lean_v<DT, 32>(l);
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
 template <int DT>
 int masked_dt(const MaskedLaunch &l)
 {
+    if constexpr (DT != kF32) {
+        if (lean_fits(l))
+            return lean_dt<DT>(l);
+    }
     return l.plan.variant == SOFTMAX_VARIANT_ROWGROUP ? mrg_dt<DT>(l) : mblk_dt<DT>(l);
 }
 

@@ -192,3 +192,73 @@ def test_torch_api_and_errors():
     big = torch.randn(2, 20000, device="cuda")
     assert osd.softmax_fwd_masked(big.data_ptr(), torch.empty_like(big).data_ptr(), 2, 20000, 0, 1.0, 0, 0, 0,
                                   s) == -5
+
+
+# The lean form: 16-bit rows on the 16-byte grid, no additive mask, scale > 0
+# (the kernel takes the max on packed x and r mod causal_q by a multiply-high).
+LEAN_COLS = (8, 16, 24, 32, 40, 64, 120, 128, 136, 256, 264, 512, 520, 1000, 1024)
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+def test_lean_form_shapes_scales_and_causal_cuts(dt):
+    rng = np.random.default_rng(70 + dt)
+    for cols in LEAN_COLS:
+        rows = 37  # not a multiple of the rows a CTA takes
+        x = _quant(rng.normal(0, 5, (rows, cols)), dt)
+        for scale in (0.125, 80 ** -0.5, 1.0, 3.0):
+            for causal in (0, 1, 3, 7, cols, cols + 5):
+                rc, y = run_masked(x, dt, scale, None, causal)
+                assert rc == 0, (cols, scale, causal)
+                # causal_q > cols leaves the first queries of a block without a key
+                check_masked(x, y, dt, scale, None, causal, finite_expected=causal <= cols)
+        # the general kernel takes the other scales
+        for scale in (-0.5, 0.0):
+            rc, y = run_masked(x, dt, scale, None, 3)
+            assert rc == 0
+            check_masked(x, y, dt, scale, None, 3)
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+def test_lean_form_large_logits_and_the_pair_threshold(dt):
+    rng = np.random.default_rng(80 + dt)
+    x = _quant(rng.normal(0, 200, (64, 704)), dt)
+    for scale in (40.0, 40.0 + 2.0**-9, 80 ** -0.5 * 300):
+        rc, y = run_masked(x, dt, scale, None, 64)
+        assert rc == 0
+        check_masked(x, y, dt, scale, None, 64)
+    for centre in (440.0, 506.0, 520.0, -420.0, -506.0, -530.0):
+        xc = _quant(rng.uniform(centre - 100.0, centre, (48, 896)) / 0.7, dt)
+        for causal in (0, 48):
+            rc, y = run_masked(xc, dt, 0.7, None, causal)
+            assert rc == 0
+            check_masked(xc, y, dt, 0.7, None, causal)
+
+
+def test_lean_form_in_place_matches_out_of_place():
+    for dt, tdt in ((1, torch.float16), (2, torch.bfloat16)):
+        x = (torch.randn(4 * 512, 512, device="cuda") * 3).to(tdt)
+        y = torch.empty_like(x)
+        s = torch.cuda.current_stream().cuda_stream
+        assert osd.softmax_fwd_masked(x.data_ptr(), y.data_ptr(), 2048, 512, dt, 0.125, 0, 0, 512, s) == 0
+        xi = x.clone()
+        assert osd.softmax_fwd_masked(xi.data_ptr(), xi.data_ptr(), 2048, 512, dt, 0.125, 0, 0, 512, s) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(xi.view(torch.int16), y.view(torch.int16))
+
+
+def test_lean_form_large_row_indices():
+    # 2^21 + 5 rows: the causal cut of rows far from 0 (r mod causal_q by the
+    # multiply-high) checked on blocks that start at multiples of causal_q, so
+    # that the oracle sees the same query index i = r mod causal_q
+    rows, cols, q = (1 << 21) + 5, 64, 1000
+    g = torch.Generator(device="cuda").manual_seed(5)
+    x = (torch.randn(rows, cols, device="cuda", generator=g) * 4).half()
+    y = torch.empty_like(x)
+    s = torch.cuda.current_stream().cuda_stream
+    assert osd.softmax_fwd_masked(x.data_ptr(), y.data_ptr(), rows, cols, 1, 0.125, 0, 0, q, s) == 0
+    torch.cuda.synchronize()
+    for start in (0, 1000 * q, 2096 * q):
+        n = min(2 * q, rows - start)
+        xs = x[start:start + n].cpu().numpy()
+        ys = y[start:start + n].cpu().numpy()
+        check_masked(xs, ys, 1, 0.125, None, q)
