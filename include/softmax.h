@@ -328,7 +328,10 @@ typedef struct {
                                flight per thread per streaming step (STREAM, SPLITK); else 0 */
     int rows_per_tile;      /* BLOCK_TMA: consecutive rows moved by one bulk copy; else 0 */
     int stages;             /* BLOCK_TMA: shared-memory tiles in flight per CTA; SPLITK_GRID:
-                               ring buffers per CTA (0: streaming form); else 0 */
+                               ring buffers per CTA (0: streaming form); STREAM: 1 if each
+                               pass after the first walks the row from the other end (the
+                               rows in flight outgrow L2: a re-read starts on the chunks
+                               read last), 0 if every pass walks it forward; else 0 */
     int block_threads;      /* threads per CTA */
     int64_t grid_x;         /* CTAs along x */
     int64_t grid_y;         /* CTAs along y (SPLITK: rows; SPLITK_GRID: row groups) */

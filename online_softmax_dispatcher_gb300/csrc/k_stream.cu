@@ -12,13 +12,43 @@
 // partial sum costs up to an ulp, and a row whose max keeps growing would pile
 // those up past the fp32 error budget.
 //
+// Where the rows in flight outgrow L2, the re-read of a row misses if every
+// pass walks it forward: each chunk is read again a whole pass after its first
+// read.  The plan then asks (stages = 1) for each pass after the first to walk
+// the row from the other end, so that it starts on the chunks read last, still
+// in L2, and only the chunks read longest ago come from HBM again (16-bit:
+// forward, then backward; fp32: forward, backward, forward).
+//
 #include "common.cuh"
 #include "launch.h"
 #include "stream_passes.cuh"
 
 namespace osd {
 
+// A pass over chunks [0, nch) of a row taken step by step from the last
+// step: step s covers chunks [s span, (s + 1) span), span = blockDim x kStep,
+// and is handed to the pass function as a range of its own (one step each).
 template <int DT, bool ALIGNED>
+__device__ __forceinline__ typename Math<DT>::Acc sum_backward(const RowGeom &g, int64_t cols, float m)
+{
+    using M = Math<DT>;
+    const int64_t span = (int64_t)blockDim.x * kStep;
+    typename M::Acc acc = M::zero();
+    for (int64_t lo = g.nch > 0 ? (g.nch - 1) / span * span : -1; lo >= 0; lo -= span)
+        acc = M::merge(acc, pass_sum<DT, ALIGNED>(g, lo, lo + span < g.nch ? lo + span : g.nch, cols, m));
+    return acc;
+}
+
+template <int DT, bool ALIGNED>
+__device__ __forceinline__ void write_backward(const RowGeom &g, int64_t cols, float m, float inv, bool y_vec)
+{
+    const int64_t span = (int64_t)blockDim.x * kStep;
+    for (int64_t lo = g.nch > 0 ? (g.nch - 1) / span * span : -1; lo >= 0; lo -= span)
+        pass_write<DT, ALIGNED>(g, lo, lo + span < g.nch ? lo + span : g.nch, cols, m, inv, y_vec);
+}
+
+// BACK: the passes after the first alternate direction (see above).
+template <int DT, bool ALIGNED, bool BACK>
 __global__ void __launch_bounds__(kStreamThreads)
     k_stream(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int y_vec)
 {
@@ -29,26 +59,32 @@ __global__ void __launch_bounds__(kStreamThreads)
     __shared__ MD smd[32];
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const RowGeom g = row_geom<DT, ALIGNED>(x, y, r, cols);
-        float m, inv;
         if constexpr (DT == kF32) {
-            m = block_max(pass_max<DT, ALIGNED>(g, 0, g.nch, cols), smax);
-            const auto acc = block_sum<DT>(pass_sum<DT, ALIGNED>(g, 0, g.nch, cols, m), ssum);
-            inv = 1.0f / M::value(acc);
+            const float m = block_max(pass_max<DT, ALIGNED>(g, 0, g.nch, cols), smax);
+            typename M::Acc acc;
+            if constexpr (BACK)
+                acc = sum_backward<DT, ALIGNED>(g, cols, m);
+            else
+                acc = pass_sum<DT, ALIGNED>(g, 0, g.nch, cols, m);
+            const float inv = 1.0f / M::value(block_sum<DT>(acc, ssum));
+            pass_write<DT, ALIGNED>(g, 0, g.nch, cols, m, inv, y_vec != 0);
         } else {
             const MD md = block_md<DT>(pass_online<DT, ALIGNED>(g, 0, g.nch, cols), smd);
-            m = md.m;
-            inv = 1.0f / md.d;
+            const float inv = 1.0f / md.d;
+            if constexpr (BACK)
+                write_backward<DT, ALIGNED>(g, cols, md.m, inv, y_vec != 0);
+            else
+                pass_write<DT, ALIGNED>(g, 0, g.nch, cols, md.m, inv, y_vec != 0);
         }
-        pass_write<DT, ALIGNED>(g, 0, g.nch, cols, m, inv, y_vec != 0);
     }
 }
 
 namespace {
 
-template <int DT, bool A>
+template <int DT, bool A, bool BACK>
 int launch_stream_one(const Launch &l)
 {
-    return launch_pdl(k_stream<DT, A>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
+    return launch_pdl(k_stream<DT, A, BACK>, dim3((unsigned)l.plan.grid_x), dim3(l.plan.block_threads), 0,
                       (cudaStream_t)l.stream, no_attr(), (const char *)l.x, (char *)l.y, l.rows, l.cols,
                       (int)l.plan.y_vector);
 }
@@ -56,7 +92,9 @@ int launch_stream_one(const Launch &l)
 template <int DT>
 int stream_dt(const Launch &l)
 {
-    return l.plan.aligned ? launch_stream_one<DT, true>(l) : launch_stream_one<DT, false>(l);
+    if (l.plan.stages == 1)
+        return l.plan.aligned ? launch_stream_one<DT, true, true>(l) : launch_stream_one<DT, false, true>(l);
+    return l.plan.aligned ? launch_stream_one<DT, true, false>(l) : launch_stream_one<DT, false, false>(l);
 }
 
 }  // namespace

@@ -283,6 +283,46 @@ def test_custom_plans_persistence_and_tiles():
         check(x, torch_to_np(yt, 1), 1)
 
 
+def test_stream_walks_both_ways():
+    # the streaming kernel with every pass forward (stages 0) and with the
+    # passes after the first walking back from the row's end (stages 1): rows
+    # of several full steps (512 threads x 8 chunks), a partial last step, a
+    # row shorter than one step, rows off the 16-byte grid, special rows
+    rng = np.random.default_rng(17)
+    rc, dev = osd.softmax_device_query()
+    assert rc == 0
+    names = ("fp32", "fp16", "bf16")
+    ninf = {0: np.float32(-np.inf), 1: np.float16(-np.inf), 2: np.uint16(0xFF80)}
+    pinf = {0: np.float32(np.inf), 1: np.float16(np.inf), 2: np.uint16(0x7F80)}
+    for dt in (0, 1, 2):
+        e = ELEM[dt]
+        E = 16 // e
+        for cols, off in ((2 * 4096 * E, 0), (2 * 4096 * E + 3 * E, 0), (1000, 0), (4096 * E + 5, 1)):
+            x = W._round_to(rng.normal(0, 4, (5, cols)), names[dt])
+            x[3, : cols // 3] = ninf[dt]
+            x[4, cols // 2] = pinf[dt]
+            # the plan for run()'s buffers: a 256-byte aligned base shifted by off elements
+            rc, base = osd.softmax_plan(dev, (1 << 40) + off * e, (1 << 40) + (1 << 38) + off * e, 5, cols, dt,
+                                        osd.VARIANTS["stream"])
+            assert rc == 0 and base.aligned == (off == 0 and cols * e % 16 == 0)
+            outs = []
+            for stages in (0, 1):
+                p = osd.LaunchPlan(**{**base.as_dict(), "stages": stages})
+                rc, y = run(x, dt, plan=p, x_off=off, y_off=off)
+                assert rc == 0, (dt, cols, stages)
+                check(x[:4], y[:4], dt)
+                assert np.isnan(oracle.decode(y[4:], dt)).all()  # +inf in the row: inf - inf
+                outs.append(y)
+            if dt:
+                # the write pass goes element by element: its order changes no bit
+                assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16)), (dt, cols)
+    xd = torch.randn(4, 3 * 4096 * 8, device="cuda", dtype=torch.float16)
+    yd = torch.empty_like(xd)
+    bad = osd.LaunchPlan(**{**osd.plan_for(xd, yd, "stream").as_dict(), "stages": 2})
+    with pytest.raises(osd.SoftmaxError):
+        osd.softmax(xd, out=yd, plan=bad)
+
+
 def test_bad_custom_plan_is_refused():
     x = torch.randn(64, 512, device="cuda", dtype=torch.float16)
     y = torch.empty_like(x)
