@@ -87,7 +87,8 @@ typedef enum {
     SOFTMAX_VARIANT_STREAM = 4,    /* one CTA per row, online (m, d) pass then a re-read pass;
                                       any cols */
     SOFTMAX_VARIANT_SPLITK = 5,    /* a thread-block cluster per row; partial (m, d) merged
-                                      through distributed shared memory */
+                                      through distributed shared memory (one CTA per row when
+                                      there are at least as many rows as SMs) */
     SOFTMAX_VARIANT_SPLITK_WIDE = 6, /* P CTAs per row over all SMs, partials merged through a
                                         global workspace in a second launch (softmax_fwd_ws
                                         only: it needs the workspace) */
@@ -328,10 +329,8 @@ typedef struct {
                                flight per thread per streaming step (STREAM, SPLITK); else 0 */
     int rows_per_tile;      /* BLOCK_TMA: consecutive rows moved by one bulk copy; else 0 */
     int stages;             /* BLOCK_TMA: shared-memory tiles in flight per CTA; SPLITK_GRID:
-                               ring buffers per CTA (0: streaming form); STREAM: 1 if each
-                               pass after the first walks the row from the other end (the
-                               rows in flight outgrow L2: a re-read starts on the chunks
-                               read last), 0 if every pass walks it forward; else 0 */
+                               ring buffers per CTA (0: streaming form); SPLITK: shared-memory
+                               stages per CTA; else 0 */
     int block_threads;      /* threads per CTA */
     int64_t grid_x;         /* CTAs along x */
     int64_t grid_y;         /* CTAs along y (SPLITK: rows; SPLITK_GRID: row groups) */
@@ -341,6 +340,12 @@ typedef struct {
     int aligned;            /* 1 if every row of x and y starts 16-byte aligned and is a whole
                                number of 16-byte chunks */
     int y_vector;           /* 1 if y rows share x rows' 16-byte phase (vector stores) */
+    int back_passes;        /* STREAM: 1 if each pass over a row after the first walks it
+                               from the other end, so that a re-read starts on the chunks
+                               read last, still in L2 (the dispatcher sets it when the rows
+                               in flight outgrow half of L2); 0 if every pass walks forward;
+                               0 for the other variants.  It changes no 16-bit output bit
+                               (fp32: the order of the sum) */
 } softmax_launch_plan;
 
 /*

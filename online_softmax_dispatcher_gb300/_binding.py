@@ -77,7 +77,8 @@ class LaunchPlan(ctypes.Structure):
                 ("chunks_per_thread", ctypes.c_int), ("rows_per_tile", ctypes.c_int),
                 ("stages", ctypes.c_int), ("block_threads", ctypes.c_int),
                 ("grid_x", ctypes.c_int64), ("grid_y", ctypes.c_int64), ("cluster_x", ctypes.c_int),
-                ("smem_bytes", ctypes.c_int), ("aligned", ctypes.c_int), ("y_vector", ctypes.c_int)]
+                ("smem_bytes", ctypes.c_int), ("aligned", ctypes.c_int), ("y_vector", ctypes.c_int),
+                ("back_passes", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

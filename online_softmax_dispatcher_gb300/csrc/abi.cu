@@ -313,14 +313,16 @@ namespace {
 
 // The plan softmax_fwd_ws launches: the dispatcher's choice, with the two-launch
 // SPLITK_WIDE (partials in the caller's workspace) in place of the cluster or
-// grid split (few, very long rows).
+// grid split of few, very long rows (fewer rows than SMs; many long rows keep
+// the cluster split's one CTA per row, which needs no workspace).
 int plan_ws(const DeviceCache &dc, const void *x, const void *y, int64_t rows, int64_t cols, int dtype,
             softmax_launch_plan *plan)
 {
     int rc = softmax_plan(&dc.info, x, y, rows, cols, dtype, SOFTMAX_VARIANT_AUTO, plan);
     if (rc != SOFTMAX_OK)
         return rc;
-    if (plan->variant == SOFTMAX_VARIANT_SPLITK || plan->variant == SOFTMAX_VARIANT_SPLITK_GRID) {
+    if ((plan->variant == SOFTMAX_VARIANT_SPLITK && rows < dc.info.sm_count) ||
+        plan->variant == SOFTMAX_VARIANT_SPLITK_GRID) {
         softmax_launch_plan wide;
         if (softmax_plan(&dc.info, x, y, rows, cols, dtype, SOFTMAX_VARIANT_SPLITK_WIDE, &wide) == SOFTMAX_OK)
             *plan = wide;

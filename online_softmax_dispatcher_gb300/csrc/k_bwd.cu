@@ -326,7 +326,10 @@ __global__ void __launch_bounds__(512, V >= 8 ? 1 : 2) k_bwd_block(const BwdArgs
     }
 }
 
-template <int DT, bool ALIGNED>
+// BACK: the write pass walks the row from its end, step by step, so that it
+// starts on the y and dy chunks the sum pass read last (still in L2 when the
+// rows in flight outgrow it); it changes no output bit.
+template <int DT, bool ALIGNED, bool BACK>
 __global__ void __launch_bounds__(kStreamThreads) k_bwd_stream(const BwdArgs a)
 {
     pdl_enter();
@@ -351,7 +354,11 @@ __global__ void __launch_bounds__(kStreamThreads) k_bwd_stream(const BwdArgs a)
         }
         acc = block_sum<kF32>(acc, slots);
         const float s = acc.s + acc.c;
-        for (int64_t k0 = threadIdx.x; k0 < g.nch; k0 += T * U) {
+        const int64_t span = T * U;
+        const int64_t nst = (g.nch + span - 1) / span;
+        for (int64_t st = 0; st < nst; st++) {
+            // k >= nch loads give neutral chunks and are not stored
+            const int64_t k0 = threadIdx.x + (BACK ? nst - 1 - st : st) * span;
             uint4 yc[U], dc[U];
 #pragma unroll
             for (int u = 0; u < U; u++) {
@@ -479,8 +486,16 @@ int bwd_stream_dt(const BwdLaunch &l)
 {
     const dim3 grid((unsigned)l.plan.grid_x), block(l.plan.block_threads);
     if (l.plan.aligned)
-        return launch_pdl(k_bwd_stream<DT, true>, grid, block, 0, (cudaStream_t)l.stream, no_attr(), args_of(l));
-    return launch_pdl(k_bwd_stream<DT, false>, grid, block, 0, (cudaStream_t)l.stream, no_attr(), args_of(l));
+        return l.plan.back_passes == 1
+                   ? launch_pdl(k_bwd_stream<DT, true, true>, grid, block, 0, (cudaStream_t)l.stream, no_attr(),
+                                args_of(l))
+                   : launch_pdl(k_bwd_stream<DT, true, false>, grid, block, 0, (cudaStream_t)l.stream, no_attr(),
+                                args_of(l));
+    return l.plan.back_passes == 1
+               ? launch_pdl(k_bwd_stream<DT, false, true>, grid, block, 0, (cudaStream_t)l.stream, no_attr(),
+                            args_of(l))
+               : launch_pdl(k_bwd_stream<DT, false, false>, grid, block, 0, (cudaStream_t)l.stream, no_attr(),
+                            args_of(l));
 }
 
 template <int DT>

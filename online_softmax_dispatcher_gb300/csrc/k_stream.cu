@@ -14,7 +14,7 @@
 //
 // Where the rows in flight outgrow L2, the re-read of a row misses if every
 // pass walks it forward: each chunk is read again a whole pass after its first
-// read.  The plan then asks (stages = 1) for each pass after the first to walk
+// read.  The plan then asks (back_passes = 1) for each pass after the first to walk
 // the row from the other end, so that it starts on the chunks read last, still
 // in L2, and only the chunks read longest ago come from HBM again (16-bit:
 // forward, then backward; fp32: forward, backward, forward).
@@ -92,7 +92,7 @@ int launch_stream_one(const Launch &l)
 template <int DT>
 int stream_dt(const Launch &l)
 {
-    if (l.plan.stages == 1)
+    if (l.plan.back_passes == 1)
         return l.plan.aligned ? launch_stream_one<DT, true, true>(l) : launch_stream_one<DT, false, true>(l);
     return l.plan.aligned ? launch_stream_one<DT, true, false>(l) : launch_stream_one<DT, false, false>(l);
 }

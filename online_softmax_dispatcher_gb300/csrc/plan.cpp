@@ -193,7 +193,7 @@ bool tma_fits(const Geometry &g, const softmax_device_info &dev)
     return tma_stage_bytes(g, 1) * 2 <= tma_budget(dev);
 }
 
-// STREAM: one CTA per row.  stages = 1 (the passes after the first walk each
+// STREAM: one CTA per row.  back_passes = 1 (the passes after the first walk each
 // row from the other end) where the rows in flight hold more than half of L2,
 // so that a re-read starts on the chunks read last; the rows in flight are the
 // resident CTAs, 2 per SM for rows on the 16-byte grid (those instances fit 64
@@ -209,13 +209,15 @@ void plan_stream(const Geometry &g, int64_t rows, const softmax_device_info &dev
     p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
     const int64_t resident = int64_t(dev.sm_count > 0 ? dev.sm_count : 1) * (g.aligned ? 2 : 1);
     const int64_t in_flight = rows < resident ? rows : resident;
-    p.stages = dev.l2_bytes > 0 && in_flight * g.row_bytes > int64_t(dev.l2_bytes) / 2 ? 1 : 0;
+    p.back_passes = dev.l2_bytes > 0 && in_flight * g.row_bytes > int64_t(dev.l2_bytes) / 2 ? 1 : 0;
 }
 
 // Cluster size (power of two, <= 16): about two CTAs per SM over all rows,
 // and at least two full shared-memory stages of work per CTA.
 int splitk_cluster(const Geometry &g, int64_t rows, const softmax_device_info &dev)
 {
+    if (rows >= dev.sm_count)
+        return 1;  // as many rows as SMs: one CTA per row
     int64_t c = next_pow2(ceil_div(2 * int64_t(dev.sm_count > 0 ? dev.sm_count : 1), rows > 0 ? rows : 1));
     const int64_t by_work = pow2_floor(g.nch_max / (2 * int64_t(kSplitStageBytes / 16)));
     if (c > by_work)
@@ -356,6 +358,23 @@ bool splitk_possible(int64_t rows, const softmax_device_info &dev)
            dev.max_smem_optin >= kSplitStages * kSplitStageBytes + 1024;
 }
 
+// Many 16-bit rows on the 16-byte grid of more than 256 KiB and less than 2
+// MiB: the cluster split with one CTA per row, whose bulk copies keep 192 KB
+// in flight per SM and whose one row per SM in flight leaves more of a row in
+// L2 for its re-read, beat the streaming kernel (measured on GB300, us:
+// [3072, 196608] fp16 448 against 507; [2048, 262144] fp16 426 against 458,
+// bf16 428 against 458; [1024, 262144] fp16 222 against 237; [2048, 393216]
+// bf16 683 against 702; [1024, 524288] fp16 465 against 481; level at 256
+// KiB, [4096, 131072] bf16 438 against 436, and at 2 MiB, [512, 1048576] fp16
+// 488 against 484).  fp32 rows and shorter rows stay with the streaming
+// kernel ([1024, 262144] fp32 714 against 622 - 657, [4096, 65600] fp16 278
+// against 185).
+bool splitk_long_rows(const Geometry &g, int64_t rows, const softmax_device_info &dev)
+{
+    return g.S == 2 && g.aligned && rows >= dev.sm_count && rows <= 65535 && splitk_possible(rows, dev) &&
+           g.row_bytes > (int64_t(1) << 18) && g.row_bytes < (int64_t(1) << 21);
+}
+
 }  // namespace
 
 int validate_args(const void *x, const void *y, int64_t rows, int64_t cols, int dtype)
@@ -394,6 +413,9 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
         return SOFTMAX_ERR_INVALID_ARG;
     if (p.grid_x < 1 || p.grid_x > INT32_MAX || p.smem_bytes < 0)
         return SOFTMAX_ERR_INVALID_ARG;
+    // the walk direction of the streaming kernel's re-read passes
+    if (p.back_passes != 0 && (p.back_passes != 1 || p.variant != SOFTMAX_VARIANT_STREAM))
+        return SOFTMAX_ERR_INVALID_ARG;
     const int V = p.chunks_per_thread;
     switch (p.variant) {
     case SOFTMAX_VARIANT_ROWGROUP: {
@@ -430,7 +452,7 @@ int validate_plan(const softmax_device_info &dev, const void *x, const void *y, 
     }
     case SOFTMAX_VARIANT_STREAM:
         if (V != kStreamUnroll || p.block_threads > kStreamThreads || p.grid_y != 1 || p.cluster_x != 1 ||
-            p.stages < 0 || p.stages > 1)
+            p.stages != 0)
             return SOFTMAX_ERR_INVALID_ARG;
         return SOFTMAX_OK;
     case SOFTMAX_VARIANT_SPLITK_WIDE:
@@ -757,6 +779,12 @@ int plan_bwd(const softmax_device_info &dev, const void *y, const void *dy, cons
         p.chunks_per_thread = 4;
         p.block_threads = kStreamThreads;
         p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
+        // the write pass walks each row from its end (back_passes = 1) where the
+        // rows in flight (2 CTAs per SM on the 16-byte grid, else 1) hold
+        // more than half of L2 in y and dy, as the forward streaming kernel
+        const int64_t resident = int64_t(dev.sm_count > 0 ? dev.sm_count : 1) * (aligned ? 2 : 1);
+        const int64_t in_flight = rows < resident ? rows : resident;
+        p.back_passes = dev.l2_bytes > 0 && in_flight * 2 * g.row_bytes > int64_t(dev.l2_bytes) / 2 ? 1 : 0;
     } else {
         return SOFTMAX_ERR_UNSUPPORTED_SHAPE;
     }
@@ -815,6 +843,8 @@ extern "C" __attribute__((visibility("default"))) int softmax_plan(
         else if (tma_fits(g, *dev))
             v = SOFTMAX_VARIANT_BLOCK_TMA;
         else if (rows < dev->sm_count && splitk_possible(rows, *dev))
+            v = SOFTMAX_VARIANT_SPLITK;
+        else if (splitk_long_rows(g, rows, *dev))
             v = SOFTMAX_VARIANT_SPLITK;
         else
             v = SOFTMAX_VARIANT_STREAM;

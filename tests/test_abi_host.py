@@ -259,8 +259,9 @@ def test_library_refuses_to_load_when_missing(tmp_path, monkeypatch):
 
 def test_plan_struct_layout():
     # the ctypes mirror must match the C struct (ints, then int64 grid dims)
-    assert ctypes.sizeof(B.LaunchPlan) == 56
+    assert ctypes.sizeof(B.LaunchPlan) == 64
     assert B.LaunchPlan.grid_x.offset == 24 and B.LaunchPlan.cluster_x.offset == 40
+    assert B.LaunchPlan.back_passes.offset == 56
     assert ctypes.sizeof(B.DeviceInfo) == 24
 
 
@@ -359,7 +360,7 @@ def test_long_block_rows_dispatch(lib):
 
 
 def test_stream_walk_direction(lib):
-    # stages = 1 (re-read passes walk each row from the other end) once the
+    # back_passes = 1 (re-read passes walk each row from the other end) once the
     # rows in flight (2 CTAs per SM on the 16-byte grid, else 1) hold more
     # than half of L2
     half = GB300.l2_bytes // 2
@@ -377,8 +378,43 @@ def test_stream_walk_direction(lib):
         assert rc == B.OK and p.variant == B.VARIANT_STREAM, (rows, cols)
         resident = 152 * (2 if p.aligned else 1)
         assert (min(rows, resident) * cols * e > half) == bool(want)
-        assert p.stages == want, (rows, cols, dt, p.stages)
+        assert p.back_passes == want and p.stages == 0, (rows, cols, dt, p.back_passes)
     # a device that reports no L2 size: forward
     dev = B.DeviceInfo(**{**{f: getattr(GB300, f) for f, _ in GB300._fields_}, "l2_bytes": 0})
     rc, p = B.softmax_plan(dev, BASE, BASE + (1 << 36), 2048, 262144, 1, B.VARIANT_STREAM)
-    assert rc == B.OK and p.stages == 0
+    assert rc == B.OK and p.back_passes == 0
+
+
+def test_bwd_stream_walk_direction(lib):
+    half = GB300.l2_bytes // 2
+    for rows, cols, dt, off, want in ((400, 65600, 1, 0, 1), (4096, 40000, 1, 0, 0), (4096, 128256, 2, 0, 1),
+                                      (512, 262144, 0, 0, 1), (400, 65601, 1, 1, 0), (40, 65536, 0, 0, 0)):
+        e = (4, 2, 2)[dt]
+        rc, p = B.softmax_bwd_plan(GB300, BASE + off * e, BASE + (1 << 36) + off * e, BASE + (2 << 36) + off * e,
+                                   rows, cols, dt, 0)
+        assert rc == B.OK and p.variant == B.VARIANT_STREAM, (rows, cols)
+        resident = 152 * (2 if p.aligned else 1)
+        assert (min(rows, resident) * 2 * cols * e > half) == bool(want)
+        assert p.back_passes == want, (rows, cols, dt)
+
+
+def test_many_long_16bit_rows_take_the_cluster_split(lib):
+    # 16-bit rows on the 16-byte grid of more than 256 KiB and less than 2 MiB,
+    # at least as many as SMs: the cluster split with one CTA per row
+    for rows, cols, dt, off, want in ((2048, 262144, 1, 0, B.VARIANT_SPLITK), (3072, 196608, 1, 0, B.VARIANT_SPLITK),
+                                      (152, 262144, 2, 0, B.VARIANT_SPLITK), (1024, 524288, 1, 0, B.VARIANT_SPLITK),
+                                      (4096, 131072, 2, 0, B.VARIANT_STREAM),   # 256 KiB
+                                      (512, 1 << 20, 1, 0, B.VARIANT_STREAM),   # 2 MiB
+                                      (1024, 262144, 0, 0, B.VARIANT_STREAM),   # fp32
+                                      (2048, 262143, 1, 1, B.VARIANT_STREAM),   # off the grid
+                                      (70000, 131080, 1, 0, B.VARIANT_STREAM)):  # more rows than a grid's y
+        e = (4, 2, 2)[dt]
+        rc, p = B.softmax_plan(GB300, BASE + off * e, BASE + (1 << 38) + off * e, rows, cols, dt)
+        assert rc == B.OK and p.variant == want, (rows, cols, dt, p.variant)
+        if want == B.VARIANT_SPLITK:
+            assert (p.cluster_x, p.grid_x, p.grid_y, p.back_passes) == (1, 1, rows, 0)
+    # a forced cluster split on at least as many rows as SMs: one CTA per row
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 38), 200, 1 << 20, 1, B.VARIANT_SPLITK)
+    assert rc == B.OK and p.cluster_x == 1 and p.grid_y == 200
+    rc, p = B.softmax_plan(GB300, BASE, BASE + (1 << 38), 100, 1 << 20, 1, B.VARIANT_SPLITK)
+    assert rc == B.OK and p.cluster_x == 4

@@ -134,3 +134,24 @@ def test_bwd_torch_api_and_alias():
     # y and dy may be the same buffer (both are only read)
     dx2 = osd.softmax_backward(y, y)
     check_bwd(y.cpu().numpy(), y.cpu().numpy(), dx2.cpu().numpy(), 0)
+
+
+def test_bwd_stream_walks_back_on_long_rows():
+    # the streaming backward kernel's write pass walks each row from its end
+    # where the rows in flight hold more than half of L2 in y and dy: parity
+    # on shapes on both sides of that line, on and off the 16-byte grid
+    rc, dev = osd.softmax_device_query()
+    assert rc == 0
+    for dt, rows, cols, off in ((1, 400, 65600, 0), (2, 400, 65600, 0), (0, 320, 65536, 0), (1, 400, 131073, 1),
+                                (1, 400, 65601, 1), (0, 40, 65536, 0)):
+        e = ELEM[dt]
+        b = 1 << 40
+        rc, p = osd.softmax_bwd_plan(dev, b + off * e, b + (1 << 38) + off * e, b + (2 << 38) + off * e, rows, cols,
+                                     dt, 0)
+        assert rc == 0 and p.variant == osd.VARIANTS["stream"]
+        resident = dev.sm_count * (2 if p.aligned else 1)
+        assert p.back_passes == int(min(rows, resident) * 2 * cols * e > dev.l2_bytes // 2), (dt, rows, cols)
+        y, dy = make_case(rows, cols, dt, seed=rows + cols)
+        rc, dx = run_bwd(y, dy, dt, 0, (off, off, off))
+        assert rc == 0
+        check_bwd(y, dy, dx, dt)

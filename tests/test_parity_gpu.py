@@ -284,8 +284,8 @@ def test_custom_plans_persistence_and_tiles():
 
 
 def test_stream_walks_both_ways():
-    # the streaming kernel with every pass forward (stages 0) and with the
-    # passes after the first walking back from the row's end (stages 1): rows
+    # the streaming kernel with every pass forward (back_passes 0) and with
+    # the passes after the first walking back from the row's end (1): rows
     # of several full steps (512 threads x 8 chunks), a partial last step, a
     # row shorter than one step, rows off the 16-byte grid, special rows
     rng = np.random.default_rng(17)
@@ -306,10 +306,10 @@ def test_stream_walks_both_ways():
                                         osd.VARIANTS["stream"])
             assert rc == 0 and base.aligned == (off == 0 and cols * e % 16 == 0)
             outs = []
-            for stages in (0, 1):
-                p = osd.LaunchPlan(**{**base.as_dict(), "stages": stages})
+            for back in (0, 1):
+                p = osd.LaunchPlan(**{**base.as_dict(), "back_passes": back})
                 rc, y = run(x, dt, plan=p, x_off=off, y_off=off)
-                assert rc == 0, (dt, cols, stages)
+                assert rc == 0, (dt, cols, back)
                 check(x[:4], y[:4], dt)
                 assert np.isnan(oracle.decode(y[4:], dt)).all()  # +inf in the row: inf - inf
                 outs.append(y)
@@ -318,9 +318,43 @@ def test_stream_walks_both_ways():
                 assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16)), (dt, cols)
     xd = torch.randn(4, 3 * 4096 * 8, device="cuda", dtype=torch.float16)
     yd = torch.empty_like(xd)
-    bad = osd.LaunchPlan(**{**osd.plan_for(xd, yd, "stream").as_dict(), "stages": 2})
+    for field, value in (("back_passes", 2), ("stages", 1)):
+        bad = osd.LaunchPlan(**{**osd.plan_for(xd, yd, "stream").as_dict(), field: value})
+        with pytest.raises(osd.SoftmaxError):
+            osd.softmax(xd, out=yd, plan=bad)
+    # only the streaming kernel takes back_passes
+    xs = torch.randn(64, 512, device="cuda", dtype=torch.float16)
+    ys = torch.empty_like(xs)
+    bad = osd.LaunchPlan(**{**osd.plan_for(xs, ys).as_dict(), "back_passes": 1})
     with pytest.raises(osd.SoftmaxError):
-        osd.softmax(xd, out=yd, plan=bad)
+        osd.softmax(xs, out=ys, plan=bad)
+
+
+def test_many_long_rows_cluster_split():
+    # 16-bit rows of 384 KiB, more of them than SMs: the dispatcher's cluster
+    # split with one CTA per row, against the oracle; the workspace entry point
+    # keeps that plan (it needs no workspace) and gives the same bits
+    rc, dev = osd.softmax_device_query()
+    assert rc == 0
+    rng = np.random.default_rng(23)
+    rows, cols = dev.sm_count + 9, 196608
+    for dt in (1, 2):
+        x = W._round_to(rng.normal(0, 3, (rows, cols)), ("fp32", "fp16", "bf16")[dt])
+        x[5, : cols // 2] = (np.float16(-np.inf) if dt == 1 else np.uint16(0xFF80))
+        xd = np_to_torch(x, dt).cuda()
+        yd = torch.empty_like(xd)
+        p = osd.plan_for(xd, yd)
+        assert p.variant == osd.VARIANTS["splitk"] and p.cluster_x == 1 and p.grid_y == rows
+        s = torch.cuda.current_stream().cuda_stream
+        assert osd.softmax_fwd(xd.data_ptr(), yd.data_ptr(), rows, cols, dt, s) == 0
+        rc, need = osd.softmax_workspace_size(xd.data_ptr(), yd.data_ptr(), rows, cols, dt)
+        assert rc == 0 and need == 0
+        yw = torch.empty_like(xd)
+        ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+        assert osd.softmax_fwd_ws(xd.data_ptr(), yw.data_ptr(), rows, cols, dt, ws.data_ptr(), 16, s) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(yd.view(torch.int16), yw.view(torch.int16))
+        check(x, torch_to_np(yd, dt), dt)
 
 
 def test_bad_custom_plan_is_refused():
