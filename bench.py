@@ -438,17 +438,26 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         # causal limit are never read), all of y
         esz = set_bytes // (2 * rows * cols)
         set_bytes = masked_visible_elems(rows, cols, causal_q) * esz + rows * cols * esz
+        mask_t, mp, mrows = None, None, 0
+        if args.mask:
+            # an ALiBi-style additive bias, -0.05 x the query-key distance, one
+            # row per query of the block (read by every block: counted once)
+            qi = torch.arange(causal_q, device=dev, dtype=torch.float64)[:, None] + (cols - causal_q)
+            kj = torch.arange(cols, device=dev, dtype=torch.float64)[None, :]
+            mask_t = (-0.05 * (qi - kj).abs()).to(xs[0].dtype).contiguous()
+            mp, mrows = mask_t.data_ptr(), causal_q
+            set_bytes += mask_t.numel() * mask_t.element_size()
         rc, plan = osd.softmax_masked_plan(osd.softmax_device_query()[1], ptrs[0][0], ptrs[0][1], rows, cols, dt)
         if rc != 0:
             raise osd.SoftmaxError(rc)
 
         def api(dev_in, out, i=0):
-            osd.softmax_masked(dev_in[0].view(-1, causal_q, cols), scale=0.125, causal=True,
+            osd.softmax_masked(dev_in[0].view(-1, causal_q, cols), scale=0.125, mask=mask_t, causal=True,
                                out=out.view(-1, causal_q, cols))
 
         def step(i):
             xp, yp = ptrs[i % nbuf]
-            rc = masked(xp, yp, rows, cols, dt, 0.125, None, 0, causal_q, s)
+            rc = masked(xp, yp, rows, cols, dt, 0.125, mp, mrows, causal_q, s)
             if rc != 0:
                 raise osd.SoftmaxError(rc)
     elif args.workspace:
@@ -574,6 +583,8 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     per_launch_ms = ms / args.steps
     achieved = set_bytes / (per_launch_ms / 1e3) / 1e9
     rec_key = f"{w.name}:ws" if args.workspace else (w.name if args.op == "forward" else f"{w.name}:{args.op}")
+    if args.op == "masked" and args.mask:
+        rec_key += "+mask"
     traffic, tsrc = recorded_traffic(rec_key, variant, plan.as_dict())
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
@@ -606,7 +617,9 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     }
     if args.op == "masked":
         res["roofline"]["algorithmic_bytes_note"] = (
-            "visible x (keys past the causal limit are never read) + all of y")
+            "visible x (keys past the causal limit are never read) + all of y"
+            + (" + the additive mask once" if args.mask else ""))
+        res["config"]["mask"] = "ALiBi-style [512, cols], -0.05 x distance" if args.mask else None
     if per_config_wanted(args):
         # free the headline's buffers first: the vocabulary workload needs ~8 GB
         del xs, ys, dev_ins, out_devs
@@ -740,6 +753,9 @@ def main():
                          "and a causal cut over query blocks of 512 rows (attention scores [B, H, 512, cols]); "
                          "norm times layernorm_fwd / rmsnorm_fwd on a normalisation workload "
                          "(ln_fp16_131040x192, ln_fp16_32760x384, rms_bf16_16384x4096)")
+    ap.add_argument("--mask", action="store_true",
+                    help="with --op masked: add an additive ALiBi-style bias (-0.05 x query-key distance, one "
+                         "row per query of a 512-row block), which the general masked kernel serves")
     ap.add_argument("--workspace", action="store_true",
                     help="forward through softmax_fwd_ws with a workspace the bench allocates (lets few, very "
                          "long rows use every SM)")
@@ -753,6 +769,8 @@ def main():
     args = ap.parse_args()
     if args.shape is not None and args.op == "norm":
         ap.error("--shape is for the softmax operations (norm workloads are named by --workload)")
+    if args.mask and args.op != "masked":
+        ap.error("--mask applies to --op masked")
     if args.variant is not None and (args.op != "forward" or args.workspace):
         ap.error("--variant applies to the forward softmax without --workspace")
     if args.warmup < 3:

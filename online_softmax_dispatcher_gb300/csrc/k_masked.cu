@@ -58,12 +58,33 @@ struct MaskedArgs {
     const char *mask;  // NULL: no additive mask
     int64_t mask_rows;
     int64_t causal_q;  // 0: no causal cut
+    // rows, causal_q and mask_rows all below 2^31: r mod causal_q and r mod
+    // mask_rows by a multiply-high with these host-made constants (the lean
+    // form's account below), not by a 64-bit division
+    int div32;
+    uint32_t q_magic, q_shift, m_magic, m_shift;
 };
+
+// r mod d for 0 <= r < 2^31 and 1 <= d < 2^31 by the round-up multiply-high.
+__device__ __forceinline__ uint32_t mod_u31(uint32_t r, uint32_t d, uint32_t magic, uint32_t shift)
+{
+    return r - ((__umulhi(r, magic) + r) >> shift) * d;
+}
 
 // Visible keys of row r: j < limit.
 __device__ __forceinline__ int64_t visible_limit(const MaskedArgs &a, int64_t r)
 {
-    return a.causal_q > 0 ? r % a.causal_q + (a.cols - a.causal_q) + 1 : a.cols;
+    if (a.causal_q <= 0)
+        return a.cols;
+    const int64_t i = a.div32 ? (int64_t)mod_u31((uint32_t)r, (uint32_t)a.causal_q, a.q_magic, a.q_shift)
+                              : r % a.causal_q;
+    return i + (a.cols - a.causal_q) + 1;
+}
+
+// The mask row of row r.
+__device__ __forceinline__ int64_t mask_row_of(const MaskedArgs &a, int64_t r)
+{
+    return a.div32 ? (int64_t)mod_u31((uint32_t)r, (uint32_t)a.mask_rows, a.m_magic, a.m_shift) : r % a.mask_rows;
 }
 
 // A mask row is typically shared by many rows, so its reads may allocate in L1.
@@ -289,7 +310,7 @@ __device__ __forceinline__ void masked_row(const MaskedArgs &a, int64_t r, bool 
     constexpr bool KEEP_Z = KEEP && DT == kF32;  // fp32 logit pairs kept from the max pass
     const int64_t rr = valid ? r : 0;
     const ShortRow g = short_row<DT, MODE == kMFast>(a.x, a.y, rr, (int)a.cols);
-    const char *mrow = HAS_MASK ? a.mask + (rr % a.mask_rows) * a.cols * S : nullptr;
+    const char *mrow = HAS_MASK ? a.mask + mask_row_of(a, rr) * a.cols * S : nullptr;
     const bool m_vec = HAS_MASK && ((reinterpret_cast<uintptr_t>(mrow) - reinterpret_cast<uintptr_t>(g.xr)) & 15) == 0;
     // row-local indices fit 32 bits: these kernels serve rows of at most 64 KiB
     const int lim = valid ? (int)visible_limit(a, rr) : 0;
@@ -624,10 +645,34 @@ __global__ void __launch_bounds__(kRowgroupThreads) k_masked_lean(const LeanArgs
 
 namespace {
 
+// The multiply-high constants of the round-up method for a divisor 1 <= d <
+// 2^31 (shift = ceil(log2 d), magic = floor(2^32 (2^shift - d) / d) + 1; d = 1:
+// magic 1, shift 0, which gives r).
+void magic_u31(int64_t d, uint32_t &magic, uint32_t &shift)
+{
+    magic = 1u;
+    shift = 0u;
+    if (d <= 1)
+        return;
+    const uint64_t q = (uint64_t)d;
+    uint32_t lg = 0;
+    while ((1ull << lg) < q)
+        lg++;
+    shift = lg;
+    magic = (uint32_t)((((1ull << lg) - q) << 32) / q + 1);
+}
+
 MaskedArgs args_of(const MaskedLaunch &l)
 {
-    return MaskedArgs{(const char *)l.x, (char *)l.y, l.rows, l.cols, l.plan.y_vector, l.scale,
-                      (const char *)l.mask, l.mask_rows, l.causal_q};
+    MaskedArgs a{(const char *)l.x, (char *)l.y, l.rows, l.cols, l.plan.y_vector, l.scale,
+                 (const char *)l.mask, l.mask_rows, l.causal_q, 0, 1u, 0u, 1u, 0u};
+    a.div32 = l.rows <= INT32_MAX && l.causal_q <= INT32_MAX && (l.mask == nullptr || l.mask_rows <= INT32_MAX);
+    if (a.div32) {
+        magic_u31(l.causal_q, a.q_magic, a.q_shift);
+        if (l.mask)
+            magic_u31(l.mask_rows, a.m_magic, a.m_shift);
+    }
+    return a;
 }
 
 int mode_of(const MaskedLaunch &l)
@@ -753,14 +798,7 @@ bool lean_fits(const MaskedLaunch &l)
 LeanArgs lean_args_of(const MaskedLaunch &l)
 {
     LeanArgs a{(const char *)l.x, (char *)l.y, (uint32_t)l.rows, (int)l.cols, l.scale, (int)l.causal_q, 1u, 0u};
-    if (l.causal_q > 1) {
-        const uint64_t q = (uint64_t)l.causal_q;
-        uint32_t lg = 0;
-        while ((1ull << lg) < q)
-            lg++;  // ceil(log2 q)
-        a.q_shift = lg;
-        a.q_magic = (uint32_t)((((1ull << lg) - q) << 32) / q + 1);
-    }
+    magic_u31(l.causal_q, a.q_magic, a.q_shift);
     return a;
 }
 
