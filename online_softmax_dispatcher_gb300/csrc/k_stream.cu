@@ -14,10 +14,16 @@
 //
 // Where the rows in flight outgrow L2, the re-read of a row misses if every
 // pass walks it forward: each chunk is read again a whole pass after its first
-// read.  The plan then asks (back_passes = 1) for each pass after the first to walk
-// the row from the other end, so that it starts on the chunks read last, still
-// in L2, and only the chunks read longest ago come from HBM again (16-bit:
-// forward, then backward; fp32: forward, backward, forward).
+// read.  The plan then asks (back_passes = 1) for each pass after the first
+// to walk the row from the other end, so that it starts on the chunks read
+// last, still in L2, and only the chunks read longest ago come from HBM again
+// (16-bit: forward, then backward; fp32: forward, backward, forward).  Those
+// launches also mark the lines of every pass but the last evict-last in L2
+// and the last pass's evict-first (rows on the 16-byte grid), which keeps
+// still more of a row for its re-read (measured: [4096, 131072] bf16 409.0 ->
+// 370.5 us, [2048, 131072] bf16 206.3 -> 191.6, [2048, 262144] fp16 441.4 ->
+// 415.6; fp32 within 1.5 %); forward launches keep plain loads (with the
+// policies, [4096, 65600] fp16 was 4 % slower).
 //
 #include "common.cuh"
 #include "launch.h"
@@ -35,7 +41,7 @@ __device__ __forceinline__ typename Math<DT>::Acc sum_backward(const RowGeom &g,
     const int64_t span = (int64_t)blockDim.x * kStep;
     typename M::Acc acc = M::zero();
     for (int64_t lo = g.nch > 0 ? (g.nch - 1) / span * span : -1; lo >= 0; lo -= span)
-        acc = M::merge(acc, pass_sum<DT, ALIGNED>(g, lo, lo + span < g.nch ? lo + span : g.nch, cols, m));
+        acc = M::merge(acc, pass_sum<DT, ALIGNED, kStep, 1>(g, lo, lo + span < g.nch ? lo + span : g.nch, cols, m));
     return acc;
 }
 
@@ -44,7 +50,7 @@ __device__ __forceinline__ void write_backward(const RowGeom &g, int64_t cols, f
 {
     const int64_t span = (int64_t)blockDim.x * kStep;
     for (int64_t lo = g.nch > 0 ? (g.nch - 1) / span * span : -1; lo >= 0; lo -= span)
-        pass_write<DT, ALIGNED>(g, lo, lo + span < g.nch ? lo + span : g.nch, cols, m, inv, y_vec);
+        pass_write<DT, ALIGNED, kStep, 2>(g, lo, lo + span < g.nch ? lo + span : g.nch, cols, m, inv, y_vec);
 }
 
 // BACK: the passes after the first alternate direction (see above).
@@ -59,17 +65,20 @@ __global__ void __launch_bounds__(kStreamThreads)
     __shared__ MD smd[32];
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const RowGeom g = row_geom<DT, ALIGNED>(x, y, r, cols);
+        // L2 policies of the passes' loads (with the backward walk only):
+        // evict-last, then evict-first for the last pass
+        constexpr int KEEP = BACK ? 1 : 0, LAST = BACK ? 2 : 0;
         if constexpr (DT == kF32) {
-            const float m = block_max(pass_max<DT, ALIGNED>(g, 0, g.nch, cols), smax);
+            const float m = block_max(pass_max<DT, ALIGNED, kStep, KEEP>(g, 0, g.nch, cols), smax);
             typename M::Acc acc;
             if constexpr (BACK)
                 acc = sum_backward<DT, ALIGNED>(g, cols, m);
             else
                 acc = pass_sum<DT, ALIGNED>(g, 0, g.nch, cols, m);
             const float inv = 1.0f / M::value(block_sum<DT>(acc, ssum));
-            pass_write<DT, ALIGNED>(g, 0, g.nch, cols, m, inv, y_vec != 0);
+            pass_write<DT, ALIGNED, kStep, LAST>(g, 0, g.nch, cols, m, inv, y_vec != 0);
         } else {
-            const MD md = block_md<DT>(pass_online<DT, ALIGNED>(g, 0, g.nch, cols), smd);
+            const MD md = block_md<DT>(pass_online<DT, ALIGNED, kStep, KEEP>(g, 0, g.nch, cols), smd);
             const float inv = 1.0f / md.d;
             if constexpr (BACK)
                 write_backward<DT, ALIGNED>(g, cols, md.m, inv, y_vec != 0);

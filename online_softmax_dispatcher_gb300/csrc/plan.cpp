@@ -361,14 +361,14 @@ bool splitk_possible(int64_t rows, const softmax_device_info &dev)
 // Many 16-bit rows on the 16-byte grid of more than 256 KiB and less than 2
 // MiB: the cluster split with one CTA per row, whose bulk copies keep 192 KB
 // in flight per SM and whose one row per SM in flight leaves more of a row in
-// L2 for its re-read, beat the streaming kernel (measured on GB300, us:
-// [3072, 196608] fp16 448 against 507; [2048, 262144] fp16 426 against 458,
-// bf16 428 against 458; [1024, 262144] fp16 222 against 237; [2048, 393216]
-// bf16 683 against 702; [1024, 524288] fp16 465 against 481; level at 256
-// KiB, [4096, 131072] bf16 438 against 436, and at 2 MiB, [512, 1048576] fp16
-// 488 against 484).  fp32 rows and shorter rows stay with the streaming
-// kernel ([1024, 262144] fp32 714 against 622 - 657, [4096, 65600] fp16 278
-// against 185).
+// L2 for its re-read, beats the streaming kernel (both with their L2 policies;
+// measured on GB300, us: [2048, 262144] fp16 404.5 against 416.5, [2048,
+// 393216] bf16 613.6 against 647.8, [1024, 524288] fp16 447.0 against 460.8;
+// level at 384 KiB, [3072, 196608] fp16 448.7 against 449.7).  At 256 KiB and
+// at 2 MiB the streaming kernel is as fast or faster ([4096, 131072] bf16
+// 370.7 against 437.9; [512, 1048576] fp16 474.2 against 482.3), and fp32
+// rows and shorter rows stay with it ([1024, 262144] fp32 714 against 622 -
+// 657 before the policies, [4096, 65600] fp16 278 against 185).
 bool splitk_long_rows(const Geometry &g, int64_t rows, const softmax_device_info &dev)
 {
     return g.S == 2 && g.aligned && rows >= dev.sm_count && rows <= 65535 && splitk_possible(rows, dev) &&

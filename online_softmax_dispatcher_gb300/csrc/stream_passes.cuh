@@ -11,7 +11,31 @@
 namespace osd {
 constexpr int kStep = kStreamUnroll;  // chunks per thread per step
 
-template <int DT, bool ALIGNED, int STEP>
+// L2 policy of a pass's loads on rows on the 16-byte grid: 0 none, 1
+// evict-last (the row is read again later in the launch), 2 evict-first (its
+// last read).  Taken by the streaming kernel when the rows in flight outgrow
+// L2 (its backward walk), where it keeps more of each row there for the
+// re-read; where the rows fit L2 the plain loads measured faster.
+template <int POL>
+__device__ __forceinline__ uint4 ld_chunk_pol(const void *p)
+{
+    if constexpr (POL == 0) {
+        return ld_chunk(p);
+    } else {
+        uint64_t pol;
+        if constexpr (POL == 1)
+            asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+        else
+            asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+        uint4 v;
+        asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(p), "l"(pol));
+        return v;
+    }
+}
+
+template <int DT, bool ALIGNED, int STEP, int POL = 0>
 __device__ __forceinline__ void load_step(const RowGeom &g, int64_t k0, int64_t ke, int64_t cols,
                                           uint4 (&raw)[STEP])
 {
@@ -19,12 +43,15 @@ __device__ __forceinline__ void load_step(const RowGeom &g, int64_t k0, int64_t 
 #pragma unroll
     for (int u = 0; u < STEP; u++) {
         const int64_t k = k0 + u * T;
-        raw[u] = k < ke ? load_chunk<DT, ALIGNED>(g, k, cols) : neg_inf_chunk<DT>();
+        if constexpr (ALIGNED && POL != 0)
+            raw[u] = k < ke ? ld_chunk_pol<POL>(g.x0 + 16 * k) : neg_inf_chunk<DT>();
+        else
+            raw[u] = k < ke ? load_chunk<DT, ALIGNED>(g, k, cols) : neg_inf_chunk<DT>();
     }
 }
 
 // online (m, d) over chunks [kb, ke) of a row, this thread's share.
-template <int DT, bool ALIGNED, int STEP = kStep>
+template <int DT, bool ALIGNED, int STEP = kStep, int POL = 0>
 __device__ MD pass_online(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols)
 {
     using M = Math<DT>;
@@ -33,7 +60,7 @@ __device__ MD pass_online(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols
     const int64_t T = blockDim.x;
     for (int64_t k0 = kb + threadIdx.x; k0 < ke; k0 += T * STEP) {
         uint4 raw[STEP];
-        load_step<DT, ALIGNED, STEP>(g, k0, ke, cols, raw);
+        load_step<DT, ALIGNED, STEP, POL>(g, k0, ke, cols, raw);
         float mt = -INFINITY;
 #pragma unroll
         for (int u = 0; u < STEP; u++)
@@ -62,14 +89,14 @@ __device__ MD pass_online(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols
     return md;
 }
 
-template <int DT, bool ALIGNED, int STEP = kStep>
+template <int DT, bool ALIGNED, int STEP = kStep, int POL = 0>
 __device__ float pass_max(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols)
 {
     float m = -INFINITY;
     const int64_t T = blockDim.x;
     for (int64_t k0 = kb + threadIdx.x; k0 < ke; k0 += T * STEP) {
         uint4 raw[STEP];
-        load_step<DT, ALIGNED, STEP>(g, k0, ke, cols, raw);
+        load_step<DT, ALIGNED, STEP, POL>(g, k0, ke, cols, raw);
 #pragma unroll
         for (int u = 0; u < STEP; u++)
             m = fmaxf(m, chunk_max<DT>(raw[u]));
@@ -77,7 +104,7 @@ __device__ float pass_max(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols
     return m;
 }
 
-template <int DT, bool ALIGNED, int STEP = kStep>
+template <int DT, bool ALIGNED, int STEP = kStep, int POL = 0>
 __device__ typename Math<DT>::Acc pass_sum(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols, float m)
 {
     using M = Math<DT>;
@@ -86,7 +113,7 @@ __device__ typename Math<DT>::Acc pass_sum(const RowGeom &g, int64_t kb, int64_t
     const int64_t T = blockDim.x;
     for (int64_t k0 = kb + threadIdx.x; k0 < ke; k0 += T * STEP) {
         uint4 raw[STEP];
-        load_step<DT, ALIGNED, STEP>(g, k0, ke, cols, raw);
+        load_step<DT, ALIGNED, STEP, POL>(g, k0, ke, cols, raw);
 #pragma unroll
         for (int u = 0; u < STEP; u++) {
             float f[E];
@@ -99,7 +126,7 @@ __device__ typename Math<DT>::Acc pass_sum(const RowGeom &g, int64_t kb, int64_t
     return acc;
 }
 
-template <int DT, bool ALIGNED, int STEP = kStep>
+template <int DT, bool ALIGNED, int STEP = kStep, int POL = 0>
 __device__ void pass_write(const RowGeom &g, int64_t kb, int64_t ke, int64_t cols, float m, float inv,
                            bool y_vec)
 {
@@ -108,7 +135,7 @@ __device__ void pass_write(const RowGeom &g, int64_t kb, int64_t ke, int64_t col
     const int64_t T = blockDim.x;
     for (int64_t k0 = kb + threadIdx.x; k0 < ke; k0 += T * STEP) {
         uint4 raw[STEP];
-        load_step<DT, ALIGNED, STEP>(g, k0, ke, cols, raw);
+        load_step<DT, ALIGNED, STEP, POL>(g, k0, ke, cols, raw);
 #pragma unroll
         for (int u = 0; u < STEP; u++) {
             const int64_t k = k0 + u * T;
