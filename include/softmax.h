@@ -343,7 +343,9 @@ typedef struct {
     int back_passes;        /* STREAM: 1 if each pass over a row after the first walks it
                                from the other end, so that a re-read starts on the chunks
                                read last, still in L2 (the dispatcher sets it when the rows
-                               in flight outgrow half of L2); 0 if every pass walks forward;
+                               in flight hold more than 5/12 of L2; the loads then also
+                               carry L2 evict-last / evict-first policies); 0 if every pass
+                               walks forward;
                                0 for the other variants.  It changes no 16-bit output bit
                                (fp32: the order of the sum) */
 } softmax_launch_plan;

@@ -194,13 +194,17 @@ bool tma_fits(const Geometry &g, const softmax_device_info &dev)
 }
 
 // STREAM: one CTA per row.  back_passes = 1 (the passes after the first walk each
-// row from the other end) where the rows in flight hold more than half of L2,
+// row from the other end, their loads with L2 policies) where the rows in
+// flight hold more than 5/12 of L2 (55 MB of GB300's; measured between the
+// forward walk's last win, 50 MB, and the backward walk's first, 60 MB),
 // so that a re-read starts on the chunks read last; the rows in flight are the
 // resident CTAs, 2 per SM for rows on the 16-byte grid (those instances fit 64
 // registers at 512 threads) and 1 otherwise.  Measured on GB300 (rows in
-// flight x row bytes): [4096, 65600] fp16 (40 MB) 184 us forward against 194
-// us backward; [2048, 131072] bf16 (80 MB) 225 against 208; [2048, 262144]
-// fp16 (159 MB) 461 against 442; [1024, 262144] fp32 (318 MB) 641 against 622.
+// flight x row bytes; forward against backward with the policies, us):
+// [4096, 65600] fp16 (40 MB) 181.5 against 190.1; [8192, 81920] fp16 (50 MB)
+// 451.7 against 456.3; [6144, 98304] fp16 (60 MB) 461.3 against 389.0;
+// [2048, 65536] fp32 (80 MB) 312.6 against 274.4; [4096, 131072] bf16 (80 MB)
+// 409.0 against 370.5.
 void plan_stream(const Geometry &g, int64_t rows, const softmax_device_info &dev, softmax_launch_plan &p)
 {
     p.variant = SOFTMAX_VARIANT_STREAM;
@@ -209,7 +213,7 @@ void plan_stream(const Geometry &g, int64_t rows, const softmax_device_info &dev
     p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
     const int64_t resident = int64_t(dev.sm_count > 0 ? dev.sm_count : 1) * (g.aligned ? 2 : 1);
     const int64_t in_flight = rows < resident ? rows : resident;
-    p.back_passes = dev.l2_bytes > 0 && in_flight * g.row_bytes > int64_t(dev.l2_bytes) / 2 ? 1 : 0;
+    p.back_passes = dev.l2_bytes > 0 && in_flight * g.row_bytes * 12 > int64_t(dev.l2_bytes) * 5 ? 1 : 0;
 }
 
 // Cluster size (power of two, <= 16): about two CTAs per SM over all rows,
@@ -781,7 +785,8 @@ int plan_bwd(const softmax_device_info &dev, const void *y, const void *dy, cons
         p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
         // the write pass walks each row from its end (back_passes = 1) where the
         // rows in flight (2 CTAs per SM on the 16-byte grid, else 1) hold
-        // more than half of L2 in y and dy, as the forward streaming kernel
+        // more than half of L2 in y and dy (the forward streaming kernel's own
+        // line, 5/12, was measured on its shapes; this one on the backward's)
         const int64_t resident = int64_t(dev.sm_count > 0 ? dev.sm_count : 1) * (aligned ? 2 : 1);
         const int64_t in_flight = rows < resident ? rows : resident;
         p.back_passes = dev.l2_bytes > 0 && in_flight * 2 * g.row_bytes > int64_t(dev.l2_bytes) / 2 ? 1 : 0;
