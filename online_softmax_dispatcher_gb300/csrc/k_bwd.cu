@@ -326,9 +326,48 @@ __global__ void __launch_bounds__(512, V >= 8 ? 1 : 2) k_bwd_block(const BwdArgs
     }
 }
 
+// A 16-byte load of y or dy with an L2 policy: 1 evict-last (read again in
+// this launch), 2 evict-first (its last read).
+template <int POL>
+__device__ __forceinline__ uint4 ld_chunk_l2(const void *p)
+{
+    uint64_t pol;
+    if constexpr (POL == 1)
+        asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
+// Chunk k of y and of dy for a pass with L2 policy POL (0: plain loads; the
+// policies apply to rows on the 16-byte grid).
+template <int DT, bool ALIGNED, int POL>
+__device__ __forceinline__ void load_y_dy(const RowGeom &g, const char *dyrow, bool dy_vec, int64_t k, int64_t cols,
+                                          uint4 &yc, uint4 &dc)
+{
+    if constexpr (ALIGNED && POL != 0) {
+        if (k < g.nch) {
+            yc = ld_chunk_l2<POL>(g.x0 + 16 * k);
+            dc = ld_chunk_l2<POL>(dyrow + 16 * k);
+        } else {
+            yc = neg_inf_chunk<DT>();
+            dc = make_uint4(0, 0, 0, 0);
+        }
+    } else {
+        yc = load_chunk<DT, ALIGNED>(g, k, cols);
+        dc = load_other<DT, ALIGNED>(g, dyrow, dy_vec, k, cols);
+    }
+}
+
 // BACK: the write pass walks the row from its end, step by step, so that it
 // starts on the y and dy chunks the sum pass read last (still in L2 when the
-// rows in flight outgrow it); it changes no output bit.
+// rows in flight outgrow it), and (rows on the 16-byte grid) the sum pass's
+// loads mark their lines evict-last in L2, the write pass's evict-first; it
+// changes no output bit.
 template <int DT, bool ALIGNED, bool BACK>
 __global__ void __launch_bounds__(kStreamThreads) k_bwd_stream(const BwdArgs a)
 {
@@ -343,11 +382,8 @@ __global__ void __launch_bounds__(kStreamThreads) k_bwd_stream(const BwdArgs a)
         for (int64_t k0 = threadIdx.x; k0 < g.nch; k0 += T * U) {
             uint4 yc[U], dc[U];
 #pragma unroll
-            for (int u = 0; u < U; u++) {
-                const int64_t k = k0 + u * T;
-                yc[u] = load_chunk<DT, ALIGNED>(g, k, a.cols);
-                dc[u] = load_other<DT, ALIGNED>(g, a.dy + off, a.dy_vec != 0, k, a.cols);
-            }
+            for (int u = 0; u < U; u++)
+                load_y_dy<DT, ALIGNED, BACK ? 1 : 0>(g, a.dy + off, a.dy_vec != 0, k0 + u * T, a.cols, yc[u], dc[u]);
 #pragma unroll
             for (int u = 0; u < U; u++)
                 dot_chunk<DT, ALIGNED>(yc[u], dc[u], g, k0 + u * T, a.cols, acc);
@@ -361,11 +397,8 @@ __global__ void __launch_bounds__(kStreamThreads) k_bwd_stream(const BwdArgs a)
             const int64_t k0 = threadIdx.x + (BACK ? nst - 1 - st : st) * span;
             uint4 yc[U], dc[U];
 #pragma unroll
-            for (int u = 0; u < U; u++) {
-                const int64_t k = k0 + u * T;
-                yc[u] = load_chunk<DT, ALIGNED>(g, k, a.cols);
-                dc[u] = load_other<DT, ALIGNED>(g, a.dy + off, a.dy_vec != 0, k, a.cols);
-            }
+            for (int u = 0; u < U; u++)
+                load_y_dy<DT, ALIGNED, BACK ? 2 : 0>(g, a.dy + off, a.dy_vec != 0, k0 + u * T, a.cols, yc[u], dc[u]);
 #pragma unroll
             for (int u = 0; u < U; u++) {
                 const int64_t k = k0 + u * T;
