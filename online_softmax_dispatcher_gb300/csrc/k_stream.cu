@@ -53,9 +53,14 @@ __device__ __forceinline__ void write_backward(const RowGeom &g, int64_t cols, f
         pass_write<DT, ALIGNED, kStep, 2>(g, lo, lo + span < g.nch ? lo + span : g.nch, cols, m, inv, y_vec);
 }
 
-// BACK: the passes after the first alternate direction (see above).
+// BACK: the passes after the first alternate direction (see above).  Two
+// CTAs per SM for every instance: rows off the 16-byte grid (98 - 116
+// registers unbounded, one CTA per SM) then spill 8 - 24 bytes but keep twice
+// the loads in flight (measured: [4096, 65599] fp16 330.8 -> 261.0 us,
+// [2048, 131071] fp16 288.7 -> 254.3, [1024, 262143] fp32 801.1 -> 714.6,
+// [512, 1048575] fp16 594.4 -> 546.7).
 template <int DT, bool ALIGNED, bool BACK>
-__global__ void __launch_bounds__(kStreamThreads)
+__global__ void __launch_bounds__(kStreamThreads, 2)
     k_stream(const char *__restrict__ x, char *__restrict__ y, int64_t rows, int64_t cols, int y_vec)
 {
     pdl_enter();

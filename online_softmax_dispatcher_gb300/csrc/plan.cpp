@@ -198,8 +198,7 @@ bool tma_fits(const Geometry &g, const softmax_device_info &dev)
 // flight hold more than 5/12 of L2 (55 MB of GB300's; measured between the
 // forward walk's last win, 50 MB, and the backward walk's first, 60 MB),
 // so that a re-read starts on the chunks read last; the rows in flight are the
-// resident CTAs, 2 per SM for rows on the 16-byte grid (those instances fit 64
-// registers at 512 threads) and 1 otherwise.  Measured on GB300 (rows in
+// resident CTAs, 2 per SM (every instance fits 64 registers at 512 threads).  Measured on GB300 (rows in
 // flight x row bytes; forward against backward with the policies, us):
 // [4096, 65600] fp16 (40 MB) 181.5 against 190.1; [8192, 81920] fp16 (50 MB)
 // 451.7 against 456.3; [6144, 98304] fp16 (60 MB) 461.3 against 389.0;
@@ -211,7 +210,7 @@ void plan_stream(const Geometry &g, int64_t rows, const softmax_device_info &dev
     p.chunks_per_thread = kStreamUnroll;
     p.block_threads = kStreamThreads;
     p.grid_x = rows < INT32_MAX ? rows : INT32_MAX;
-    const int64_t resident = int64_t(dev.sm_count > 0 ? dev.sm_count : 1) * (g.aligned ? 2 : 1);
+    const int64_t resident = int64_t(dev.sm_count > 0 ? dev.sm_count : 1) * 2;
     const int64_t in_flight = rows < resident ? rows : resident;
     p.back_passes = dev.l2_bytes > 0 && in_flight * g.row_bytes * 12 > int64_t(dev.l2_bytes) * 5 ? 1 : 0;
 }

@@ -361,8 +361,7 @@ def test_long_block_rows_dispatch(lib):
 
 def test_stream_walk_direction(lib):
     # back_passes = 1 (re-read passes walk each row from the other end) once the
-    # rows in flight (2 CTAs per SM on the 16-byte grid, else 1) hold more
-    # than 5/12 of L2
+    # rows in flight (2 CTAs per SM) hold more than 5/12 of L2
     line = GB300.l2_bytes * 5 / 12
     for rows, cols, dt, x_off, want in (
             (4096, 65600, 1, 0, 0),      # 304 rows x 131 KB = 40 MB
@@ -370,7 +369,8 @@ def test_stream_walk_direction(lib):
             (2048, 262144, 1, 0, 1),
             (1024, 262144, 0, 0, 1),
             (8, 1 << 20, 1, 0, 0),       # few rows: 8 x 2 MB
-            (2048, 131071, 1, 1, 0),     # off the grid: 152 rows x 262 KB = 40 MB
+            (2048, 131071, 1, 1, 1),     # off the grid: 304 rows x 262 KB = 80 MB
+            (4096, 65599, 1, 1, 0),      # off the grid: 40 MB
             (2048, 262143, 1, 1, 1),     # off the grid: 80 MB
             (6144, 98304, 1, 0, 1),      # 60 MB
             (8192, 81920, 1, 0, 0)):     # 50 MB
@@ -378,8 +378,7 @@ def test_stream_walk_direction(lib):
         rc, p = B.softmax_plan(GB300, BASE + x_off * e, BASE + (1 << 36) + x_off * e, rows, cols, dt,
                                B.VARIANT_STREAM)
         assert rc == B.OK and p.variant == B.VARIANT_STREAM, (rows, cols)
-        resident = 152 * (2 if p.aligned else 1)
-        assert (min(rows, resident) * cols * e > line) == bool(want)
+        assert (min(rows, 304) * cols * e > line) == bool(want)
         assert p.back_passes == want and p.stages == 0, (rows, cols, dt, p.back_passes)
     # a device that reports no L2 size: forward
     dev = B.DeviceInfo(**{**{f: getattr(GB300, f) for f, _ in GB300._fields_}, "l2_bytes": 0})
