@@ -230,9 +230,21 @@ def recorded_traffic(workload: str, variant: str, plan: dict) -> tuple[float | N
 # ----------------------------------------------------------------------------- CPU oracle timing
 
 
-def oracle_pass(w, op: str, rows: int):
+def alibi_mask(causal_q: int, cols: int):
+    """The --mask bias as float64: -0.05 x |query position - key| for the
+    causal_q queries of a block (query i sits at key cols - causal_q + i)."""
+    import numpy as np
+
+    qi = np.arange(causal_q, dtype=np.float64)[:, None] + (cols - causal_q)
+    kj = np.arange(cols, dtype=np.float64)[None, :]
+    return -0.05 * np.abs(qi - kj)
+
+
+def oracle_pass(w, op: str, rows: int, mask: bool = False):
     """(one oracle pass of `op` over the first `rows` rows of w, bytes it
-    stands for, oracle).  Inputs are prepared outside the pass."""
+    stands for, oracle).  Inputs are prepared outside the pass.  The bytes are
+    those the GPU line counts for the same op (masked: the visible part of x,
+    all of y, and the --mask bias once)."""
     import numpy as np
 
     import oracle
@@ -247,16 +259,23 @@ def oracle_pass(w, op: str, rows: int):
         dy = np.random.default_rng(0).standard_normal(y.shape)
         return (lambda: o.softmax_bwd_f64(y, dy)), nbytes // 2 * 3, o
     if op == "masked":
-        return (lambda: o.softmax_masked(x, dt, 0.125, None, min(512, w.rows))), nbytes, o
+        q = min(512, w.rows)
+        esz = nbytes // (2 * rows * w.cols)
+        nbytes = (masked_visible_elems(rows, w.cols, q) + rows * w.cols) * esz
+        m = None
+        if mask:
+            m = W._round_to(alibi_mask(q, w.cols), w.dtype)
+            nbytes += m.size * esz
+        return (lambda: o.softmax_masked(x, dt, 0.125, m, q)), nbytes, o
     if op == "norm":
         g, b = W.norm_params(w)
         return (lambda: o.norm_f64(w.kind, x, dt, g, b, w.eps)), nbytes, o
     return (lambda: o.softmax(x, dt)), nbytes, o
 
 
-def time_oracle(w, op: str, sample_rows: int, reps: int, budget_s: float) -> dict:
+def time_oracle(w, op: str, sample_rows: int, reps: int, budget_s: float, mask: bool = False) -> dict:
     """The oracle (fp64, OpenMP over rows) on the first sample_rows rows."""
-    one, nbytes, o = oracle_pass(w, op, sample_rows)
+    one, nbytes, o = oracle_pass(w, op, sample_rows, mask)
     one()  # warm
     times = []
     t_all = time.perf_counter()
@@ -296,17 +315,17 @@ def cpu_model() -> str:
     return "unknown"
 
 
-def cpu_baseline_leg(w, op: str) -> dict:
+def cpu_baseline_leg(w, op: str, mask: bool = False) -> dict:
     """The oracle on all host cores (the sample of oracle_sample_rows), then on
     one core over a smaller sample; both as GB/s of the same algorithmic bytes."""
     import oracle
 
-    res = time_oracle(w, op, oracle_sample_rows(w), reps=5, budget_s=20.0)
+    res = time_oracle(w, op, oracle_sample_rows(w), reps=5, budget_s=20.0, mask=mask)
     o = oracle.default()
     all_cores = o.num_threads()
     o.set_num_threads(1)
     try:
-        one = time_oracle(w, op, oracle_sample_rows(w, 1 << 22), reps=3, budget_s=15.0)
+        one = time_oracle(w, op, oracle_sample_rows(w, 1 << 22), reps=3, budget_s=15.0, mask=mask)
     finally:
         o.set_num_threads(all_cores)
     res["one_core"] = {"value": one["value"], "unit": "GB/s", "cores": 1, "sample": one["sample"],
@@ -442,9 +461,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         if args.mask:
             # an ALiBi-style additive bias, -0.05 x the query-key distance, one
             # row per query of the block (read by every block: counted once)
-            qi = torch.arange(causal_q, device=dev, dtype=torch.float64)[:, None] + (cols - causal_q)
-            kj = torch.arange(cols, device=dev, dtype=torch.float64)[None, :]
-            mask_t = (-0.05 * (qi - kj).abs()).to(xs[0].dtype).contiguous()
+            mask_t = W.as_torch(W._round_to(alibi_mask(causal_q, cols), w.dtype), w.dtype).to(dev).contiguous()
             mp, mrows = mask_t.data_ptr(), causal_q
             set_bytes += mask_t.numel() * mask_t.element_size()
         rc, plan = osd.softmax_masked_plan(osd.softmax_device_query()[1], ptrs[0][0], ptrs[0][1], rows, cols, dt)
@@ -626,7 +643,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         torch.cuda.empty_cache()
         res["per_config"] = run_per_config(args, ws)
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline_leg(w, args.op)
+        res["cpu_baseline"] = cpu_baseline_leg(w, args.op, args.op == "masked" and args.mask)
     return res if rank == 0 else None
 
 
@@ -714,7 +731,7 @@ def run_reference(args, rank: int, ws: int) -> dict | None:
 
     w = find_workload(W, args)
     rows = oracle_sample_rows(w, target_elems=1 << 23)
-    one, nbytes, o = oracle_pass(w, args.op, rows)
+    one, nbytes, o = oracle_pass(w, args.op, rows, args.op == "masked" and args.mask)
     for _ in range(max(0, min(args.warmup, 3))):
         one()
     t = time.perf_counter()
@@ -723,12 +740,15 @@ def run_reference(args, rank: int, ws: int) -> dict | None:
     dt_s = (time.perf_counter() - t) / max(1, args.steps)
     value = nbytes / dt_s / 1e9
     sample = f"each step: {args.op} on the first {rows} of {w.rows} rows of {w.name}"
+    config = {"workload": w.name, "rows": w.rows, "cols": w.cols, "about": w.about, "op": args.op,
+              "reference": "fp64 CPU oracle (OpenMP over rows) standing in for the pages' method"}
+    if args.op == "masked":
+        config["mask"] = "ALiBi-style [512, cols], -0.05 x distance" if args.mask else None
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt_s * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "about": w.about, "op": args.op,
-                   "reference": "fp64 CPU oracle (OpenMP over rows) standing in for the pages' method"},
+        "config": config,
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
